@@ -1,0 +1,350 @@
+#!/usr/bin/env python
+"""Decode benchmark: greedy KV-cached decode on the SmolLM2-135M shape at batch 1.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``
+
+One step = one ``slm_decode_step`` (every phase of the decode step for the batch) on
+synthetic random-init bf16 weights (~N(0, 0.02)) and a seeded random 5-token prompt;
+the next ids stay on the device and feed the following step.  Weights (269 MB) stream
+from HBM every step and exceed the 129 MB L2, so no flush is needed between steps.
+Prints one JSON line.  Under torchrun each rank runs an independent replica (the path
+has no exchange step), the timed region is bracketed by barriers and the slowest
+rank's time counts.  ``--impl reference`` times the CPU oracle on the host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "decode tokens/sec at batch 1 and 16; achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "tokens/s"
+WORKLOAD = "smol_b1"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "llama_decode_kv_gb300", "csrc", "decode_kernel.cu")
+PROFILE = os.path.join(ROOT, "profiles", "decode_step_kernel.smol_b1.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kv_bytes_read(shape, ctx: int) -> int:
+    """K and V bytes one row reads in one step at context length ctx (all layers)."""
+    esz = 2 if shape.kv_dtype == synth.DTYPE_BF16 else 4
+    return 2 * ctx * shape.head_dim * shape.n_kv_heads * esz * shape.n_layers
+
+
+def profile_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the source."""
+    try:
+        src = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+        fields = {}
+        for line in open(PROFILE):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != src:
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_baseline(shape, W, prompt, budget_s: float):
+    """The oracle, as it stands, on the host: greedy decode steps after the prompt."""
+    import oracle
+    m = oracle.Model(shape, W)
+    _, nid = m.prefill(0, prompt)
+    steps, pos = 0, len(prompt)
+    t0 = time.perf_counter()
+    while True:
+        _, ids = m.decode_step([0], [nid], [pos])
+        nid, pos, steps = int(ids[0]), pos + 1, steps + 1
+        if time.perf_counter() - t0 >= budget_s or pos >= shape.max_seq:
+            break
+    dt = time.perf_counter() - t0
+    m.close()
+    return {"value": steps / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} single-threaded oracle decode steps (contexts {len(prompt) + 1}.."
+                      f"{pos}) after a {len(prompt)}-token prompt, SmolLM2-135M shape, batch 1"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[WORKLOAD]
+    s = wl.shape
+    W = synth.make_weights(s)
+    prompt = synth.make_prompt(s, 0, wl.prompt_len)
+    import oracle
+    m = oracle.Model(s, W)
+    _, nid = m.prefill(0, prompt)
+    pos = len(prompt)
+    for _ in range(args.warmup):
+        _, ids = m.decode_step([0], [nid], [pos])
+        nid, pos = int(ids[0]), pos + 1
+    t0 = time.perf_counter()
+    steps = 0
+    cap_s = 150.0
+    while steps < args.steps and pos < s.max_seq:
+        _, ids = m.decode_step([0], [nid], [pos])
+        nid, pos, steps = int(ids[0]), pos + 1, steps + 1
+        if time.perf_counter() - t0 > cap_s:
+            break
+    dt = time.perf_counter() - t0
+    value = steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: SmolLM2-135M shape, batch 1, 5-token prompt, greedy "
+                               "decode", "batch": 1, "weights": "bf16", "kv": "f32"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} oracle decode steps after {args.warmup} warm-up steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import llama_decode_kv_gb300 as slm
+
+    torch.cuda.set_device(local)
+    wl = synth.WORKLOADS[WORKLOAD]
+    s = wl.shape
+    W = synth.make_weights(s)
+    prompt = synth.make_prompt(s, rank, wl.prompt_len)
+    eng = slm.Engine(s, W)
+    dev = torch.device("cuda", local)
+    toks = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(2)]
+    _, nid = eng.prefill_checked(0, prompt, want_logits=False)
+    toks[0].copy_(nid)
+    state = {"pos": len(prompt), "cur": 0, "ctx": []}
+
+    def step():
+        if state["pos"] >= s.max_seq:  # wrap: the sequence starts over (host-side reset)
+            eng.reset(0)
+            state["pos"] = 0
+        c = state["cur"]
+        rc = eng.decode_step([0], toks[c], [state["pos"]], None, toks[1 - c])
+        if rc != 0:
+            raise RuntimeError(f"slm_decode_step: {slm.STATUS.get(rc)} {eng.last_error()}")
+        state["ctx"].append(state["pos"] + 1)
+        state["pos"] += 1
+        state["cur"] = 1 - c
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    state["ctx"].clear()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    total_ms = ev[0].elapsed_time(ev[-1])
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    rc = eng.sync()
+    if rc != 0:
+        raise RuntimeError(f"device status after the timed region: {eng.last_error()}")
+    t_max = max_over_ranks(total_ms, world)
+    tokens = args.steps * wl.batch * world
+    value = tokens / (t_max / 1e3)
+
+    wbytes = synth.weight_bytes(s)
+    alg_bytes = sum(wbytes + kv_bytes_read(s, c) for c in state["ctx"])
+    per_launch_bytes = alg_bytes / args.steps
+    per_launch_s = total_ms / 1e3 / args.steps
+    achieved = per_launch_bytes / per_launch_s / 1e9
+    peak, peak_kind = peaks()
+    traffic = profile_traffic()
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    tok_h = np.array([int(toks[state["cur"]].item())], dtype=np.int32)
+    ids_h = np.empty(1, dtype=np.int32)
+    e2e_steps = args.steps
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        if state["pos"] >= s.max_seq:
+            eng.reset(0)
+            state["pos"] = 0
+        rc = eng.decode_step([0], tok_h, [state["pos"]], None, ids_h)
+        if rc != 0:
+            raise RuntimeError(f"slm_decode_step (host buffers): {eng.last_error()}")
+        tok_h[0] = ids_h[0]
+        state["pos"] += 1
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = e2e_steps * wl.batch * world / e2e_s
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (random-init bf16 weights ~N(0,0.02), seeded random prompt)",
+        "config": {
+            "workload": f"{WORKLOAD}: SmolLM2-135M shape (dim 576, 30 layers, 9/3 heads, "
+                        "hidden 1536, vocab 49152), batch 1, 5-token prompt, greedy decode",
+            "batch": wl.batch, "weights": "bf16", "kv": "f32", "accumulate": "f32",
+            "contexts": [min(state["ctx"]), max(state["ctx"])] if state["ctx"] else None,
+            "l2": "inputs larger than L2: 269 MB of weights stream from HBM every step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "latency_us": {"median": statistics.median(per) * 1e3,
+                       "p10": float(np.percentile(per, 10)) * 1e3,
+                       "p90": float(np.percentile(per, 90)) * 1e3},
+        "bytes_per_step": per_launch_bytes,
+        "hbm_gbs": achieved,
+        "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "decode_step_kernel", "peak_kind": peak_kind},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * wl.batch,
+                "d2h_bytes_per_step": 4 * wl.batch},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(s, W, prompt, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

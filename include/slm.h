@@ -1,0 +1,180 @@
+/*
+ * slm.h -- C ABI of the GB300 (sm_103a) KV-cached greedy decode library for
+ * LLaMA-style decoders.
+ *
+ * What one decode step computes (kasahare 0.4.0 / simple-llm, "Architecture"), for
+ * every batch row, at the row's position pos:
+ *     x = E[token]                                   (tied embedding, bf16 widened)
+ *     per block:  xn = rmsnorm(x, attn_norm)
+ *                 q, k, v = Wq xn, Wk xn, Wv xn       (no biases)
+ *                 q, k = RoPE(q, k, pos)              (pairs (i, i + head_dim/2))
+ *                 append k, v to the cache at slot pos
+ *                 o = softmax(q K^T / sqrt(head_dim)) V over slots 0..pos (GQA)
+ *                 x = x + Wo o
+ *                 xn = rmsnorm(x, ffn_norm)
+ *                 x = x + W2( silu(W1 xn) * (W3 xn) )
+ *     logits = E rmsnorm(x, output_norm);  next id = argmax (lowest index on ties)
+ * The KV cache keeps each position's key and value rows and reuses them for every
+ * later token (GOTOken: An Inference Engine in QBasic, "About one token per second").
+ *
+ * Conventions for every entry point:
+ *   - Return 0 (SLM_OK) or a negative SLM_E* code; nothing aborts, nothing throws.
+ *     After a failure, slm_last_error() returns a one-line description.
+ *   - "device" pointers are CUDA device (or managed) memory of the current device;
+ *     "host" pointers are ordinary host memory.  Where a parameter says "host or
+ *     device", the library checks the pointer's kind itself.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Work is enqueued asynchronously on it unless the call says otherwise.
+ *   - A context is not thread-safe: calls on one context must not overlap.
+ *   - Every device-side wait in the library's kernels is bounded in time; a wait that
+ *     runs out sets the context's device status word, which slm_sync() reports as
+ *     SLM_ETIMEOUT.  No kernel traps.
+ */
+#ifndef SLM_H
+#define SLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+enum { SLM_F32 = 0, SLM_BF16 = 1 };
+
+/* status codes */
+enum {
+    SLM_OK = 0,
+    SLM_EINVAL = -1,      /* bad argument or config                                  */
+    SLM_ENOMEM = -2,      /* a device or pinned-host allocation failed                */
+    SLM_ECAPACITY = -3,   /* a position would reach max_seq                           */
+    SLM_EPOS = -4,        /* a position is not the sequence's current length          */
+    SLM_ESTATE = -5,      /* the sequence is in the wrong state (prefill of non-empty) */
+    SLM_ECUDA = -6,       /* a CUDA runtime call failed                               */
+    SLM_ETIMEOUT = -7,    /* a bounded device-side wait ran out                       */
+    SLM_EDEVICE = -8,     /* the device reported a numeric fault (NaN logits)         */
+    SLM_EUNSUPPORTED = -9 /* valid config outside what this build implements          */
+};
+
+/*
+ * Model shape and storage.  Field meanings follow the kasahare config blob and the
+ * nanochat model config: dim, n_layers, n_heads, n_kv_heads (< n_heads for GQA, = for
+ * MHA, 1 for MQA: kasahare "Architecture"), head_dim, hidden (SwiGLU width), vocab.
+ * max_seq is the per-sequence cache capacity (GOTOken keeps a fixed context constant;
+ * kasahare preallocates its KvSlots), max_batch the number of sequence slots.
+ * Embeddings are always tied (kasahare "Optimisations").  weight_dtype: SLM_F32 or
+ * SLM_BF16.  kv_dtype: the cache element type, SLM_F32 or SLM_BF16 (rounded to
+ * nearest-even on append).
+ * Requirements: all counts > 0, n_heads % n_kv_heads == 0, head_dim a multiple of 8
+ * and <= 256, max_batch <= 16, norm_eps >= 0, rope_theta > 0.  Shapes whose fp32
+ * activation tile (max_batch x input width) cannot fit in shared memory give
+ * SLM_EUNSUPPORTED.
+ */
+typedef struct {
+    int32_t dim, n_layers, n_heads, n_kv_heads, head_dim, hidden, vocab, max_seq, max_batch;
+    float rope_theta, norm_eps;
+    int32_t weight_dtype, kv_dtype;
+} slm_config;
+
+typedef struct slm_ctx slm_ctx;
+
+/*
+ * slm_create -- build a context on the current CUDA device.
+ *   weights: host or device buffer of exactly `nbytes` bytes holding every tensor, in
+ *     weight_dtype, in the kasahare ".sllm" order (kasahare, "On-disk model format"):
+ *     token_emb[vocab*dim]; per block attn_norm[dim], wq[n_heads*head_dim*dim],
+ *     wk[n_kv_heads*head_dim*dim], wv[n_kv_heads*head_dim*dim], wo[dim*n_heads*head_dim],
+ *     ffn_norm[dim], w1[hidden*dim] (gate), w3[hidden*dim] (up), w2[dim*hidden];
+ *     output_norm[dim].  Matrices are row-major [out][in] (GOTOken, "About one token
+ *     per second": W(d, n) row-major).
+ *   The library copies and repacks the weights into its own device layout, so the
+ *   caller may free `weights` when the call returns (the call is synchronous).  It
+ *   also allocates the KV cache for max_batch sequences of max_seq positions, all
+ *   empty.  *out receives the context (NULL on failure).
+ *   Errors: SLM_EINVAL (NULL pointer, bad config, nbytes mismatch), SLM_ENOMEM,
+ *   SLM_ECUDA, SLM_EUNSUPPORTED.
+ */
+int slm_create(const slm_config *config, const void *weights, size_t nbytes, slm_ctx **out);
+
+/*
+ * slm_prefill -- process the prompt of one empty sequence, positions 0..n-1, and
+ * produce the first generated token (the prompt is processed once; afterwards only
+ * new tokens are processed: GOTOken, "About one token per second").
+ *   seq: sequence slot in [0, max_batch); must be empty, else SLM_ESTATE (as
+ *     nanochat refuses to prefill a non-empty KV cache).
+ *   tokens: host or device int32[n], each in [0, vocab).  n in [1, max_seq].
+ *   last_logits: NULL, or host or device float[vocab] for the last position's logits.
+ *   next_id: host or device int32[1], the argmax of the last position's logits.
+ *   On success the sequence length becomes n.  Asynchronous on `stream` when every
+ *   pointer is device memory; synchronous otherwise.  Token ids are range-checked on
+ *   the host when they are host memory, on the device (status word) otherwise.
+ */
+int slm_prefill(slm_ctx *ctx, int32_t seq, const int32_t *tokens, int32_t n, float *last_logits,
+                int32_t *next_id, void *stream);
+
+/*
+ * slm_decode_step -- one batched greedy decode step (nanochat "Engine.generate":
+ * one token column for the whole batch per forward).
+ *   batch in [1, max_batch].
+ *   seq_ids: host int32[batch], distinct sequence slots.
+ *   tokens: host or device int32[batch], the token fed to each row.
+ *   positions: host int32[batch]; positions[i] must equal the current length of
+ *     seq_ids[i] (else SLM_EPOS) and be < max_seq (else SLM_ECAPACITY).
+ *   logits: NULL, or host or device float[batch][vocab].
+ *   next_ids: host or device int32[batch], argmax of each row's logits.
+ *   Row i appends its k, v at slot positions[i]; its length becomes positions[i] + 1.
+ *   Asynchronous on `stream` when tokens, logits and next_ids are device memory (the
+ *   ids can feed the next step without a device-to-host copy); synchronous otherwise.
+ */
+int slm_decode_step(slm_ctx *ctx, int32_t batch, const int32_t *seq_ids, const int32_t *tokens,
+                    const int32_t *positions, float *logits, int32_t *next_ids, void *stream);
+
+/*
+ * slm_reset -- forget a sequence's cached positions (seq = -1: every sequence), as
+ * nanochat's KVCache.reset sets its position back to 0.  No memory is freed and no
+ * device work is issued.
+ */
+int slm_reset(slm_ctx *ctx, int32_t seq);
+
+/* slm_seq_len -- current length of a sequence (>= 0), or a negative SLM_E* code. */
+int32_t slm_seq_len(const slm_ctx *ctx, int32_t seq);
+
+/*
+ * slm_sync -- wait for the work enqueued on `stream`, then read and clear the device
+ * status word: SLM_OK, SLM_ETIMEOUT (a bounded wait ran out), SLM_EDEVICE (NaN logits
+ * or a token id out of range), or SLM_ECUDA.
+ */
+int slm_sync(slm_ctx *ctx, void *stream);
+
+/* slm_destroy -- free everything the context owns.  NULL is ignored. */
+void slm_destroy(slm_ctx *ctx);
+
+/* slm_last_error -- text of the context's last failure ("" if none). */
+const char *slm_last_error(const slm_ctx *ctx);
+
+/* slm_status_string -- static text for a status code. */
+const char *slm_status_string(int status);
+
+/*
+ * slm_debug_copy_kv -- test hook: copy the cached keys and values of positions
+ * [0, n_pos) of one (layer, sequence) to host memory as fp32 [n_kv_heads][n_pos]
+ * [head_dim] each, widening bf16 caches exactly.  n_pos = -1 means the sequence's
+ * current length; n_pos may reach max_seq, so a test can also inspect slots that no
+ * step has written.  Either output may be NULL.  Synchronous (device-wide).  Returns
+ * the number of positions copied, or a negative SLM_E* code.
+ */
+int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, float *k_host,
+                      float *v_host);
+
+/*
+ * slm_debug_fill_kv -- test hook: fill the whole KV cache (every layer, slot and
+ * position) with the fp32 value `value` (rounded to the cache type), so that a test
+ * can check that a step writes exactly the slots it should.  Synchronous.
+ */
+int slm_debug_fill_kv(slm_ctx *ctx, float value);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,190 @@
+"""Thin Python binding of the GB300 decode library (``libslm.so``, C ABI in
+``include/slm.h``).
+
+Argument marshalling only: every step of the decode path runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  Importing this package without
+the built library raises ``ImportError``: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libslm.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "slm.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m llama_decode_kv_gb300.build` "
+        "(CUDA toolkit required); there is no CPU fallback")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+SLM_F32, SLM_BF16 = 0, 1
+STATUS = {0: "SLM_OK", -1: "SLM_EINVAL", -2: "SLM_ENOMEM", -3: "SLM_ECAPACITY", -4: "SLM_EPOS",
+          -5: "SLM_ESTATE", -6: "SLM_ECUDA", -7: "SLM_ETIMEOUT", -8: "SLM_EDEVICE",
+          -9: "SLM_EUNSUPPORTED"}
+for _code, _name in STATUS.items():
+    globals()[_name] = _code
+
+
+class slm_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("dim", "n_layers", "n_heads", "n_kv_heads", "head_dim", "hidden", "vocab",
+                 "max_seq", "max_batch")] + \
+               [("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("weight_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SIGS = {
+    "slm_create": (ctypes.c_int, [ctypes.POINTER(slm_config), _P, ctypes.c_size_t, ctypes.POINTER(_P)]),
+    "slm_prefill": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _P, _P]),
+    "slm_decode_step": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P]),
+    "slm_reset": (ctypes.c_int, [_P, _I32]),
+    "slm_seq_len": (_I32, [_P, _I32]),
+    "slm_sync": (ctypes.c_int, [_P, _P]),
+    "slm_destroy": (None, [_P]),
+    "slm_last_error": (ctypes.c_char_p, [_P]),
+    "slm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "slm_debug_copy_kv": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
+    "slm_debug_fill_kv": (ctypes.c_int, [_P, ctypes.c_float]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+    globals()[_name] = _fn
+
+
+def header_symbols(path: str = HEADER) -> list:
+    """Every entry point the public header declares."""
+    text = open(path).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(slm_\w+)\s*\(", text, re.M)))
+
+
+class SlmError(RuntimeError):
+    def __init__(self, code: int, what: str, detail: str = ""):
+        super().__init__(f"{what}: {STATUS.get(code, code)} {detail}".strip())
+        self.code = code
+
+
+def config_from_shape(shape) -> slm_config:
+    return slm_config(shape.dim, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                      shape.hidden, shape.vocab, shape.max_seq, shape.max_batch,
+                      float(shape.rope_theta), float(shape.norm_eps), int(shape.weight_dtype),
+                      int(shape.kv_dtype))
+
+
+def _ptr(x) -> Optional[int]:
+    """Address of a torch tensor or numpy array (None stays None)."""
+    if x is None:
+        return None
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+class Engine:
+    """One decode context: device weights, KV cache and per-sequence lengths."""
+
+    def __init__(self, shape, weights):
+        import torch  # device memory and streams
+        self.torch = torch
+        self.shape = shape
+        self.cfg = config_from_shape(shape)
+        buf = weights if not isinstance(weights, np.ndarray) else np.ascontiguousarray(weights)
+        nbytes = buf.nbytes if isinstance(buf, np.ndarray) else buf.numel() * buf.element_size()
+        h = ctypes.c_void_p()
+        rc = slm_create(ctypes.byref(self.cfg), _ptr(buf), nbytes, ctypes.byref(h))
+        if rc != 0:
+            raise SlmError(rc, "slm_create", slm_last_error(None).decode())
+        self.ctx = h
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            slm_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, rc: int, what: str):
+        if rc != 0:
+            raise SlmError(rc, what, slm_last_error(self.ctx).decode())
+
+    # ---------------------------------------------------------------- calls
+    def prefill(self, seq: int, tokens, last_logits=None, next_id=None, stream=None) -> int:
+        """tokens / last_logits / next_id: torch tensors (device or host) or numpy arrays."""
+        n = int(tokens.numel() if hasattr(tokens, "numel") else len(tokens))
+        return slm_prefill(self.ctx, seq, _ptr(tokens), n, _ptr(last_logits), _ptr(next_id),
+                           _stream_ptr(stream))
+
+    def decode_step(self, seq_ids: Sequence[int], tokens, positions: Sequence[int], logits=None,
+                    next_ids=None, stream=None) -> int:
+        b = len(seq_ids)
+        s = (ctypes.c_int32 * b)(*seq_ids)
+        p = (ctypes.c_int32 * b)(*positions)
+        return slm_decode_step(self.ctx, b, s, _ptr(tokens), p, _ptr(logits), _ptr(next_ids),
+                               _stream_ptr(stream))
+
+    def reset(self, seq: int = -1):
+        self._check(slm_reset(self.ctx, seq), "slm_reset")
+
+    def seq_len(self, seq: int) -> int:
+        return int(slm_seq_len(self.ctx, seq))
+
+    def sync(self, stream=None) -> int:
+        return slm_sync(self.ctx, _stream_ptr(stream))
+
+    def last_error(self) -> str:
+        return slm_last_error(self.ctx).decode()
+
+    def kv(self, layer: int, seq: int, n_pos: int = -1) -> Tuple[np.ndarray, np.ndarray]:
+        n = self.seq_len(seq) if n_pos < 0 else n_pos
+        s = self.shape
+        k = np.empty((s.n_kv_heads, n, s.head_dim), dtype=np.float32)
+        v = np.empty_like(k)
+        rc = slm_debug_copy_kv(self.ctx, layer, seq, n, k.ctypes.data, v.ctypes.data)
+        if rc < 0:
+            raise SlmError(rc, "slm_debug_copy_kv", self.last_error())
+        return k, v
+
+    def fill_kv(self, value: float):
+        self._check(slm_debug_fill_kv(self.ctx, float(value)), "slm_debug_fill_kv")
+
+    # ---------------------------------------------------------------- conveniences
+    def prefill_checked(self, seq: int, tokens, want_logits: bool = True):
+        """Prefill from device tensors; returns (logits or None, next id tensor)."""
+        torch = self.torch
+        dev = torch.device("cuda")
+        t = torch.as_tensor(np.asarray(tokens, dtype=np.int32)).to(dev)
+        lg = torch.empty(self.shape.vocab, dtype=torch.float32, device=dev) if want_logits else None
+        nid = torch.empty(1, dtype=torch.int32, device=dev)
+        self._check(self.prefill(seq, t, lg, nid), "slm_prefill")
+        return lg, nid
+
+    def decode_checked(self, seq_ids, tokens_dev, positions, want_logits: bool = True):
+        torch = self.torch
+        dev = torch.device("cuda")
+        b = len(seq_ids)
+        lg = torch.empty((b, self.shape.vocab), dtype=torch.float32, device=dev) if want_logits else None
+        ids = torch.empty(b, dtype=torch.int32, device=dev)
+        self._check(self.decode_step(seq_ids, tokens_dev, positions, lg, ids), "slm_decode_step")
+        return lg, ids

@@ -1,0 +1,633 @@
+// slm_api.cu -- host runtime behind the C ABI declared in include/slm.h.
+//
+// Owns the device copy of the weights (repacked into the K-tiled layout the decode
+// kernel streams), the preallocated KV cache (kasahare 0.4.0 / simple-llm,
+// "Optimisations": a pre-allocated KvSlot per head per layer), the per-step scratch,
+// and the host-side sequence lengths that validate every position before launch.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "slm_internal.h"
+
+namespace slm {
+cudaError_t launch_decode_step(const StepParams &P, size_t smem, cudaStream_t stream);
+cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm);
+size_t decode_smem_bytes(size_t xs_bytes);
+}  // namespace slm
+
+using namespace slm;
+
+struct slm_ctx {
+    slm_config cfg{};
+    int device = 0;
+    int grid = 0;
+    size_t smem = 0;
+    Model m{};
+    std::vector<void *> allocs;
+    std::vector<int> len;
+    unsigned long long bar_base = 0;
+    int n_barriers = 0;
+    int *d_tokens = nullptr;     // staging for host-provided tokens [max(max_seq, max_batch)]
+    float *d_logits = nullptr;   // staging for host-requested logits [max_batch][vocab]
+    int *d_ids = nullptr;        // staging for host-requested ids [max_batch]
+    int *h_ids = nullptr;        // pinned
+    std::string err;
+};
+
+static thread_local std::string g_create_err;
+
+static int fail(slm_ctx *c, int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (c)
+        c->err = buf;
+    else
+        g_create_err = buf;
+    return code;
+}
+
+#define CK(ctx, call)                                                                          \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess)                                                                 \
+            return fail((ctx), SLM_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));     \
+    } while (0)
+
+// Allocation failures can be injected for tests: SLM_FAULT_ALLOC_AFTER=n makes the
+// (n+1)-th device allocation of the process fail.
+static int g_alloc_calls = 0;
+
+static int dev_alloc(slm_ctx *c, void **p, size_t bytes) {
+    const char *inj = getenv("SLM_FAULT_ALLOC_AFTER");
+    if (inj && g_alloc_calls++ >= atoi(inj)) return fail(c, SLM_ENOMEM, "injected allocation failure");
+    cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return fail(c, e == cudaErrorMemoryAllocation ? SLM_ENOMEM : SLM_ECUDA,
+                    "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+    }
+    c->allocs.push_back(*p);
+    return SLM_OK;
+}
+
+static bool is_device_ptr(const void *p) {
+    if (!p) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// ------------------------------------------------------------------ layout planning
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Choose the K tiling of a [rows][K] matrix: one tile when the fp32 activation tile of
+// every batch row fits in shared memory and a unit of rows fits in one ring slot;
+// otherwise split K (only for residual-add epilogues, where split-K partial sums can be
+// accumulated).
+static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int max_batch,
+                     bool allow_split) {
+    for (int nkt = 1; nkt <= 64; nkt++) {
+        int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), kPadElems);
+        int real_nkt = (K + KB - 1) / KB;
+        size_t xs = (size_t)max_batch * KB * 4;
+        size_t unit_bytes = (size_t)KB * esz * rows_per_unit;
+        if (xs <= kXsBudget && unit_bytes <= (size_t)kChunkBytes) {
+            if (real_nkt > 1 && !allow_split) return false;
+            M.rows = rows;
+            M.K = K;
+            M.KB = KB;
+            M.KBp = KB;
+            M.nkt = real_nkt;
+            M.rows_per_unit = rows_per_unit;
+            M.units = real_nkt * (rows / rows_per_unit);
+            int rpc = (int)(kChunkBytes / ((size_t)KB * esz));
+            rpc = rpc / rows_per_unit * rows_per_unit;
+            M.rows_per_chunk = std::max(rpc, rows_per_unit);
+            M.layer_stride = (long long)real_nkt * rows * KB * esz;
+            return true;
+        }
+        if (!allow_split) return false;
+    }
+    return false;
+}
+
+// Copy rows [r0, r0 + n) of a row-major [*, K] source into the tiled layout at row
+// offset dst_row0 of a matrix with `rows` rows.
+static void pack_rows(uint8_t *dst, const Mat &M, int dst_row0, const uint8_t *src, int n, int esz) {
+    for (int kt = 0; kt < M.nkt; kt++) {
+        int k0 = kt * M.KB;
+        int kn = std::min(M.KB, M.K - k0);
+        for (int r = 0; r < n; r++) {
+            uint8_t *d = dst + ((size_t)kt * M.rows + dst_row0 + r) * M.KBp * esz;
+            memcpy(d, src + ((size_t)r * M.K + k0) * esz, (size_t)kn * esz);
+            if (kn < M.KBp) memset(d + (size_t)kn * esz, 0, (size_t)(M.KBp - kn) * esz);
+        }
+    }
+}
+
+static float widen(const uint8_t *p, int esz, size_t i) {
+    if (esz == 4) {
+        float f;
+        memcpy(&f, p + i * 4, 4);
+        return f;
+    }
+    uint16_t b;
+    memcpy(&b, p + i * 2, 2);
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+static bool config_ok(const slm_config *c, std::string &why) {
+    char buf[256];
+    if (c->dim <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+        c->hidden <= 0 || c->vocab <= 0 || c->max_seq <= 0 || c->max_batch <= 0) {
+        why = "every size in the config must be positive";
+        return false;
+    }
+    if (c->n_heads % c->n_kv_heads) {
+        why = "n_heads must be a multiple of n_kv_heads";
+        return false;
+    }
+    if (c->head_dim % 8 || c->head_dim > 256) {
+        snprintf(buf, sizeof buf, "head_dim %d must be a multiple of 8 and at most 256", c->head_dim);
+        why = buf;
+        return false;
+    }
+    if (c->max_batch > kMaxBatch) {
+        snprintf(buf, sizeof buf, "max_batch %d above %d", c->max_batch, kMaxBatch);
+        why = buf;
+        return false;
+    }
+    if (c->weight_dtype != SLM_F32 && c->weight_dtype != SLM_BF16) {
+        why = "weight_dtype must be SLM_F32 or SLM_BF16";
+        return false;
+    }
+    if (c->kv_dtype != SLM_F32 && c->kv_dtype != SLM_BF16) {
+        why = "kv_dtype must be SLM_F32 or SLM_BF16";
+        return false;
+    }
+    if (!(c->norm_eps >= 0.f) || !(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta)) {
+        why = "norm_eps must be >= 0 and rope_theta > 0";
+        return false;
+    }
+    return true;
+}
+
+static size_t weight_count(const slm_config *c) {
+    size_t dim = c->dim, qd = (size_t)c->n_heads * c->head_dim, kvd = (size_t)c->n_kv_heads * c->head_dim,
+           hid = c->hidden;
+    size_t per_layer = 2 * dim + qd * dim + 2 * kvd * dim + dim * qd + 3 * hid * dim;
+    return (size_t)c->vocab * dim + (size_t)c->n_layers * per_layer + dim;
+}
+
+// ------------------------------------------------------------------ ABI
+
+extern "C" const char *slm_status_string(int s) {
+    switch (s) {
+    case SLM_OK: return "ok";
+    case SLM_EINVAL: return "invalid argument";
+    case SLM_ENOMEM: return "out of memory";
+    case SLM_ECAPACITY: return "sequence capacity (max_seq) reached";
+    case SLM_EPOS: return "position does not match the sequence length";
+    case SLM_ESTATE: return "sequence in the wrong state";
+    case SLM_ECUDA: return "CUDA runtime error";
+    case SLM_ETIMEOUT: return "a bounded device-side wait ran out";
+    case SLM_EDEVICE: return "device reported a numeric fault";
+    case SLM_EUNSUPPORTED: return "configuration not supported by this build";
+    default: return "unknown status";
+    }
+}
+
+extern "C" const char *slm_last_error(const slm_ctx *ctx) {
+    return ctx ? ctx->err.c_str() : g_create_err.c_str();
+}
+
+extern "C" void slm_destroy(slm_ctx *ctx) {
+    if (!ctx) return;
+    cudaDeviceSynchronize();
+    for (void *p : ctx->allocs) cudaFree(p);
+    if (ctx->h_ids) cudaFreeHost(ctx->h_ids);
+    delete ctx;
+}
+
+static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, size_t nbytes) {
+    std::string why;
+    if (!config_ok(cfg, why)) return fail(c, SLM_EINVAL, "bad config: %s", why.c_str());
+    const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4;
+    const size_t n_w = weight_count(cfg);
+    if (nbytes != n_w * esz)
+        return fail(c, SLM_EINVAL, "weights are %zu bytes, the config needs %zu", nbytes, n_w * esz);
+    c->cfg = *cfg;
+    CK(c, cudaGetDevice(&c->device));
+    int sms = 0;
+    CK(c, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
+    int coop = 0;
+    CK(c, cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device));
+    if (!coop) return fail(c, SLM_EUNSUPPORTED, "device lacks cooperative launch");
+
+    const int dim = cfg->dim, H = cfg->n_heads, KV = cfg->n_kv_heads, hd = cfg->head_dim;
+    const int hid = cfg->hidden, V = cfg->vocab, L = cfg->n_layers, B = cfg->max_batch;
+    const int qd = H * hd, kvd = KV * hd, qkv_rows = qd + 2 * kvd;
+    Model &m = c->m;
+    m.dim = dim;
+    m.n_layers = L;
+    m.n_heads = H;
+    m.n_kv_heads = KV;
+    m.head_dim = hd;
+    m.hidden = hid;
+    m.vocab = V;
+    m.max_seq = cfg->max_seq;
+    m.max_batch = B;
+    m.norm_eps = cfg->norm_eps;
+    m.weight_bf16 = cfg->weight_dtype == SLM_BF16;
+    m.kv_bf16 = cfg->kv_dtype == SLM_BF16;
+    if (!plan_mat(m.emb, V, dim, 1, esz, B, false) || !plan_mat(m.qkv, qkv_rows, dim, 1, esz, B, false) ||
+        !plan_mat(m.wo, dim, qd, 1, esz, B, true) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false) ||
+        !plan_mat(m.w2, dim, hid, 1, esz, B, true))
+        return fail(c, SLM_EUNSUPPORTED,
+                    "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
+    m.emb.layer_stride = 0;
+
+    // attention scratch shares the activation tile region
+    size_t xs = (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2)) * 4;
+    for (const Mat *M : {&m.emb, &m.qkv, &m.wo, &m.w13, &m.w2})
+        xs = std::max(xs, (size_t)B * M->KBp * 4);
+    c->smem = decode_smem_bytes(round_up(xs, 128));
+    int per_sm = 0;
+    CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
+    if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
+    c->grid = sms * per_sm;
+    c->n_barriers = 5 * L;
+
+    // ---- weights: repack on the host, then one copy to the device
+    std::vector<uint8_t> src;
+    const uint8_t *w = (const uint8_t *)weights;
+    if (is_device_ptr(weights)) {
+        try {
+            src.resize(nbytes);
+        } catch (const std::bad_alloc &) {
+            return fail(c, SLM_ENOMEM, "host staging of %zu bytes failed", nbytes);
+        }
+        CK(c, cudaMemcpy(src.data(), weights, nbytes, cudaMemcpyDeviceToHost));
+        w = src.data();
+    }
+    const size_t al = 256;
+    size_t off_emb = 0;
+    size_t off_qkv = round_up(off_emb + (size_t)m.emb.nkt * V * m.emb.KBp * esz, al);
+    size_t off_wo = round_up(off_qkv + (size_t)L * m.qkv.layer_stride, al);
+    size_t off_w13 = round_up(off_wo + (size_t)L * m.wo.layer_stride, al);
+    size_t off_w2 = round_up(off_w13 + (size_t)L * m.w13.layer_stride, al);
+    size_t off_norm = round_up(off_w2 + (size_t)L * m.w2.layer_stride, al);
+    size_t off_rope = round_up(off_norm + ((size_t)L * 2 + 1) * dim * 4, al);
+    size_t total = round_up(off_rope + (size_t)cfg->max_seq * (hd / 2) * 2 * 4, al);
+    std::vector<uint8_t> h;
+    try {
+        h.assign(total, 0);
+    } catch (const std::bad_alloc &) {
+        return fail(c, SLM_ENOMEM, "host staging of %zu bytes failed", total);
+    }
+    // walk the canonical order
+    size_t cur = 0;
+    auto take = [&](size_t count) {
+        const uint8_t *p = w + cur * esz;
+        cur += count;
+        return p;
+    };
+    pack_rows(h.data() + off_emb, m.emb, 0, take((size_t)V * dim), V, esz);
+    float *norms = (float *)(h.data() + off_norm);
+    for (int l = 0; l < L; l++) {
+        const uint8_t *an = take(dim);
+        for (int i = 0; i < dim; i++) norms[(size_t)l * 2 * dim + i] = widen(an, esz, i);
+        uint8_t *qkv = h.data() + off_qkv + (size_t)l * m.qkv.layer_stride;
+        pack_rows(qkv, m.qkv, 0, take((size_t)qd * dim), qd, esz);
+        pack_rows(qkv, m.qkv, qd, take((size_t)kvd * dim), kvd, esz);
+        pack_rows(qkv, m.qkv, qd + kvd, take((size_t)kvd * dim), kvd, esz);
+        pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, take((size_t)dim * qd), dim, esz);
+        const uint8_t *fn = take(dim);
+        for (int i = 0; i < dim; i++) norms[(size_t)l * 2 * dim + dim + i] = widen(fn, esz, i);
+        const uint8_t *w1 = take((size_t)hid * dim);
+        const uint8_t *w3 = take((size_t)hid * dim);
+        uint8_t *w13 = h.data() + off_w13 + (size_t)l * m.w13.layer_stride;
+        for (int j = 0; j < hid; j++) {  // interleave gate and up rows
+            pack_rows(w13, m.w13, 2 * j, w1 + (size_t)j * dim * esz, 1, esz);
+            pack_rows(w13, m.w13, 2 * j + 1, w3 + (size_t)j * dim * esz, 1, esz);
+        }
+        pack_rows(h.data() + off_w2 + (size_t)l * m.w2.layer_stride, m.w2, 0, take((size_t)dim * hid), dim, esz);
+    }
+    const uint8_t *on = take(dim);
+    for (int i = 0; i < dim; i++) norms[(size_t)L * 2 * dim + i] = widen(on, esz, i);
+    if (cur != n_w) return fail(c, SLM_EINVAL, "internal: weight walk consumed %zu of %zu", cur, n_w);
+    // RoPE table: angle pos * theta^(-2i/hd) in double, cos/sin rounded to fp32
+    float *rope = (float *)(h.data() + off_rope);
+    for (int p = 0; p < cfg->max_seq; p++)
+        for (int i = 0; i < hd / 2; i++) {
+            double a = (double)p * std::pow((double)cfg->rope_theta, -2.0 * i / hd);
+            rope[((size_t)p * (hd / 2) + i) * 2] = (float)std::cos(a);
+            rope[((size_t)p * (hd / 2) + i) * 2 + 1] = (float)std::sin(a);
+        }
+    void *dblock = nullptr;
+    int rc = dev_alloc(c, &dblock, total);
+    if (rc) return rc;
+    CK(c, cudaMemcpy(dblock, h.data(), total, cudaMemcpyHostToDevice));
+    uint8_t *d = (uint8_t *)dblock;
+    m.emb.base = d + off_emb;
+    m.qkv.base = d + off_qkv;
+    m.wo.base = d + off_wo;
+    m.w13.base = d + off_w13;
+    m.w2.base = d + off_w2;
+    m.norms = (const float *)(d + off_norm);
+    m.rope = (const float *)(d + off_rope);
+
+    // ---- KV cache and scratch
+    const size_t kvesz = m.kv_bf16 ? 2 : 4;
+    const size_t kv_bytes = (size_t)L * B * KV * cfg->max_seq * hd * kvesz;
+    void *p;
+    if ((rc = dev_alloc(c, &p, kv_bytes))) return rc;
+    m.kc = (uint8_t *)p;
+    if ((rc = dev_alloc(c, &p, kv_bytes))) return rc;
+    m.vc = (uint8_t *)p;
+    CK(c, cudaMemset(m.kc, 0, kv_bytes));
+    CK(c, cudaMemset(m.vc, 0, kv_bytes));
+    struct {
+        void **dst;
+        size_t bytes;
+    } bufs[] = {
+        {(void **)&m.x, (size_t)B * dim * 4},
+        {(void **)&m.qkv_out, (size_t)B * qkv_rows * 4},
+        {(void **)&m.attn_out, (size_t)B * qd * 4},
+        {(void **)&m.hbuf, (size_t)B * hid * 4},
+        {(void **)&m.part, (size_t)B * H * kMaxChunksPerSeq * (hd + 2) * 4},
+        {(void **)&m.part_count, (size_t)B * KV * 4},
+        {(void **)&m.amax_val, (size_t)B * c->grid * 4},
+        {(void **)&m.amax_idx, (size_t)B * c->grid * 4},
+        {(void **)&m.amax_count, 4},
+        {(void **)&m.bar, 8},
+        {(void **)&m.status, 4},
+        {(void **)&m.abort_flag, 4},
+        {(void **)&c->d_tokens, (size_t)std::max(cfg->max_seq, B) * 4},
+        {(void **)&c->d_logits, (size_t)B * V * 4},
+        {(void **)&c->d_ids, (size_t)B * 4},
+    };
+    for (auto &b : bufs) {
+        if ((rc = dev_alloc(c, b.dst, b.bytes))) return rc;
+        CK(c, cudaMemset(*b.dst, 0, b.bytes));
+    }
+    CK(c, cudaMallocHost((void **)&c->h_ids, (size_t)B * 4));
+    c->len.assign(B, 0);
+    CK(c, cudaDeviceSynchronize());
+    return SLM_OK;
+}
+
+extern "C" int slm_create(const slm_config *config, const void *weights, size_t nbytes, slm_ctx **out) {
+    if (!out) return fail(nullptr, SLM_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!config || !weights) return fail(nullptr, SLM_EINVAL, "config or weights is NULL");
+    slm_ctx *c = new (std::nothrow) slm_ctx();
+    if (!c) return fail(nullptr, SLM_ENOMEM, "context allocation failed");
+    int rc = create_impl(c, config, weights, nbytes);
+    if (rc != SLM_OK) {
+        g_create_err = c->err;
+        slm_destroy(c);
+        return rc;
+    }
+    *out = c;
+    return SLM_OK;
+}
+
+// Split-K geometry of the attention phase for this step: about two items per CTA, at
+// least kMinAttnChunk positions per chunk, at most kMaxChunksPerSeq chunks per row.
+static void plan_attention(const slm_ctx *c, StepParams &P) {
+    const int KV = c->m.n_kv_heads;
+    long long work = 0;
+    int max_ctx = 1;
+    for (int b = 0; b < P.batch; b++) {
+        work += (long long)(P.pos[b] + 1) * KV;
+        max_ctx = std::max(max_ctx, P.pos[b] + 1);
+    }
+    long long ch = (work + 2LL * c->grid - 1) / (2LL * c->grid);
+    ch = std::max<long long>(ch, kMinAttnChunk);
+    ch = std::max<long long>(ch, (max_ctx + kMaxChunksPerSeq - 1) / kMaxChunksPerSeq);
+    ch = (ch + 31) / 32 * 32;
+    P.attn_chunk = (int)ch;
+    P.item_start[0] = 0;
+    for (int b = 0; b < P.batch; b++) {
+        P.nchunk[b] = (int)((P.pos[b] + 1 + ch - 1) / ch);
+        P.item_start[b + 1] = P.item_start[b] + KV * P.nchunk[b];
+    }
+}
+
+static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
+    P.m = c->m;
+    P.grid = c->grid;
+    P.n_barriers = c->n_barriers;
+    P.bar_base = c->bar_base;
+    plan_attention(c, P);
+    cudaError_t e = launch_decode_step(P, c->smem, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, SLM_ECUDA, "decode launch failed: %s", cudaGetErrorString(e));
+    }
+    c->bar_base += (unsigned long long)c->n_barriers * c->grid;
+    return SLM_OK;
+}
+
+extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids, const int32_t *tokens,
+                               const int32_t *positions, float *logits, int32_t *next_ids, void *stream) {
+    if (!c) return SLM_EINVAL;
+    if (!seq_ids || !tokens || !positions || !next_ids)
+        return fail(c, SLM_EINVAL, "seq_ids, tokens, positions and next_ids must be non-NULL");
+    if (batch < 1 || batch > c->cfg.max_batch)
+        return fail(c, SLM_EINVAL, "batch %d outside [1, %d]", batch, c->cfg.max_batch);
+    StepParams P{};
+    P.batch = batch;
+    for (int i = 0; i < batch; i++) {
+        int s = seq_ids[i];
+        if (s < 0 || s >= c->cfg.max_batch) return fail(c, SLM_EINVAL, "seq id %d out of range", s);
+        for (int j = 0; j < i; j++)
+            if (seq_ids[j] == s) return fail(c, SLM_EINVAL, "seq id %d repeated in one step", s);
+        if (positions[i] != c->len[s])
+            return fail(c, SLM_EPOS, "row %d: position %d but sequence %d holds %d positions", i,
+                        positions[i], s, c->len[s]);
+        if (positions[i] >= c->cfg.max_seq)
+            return fail(c, SLM_ECAPACITY, "row %d: position %d reaches max_seq %d", i, positions[i],
+                        c->cfg.max_seq);
+        P.seq[i] = s;
+        P.pos[i] = positions[i];
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool tok_dev = is_device_ptr(tokens);
+    const bool log_dev = !logits || is_device_ptr(logits);
+    const bool ids_dev = is_device_ptr(next_ids);
+    if (!tok_dev) {
+        for (int i = 0; i < batch; i++)
+            if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab)
+                return fail(c, SLM_EINVAL, "token %d out of range at row %d", tokens[i], i);
+        CK(c, cudaMemcpyAsync(c->d_tokens, tokens, (size_t)batch * 4, cudaMemcpyHostToDevice, s));
+        P.tokens = c->d_tokens;
+    } else {
+        P.tokens = tokens;
+    }
+    P.logits = logits ? (log_dev ? logits : c->d_logits) : nullptr;
+    P.next_ids = ids_dev ? next_ids : c->d_ids;
+    P.do_logits = 1;
+    int rc = launch(c, P, s);
+    if (rc) return rc;
+    for (int i = 0; i < batch; i++) c->len[P.seq[i]] = P.pos[i] + 1;
+    if (!log_dev) CK(c, cudaMemcpyAsync(logits, c->d_logits, (size_t)batch * c->cfg.vocab * 4, cudaMemcpyDeviceToHost, s));
+    if (!ids_dev) CK(c, cudaMemcpyAsync(c->h_ids, c->d_ids, (size_t)batch * 4, cudaMemcpyDeviceToHost, s));
+    if (!tok_dev || !log_dev || !ids_dev) {
+        CK(c, cudaStreamSynchronize(s));
+        if (!ids_dev) memcpy(next_ids, c->h_ids, (size_t)batch * 4);
+    }
+    return SLM_OK;
+}
+
+extern "C" int slm_prefill(slm_ctx *c, int32_t seq, const int32_t *tokens, int32_t n, float *last_logits,
+                           int32_t *next_id, void *stream) {
+    if (!c) return SLM_EINVAL;
+    if (!tokens || !next_id) return fail(c, SLM_EINVAL, "tokens and next_id must be non-NULL");
+    if (seq < 0 || seq >= c->cfg.max_batch) return fail(c, SLM_EINVAL, "seq %d out of range", seq);
+    if (n < 1) return fail(c, SLM_EINVAL, "prompt length %d < 1", n);
+    if (c->len[seq] != 0) return fail(c, SLM_ESTATE, "sequence %d is not empty (%d positions)", seq, c->len[seq]);
+    if (n > c->cfg.max_seq) return fail(c, SLM_ECAPACITY, "prompt of %d tokens exceeds max_seq %d", n, c->cfg.max_seq);
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool tok_dev = is_device_ptr(tokens);
+    const bool log_dev = !last_logits || is_device_ptr(last_logits);
+    const bool ids_dev = is_device_ptr(next_id);
+    const int32_t *dtok = tokens;
+    if (!tok_dev) {
+        for (int i = 0; i < n; i++)
+            if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab)
+                return fail(c, SLM_EINVAL, "token %d out of range at %d", tokens[i], i);
+        CK(c, cudaMemcpyAsync(c->d_tokens, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, s));
+        dtok = c->d_tokens;
+    }
+    for (int p = 0; p < n; p++) {
+        StepParams P{};
+        P.batch = 1;
+        P.seq[0] = seq;
+        P.pos[0] = p;
+        P.tokens = dtok + p;
+        const bool last = p == n - 1;
+        P.do_logits = last;
+        P.logits = last && last_logits ? (log_dev ? last_logits : c->d_logits) : nullptr;
+        P.next_ids = last ? (ids_dev ? next_id : c->d_ids) : nullptr;
+        int rc = launch(c, P, s);
+        if (rc) {
+            c->len[seq] = p;
+            return rc;
+        }
+    }
+    c->len[seq] = n;
+    if (!log_dev) CK(c, cudaMemcpyAsync(last_logits, c->d_logits, (size_t)c->cfg.vocab * 4, cudaMemcpyDeviceToHost, s));
+    if (!ids_dev) CK(c, cudaMemcpyAsync(c->h_ids, c->d_ids, 4, cudaMemcpyDeviceToHost, s));
+    if (!tok_dev || !log_dev || !ids_dev) {
+        CK(c, cudaStreamSynchronize(s));
+        if (!ids_dev) *next_id = c->h_ids[0];
+    }
+    return SLM_OK;
+}
+
+extern "C" int slm_reset(slm_ctx *c, int32_t seq) {
+    if (!c) return SLM_EINVAL;
+    if (seq == -1) {
+        std::fill(c->len.begin(), c->len.end(), 0);
+        return SLM_OK;
+    }
+    if (seq < 0 || seq >= c->cfg.max_batch) return fail(c, SLM_EINVAL, "seq %d out of range", seq);
+    c->len[seq] = 0;
+    return SLM_OK;
+}
+
+extern "C" int32_t slm_seq_len(const slm_ctx *c, int32_t seq) {
+    if (!c || seq < 0 || seq >= c->cfg.max_batch) return SLM_EINVAL;
+    return c->len[seq];
+}
+
+extern "C" int slm_sync(slm_ctx *c, void *stream) {
+    if (!c) return SLM_EINVAL;
+    CK(c, cudaStreamSynchronize((cudaStream_t)stream));
+    int st = 0;
+    CK(c, cudaMemcpy(&st, c->m.status, 4, cudaMemcpyDeviceToHost));
+    if (st == 0) return SLM_OK;
+    // clear the sticky state so that the next step starts clean
+    CK(c, cudaMemset(c->m.status, 0, 4));
+    CK(c, cudaMemset(c->m.abort_flag, 0, 4));
+    CK(c, cudaMemset(c->m.bar, 0, 8));
+    CK(c, cudaMemset(c->m.part_count, 0, (size_t)c->cfg.max_batch * c->cfg.n_kv_heads * 4));
+    CK(c, cudaMemset(c->m.amax_count, 0, 4));
+    CK(c, cudaDeviceSynchronize());
+    c->bar_base = 0;
+    if (st & (kStBarrierTimeout | kStRingTimeout))
+        return fail(c, SLM_ETIMEOUT, "device wait timed out (status 0x%x)", st);
+    return fail(c, SLM_EDEVICE, "device status 0x%x (NaN logits or token out of range)", st);
+}
+
+// ------------------------------------------------------------------ test hooks
+
+__global__ void fill_kv_kernel(uint8_t *p, size_t n, float v, int bf16) {
+    size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    size_t stride = (size_t)gridDim.x * blockDim.x;
+    if (bf16) {
+        __nv_bfloat16 b = __float2bfloat16_rn(v);
+        for (; i < n; i += stride) ((__nv_bfloat16 *)p)[i] = b;
+    } else {
+        for (; i < n; i += stride) ((float *)p)[i] = v;
+    }
+}
+
+extern "C" int slm_debug_fill_kv(slm_ctx *c, float value) {
+    if (!c) return SLM_EINVAL;
+    const slm_config &g = c->cfg;
+    size_t n = (size_t)g.n_layers * g.max_batch * g.n_kv_heads * g.max_seq * g.head_dim;
+    fill_kv_kernel<<<1024, 256>>>(c->m.kc, n, value, c->m.kv_bf16);
+    fill_kv_kernel<<<1024, 256>>>(c->m.vc, n, value, c->m.kv_bf16);
+    CK(c, cudaGetLastError());
+    CK(c, cudaDeviceSynchronize());
+    return SLM_OK;
+}
+
+extern "C" int slm_debug_copy_kv(slm_ctx *c, int32_t layer, int32_t seq, int32_t n_pos, float *k_host,
+                                 float *v_host) {
+    if (!c) return SLM_EINVAL;
+    const slm_config &g = c->cfg;
+    if (layer < 0 || layer >= g.n_layers || seq < 0 || seq >= g.max_batch)
+        return fail(c, SLM_EINVAL, "layer %d / seq %d out of range", layer, seq);
+    if (n_pos < -1 || n_pos > g.max_seq) return fail(c, SLM_EINVAL, "n_pos %d outside [-1, max_seq]", n_pos);
+    CK(c, cudaDeviceSynchronize());
+    const int n = n_pos < 0 ? c->len[seq] : n_pos, hd = g.head_dim;
+    const size_t esz = c->m.kv_bf16 ? 2 : 4;
+    std::vector<uint8_t> tmp((size_t)n * hd * esz + 1);
+    for (int which = 0; which < 2; which++) {
+        float *dst = which ? v_host : k_host;
+        if (!dst) continue;
+        const uint8_t *base = which ? c->m.vc : c->m.kc;
+        for (int kvh = 0; kvh < g.n_kv_heads; kvh++) {
+            size_t off = ((((size_t)layer * g.max_batch + seq) * g.n_kv_heads + kvh) * g.max_seq) * hd * esz;
+            CK(c, cudaMemcpy(tmp.data(), base + off, (size_t)n * hd * esz, cudaMemcpyDeviceToHost));
+            float *o = dst + (size_t)kvh * n * hd;
+            for (size_t i = 0; i < (size_t)n * hd; i++) o[i] = widen(tmp.data(), (int)esz, i);
+        }
+    }
+    return n;
+}
