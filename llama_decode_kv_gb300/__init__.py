@@ -20,7 +20,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "slm.h")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m llama_decode_kv_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python llama_decode_kv_gb300/build.py` "
         "(CUDA toolkit required); there is no CPU fallback")
 
 _lib = ctypes.CDLL(LIB_PATH)

@@ -1,7 +1,8 @@
 """Build libslm.so (the CUDA decode library) in-tree with nvcc for sm_103a.
 
 Each translation unit compiles in parallel, then nvcc links one shared object with the
-static CUDA runtime.  Usage: ``python -m llama_decode_kv_gb300.build [--verbose]``.
+static CUDA runtime.  Usage: ``python llama_decode_kv_gb300/build.py [--verbose]`` (run
+as a script: importing the package itself requires the built library).
 """
 from __future__ import annotations
 

@@ -614,9 +614,12 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
     // shared scratch: q [kMaxGroupPass][hd], per-warp states [warps][kMaxGroupPass][hd + 2]
     float *qs = S.xs;
     float *ws = S.xs + kMaxGroupPass * hd;
-    const int LP = hd / 8;           // lanes per position
-    const int PP = 32 / LP;          // positions per warp pass
-    const int grp = lane / LP, sub = lane % LP;
+    const int LP = hd / 8;           // lanes holding data for one position
+    int LPP = 1;                     // lanes per position, rounded up to a power of two
+    while (LPP < LP) LPP <<= 1;
+    const int PP = 32 / LPP;         // positions per warp pass
+    const int grp = lane / LPP, sub = lane % LPP;
+    const bool lane_on = sub < LP;   // lanes past head_dim / 8 carry zeros
     const int d0 = sub * 8;
 
     for (int jp = 0; jp < G; jp += kMaxGroupPass) {
@@ -635,7 +638,7 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++)
 #pragma unroll
-            for (int d = 0; d < 8; d++) qv[j][d] = (j < Gp) ? qs[j * hd + d0 + d] : 0.f;
+            for (int d = 0; d < 8; d++) qv[j][d] = (j < Gp && lane_on) ? qs[j * hd + d0 + d] : 0.f;
         float mx[kMaxGroupPass], ls[kMaxGroupPass], o[kMaxGroupPass][8];
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++) {
@@ -648,7 +651,7 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
             const int t = tb + grp;
             const bool valid = t < t1;
             float kv8[8], vv8[8];
-            if (valid) {
+            if (valid && lane_on) {
                 load8<KVBF16>(kbase + (size_t)t * rowbytes, d0, kv8);
                 load8<KVBF16>(vbase + (size_t)t * rowbytes, d0, vv8);
             } else {
@@ -661,7 +664,7 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
                 float s = 0.f;
 #pragma unroll
                 for (int d = 0; d < 8; d++) s = fmaf(qv[j][d], kv8[d], s);
-                for (int off = 1; off < LP; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                for (int off = 1; off < LPP; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
                 if (valid) {
                     float mn = fmaxf(mx[j], s);
                     float corr = exp2f(mx[j] - mn);  // exp2(-inf) = 0 on the first position
@@ -677,7 +680,7 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++) {
             if (j >= Gp) break;
-            for (int off = LP; off < 32; off <<= 1) {
+            for (int off = LPP; off < LPP * PP; off <<= 1) {
                 float m2 = __shfl_xor_sync(0xffffffffu, mx[j], off);
                 float l2 = __shfl_xor_sync(0xffffffffu, ls[j], off);
                 float o2[8];
@@ -685,7 +688,7 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
                 for (int d = 0; d < 8; d++) o2[d] = __shfl_xor_sync(0xffffffffu, o[j][d], off);
                 merge_state(mx[j], ls[j], o[j], m2, l2, o2);
             }
-            if (grp == 0) {
+            if (grp == 0 && lane_on) {
                 float *w = ws + ((size_t)warp * kMaxGroupPass + j) * (hd + 2);
 #pragma unroll
                 for (int d = 0; d < 8; d++) w[2 + d0 + d] = o[j][d];
