@@ -150,7 +150,9 @@ int slm_sync(slm_ctx *ctx, void *stream);
 /* slm_destroy -- free everything the context owns.  NULL is ignored. */
 void slm_destroy(slm_ctx *ctx);
 
-/* slm_last_error -- text of the context's last failure ("" if none). */
+/* slm_last_error -- text of the context's last failure ("" if none).  With ctx = NULL:
+ * the last failure, on the calling thread, of a call that has no context
+ * (slm_create, slm_attention_decode). */
 const char *slm_last_error(const slm_ctx *ctx);
 
 /* slm_status_string -- static text for a status code. */
@@ -173,6 +175,41 @@ int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, f
  * can check that a step writes exactly the slots it should.  Synchronous.
  */
 int slm_debug_fill_kv(slm_ctx *ctx, float value);
+
+/*
+ * slm_attention_workspace_bytes -- size in bytes of the device workspace that
+ * slm_attention_decode needs for this shape (split-K partial states and arrival
+ * counters); 0 for non-positive arguments.
+ */
+size_t slm_attention_workspace_bytes(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
+                                     int32_t head_dim);
+
+/*
+ * slm_attention_decode -- the decode-attention step on its own (kasahare 0.4.0 /
+ * simple-llm, "Architecture": attn = softmax(q . K^T / sqrt(d_head)) . V with GQA), over
+ * a caller-owned cache.  For every row b and query head h, with kv head
+ * g = h / (n_heads / n_kv_heads):
+ *     out[b][h] = sum_t softmax_t(q[b][h] . k[b][g][t] / sqrt(head_dim)) v[b][g][t],
+ *     t = 0 .. ctx_len[b] - 1.
+ * Keys and values are split into chunks of positions; each chunk keeps an online
+ * softmax and the partial states are merged by rescaling to a common maximum
+ * (flash-decoding).  The query is used as given (RoPE already applied).
+ *   q: device fp32 [batch][n_heads][head_dim].
+ *   k_cache, v_cache: device [batch][n_kv_heads][capacity][head_dim] of kv_dtype
+ *     (SLM_F32 or SLM_BF16); only positions < ctx_len[b] are read.
+ *   ctx_len: host int32[batch], each in [1, capacity].
+ *   out: device fp32 [batch][n_heads][head_dim].
+ *   workspace: device memory, 256-byte aligned, at least
+ *     slm_attention_workspace_bytes(batch, n_heads, n_kv_heads, head_dim) bytes; the
+ *     call owns it until the enqueued work finishes.
+ *   batch in [1, 16]; head_dim a multiple of 8 in [8, 256]; n_heads % n_kv_heads == 0.
+ *   Asynchronous on `stream`.  Errors: SLM_EINVAL (shape, NULL pointer, workspace too
+ *   small or misaligned), SLM_ECUDA (launch failure); slm_last_error(NULL) explains.
+ */
+int slm_attention_decode(int32_t batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                         int32_t capacity, int32_t kv_dtype, const float *q, const void *k_cache,
+                         const void *v_cache, const int32_t *ctx_len, float *out, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

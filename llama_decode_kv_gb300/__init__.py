@@ -55,6 +55,9 @@ _SIGS = {
     "slm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "slm_debug_copy_kv": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
     "slm_debug_fill_kv": (ctypes.c_int, [_P, ctypes.c_float]),
+    "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
+    "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
+                                            _P, ctypes.c_size_t, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -96,6 +99,17 @@ def _stream_ptr(stream) -> Optional[int]:
         import torch
         return torch.cuda.current_stream().cuda_stream
     return getattr(stream, "cuda_stream", stream)
+
+
+def attention_decode(q, k_cache, v_cache, ctx_len, out, workspace, kv_dtype: int, stream=None) -> int:
+    """slm_attention_decode over torch tensors: q/out [B][H][hd] fp32, caches
+    [B][KV][cap][hd], ctx_len a sequence of ints, workspace a uint8 device tensor."""
+    B, H, hd = q.shape
+    KV, cap = k_cache.shape[1], k_cache.shape[2]
+    lens = (ctypes.c_int32 * B)(*[int(x) for x in ctx_len])
+    return slm_attention_decode(B, H, KV, hd, cap, kv_dtype, _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                lens, _ptr(out), _ptr(workspace), workspace.numel(),
+                                _stream_ptr(stream))
 
 
 class Engine:

@@ -29,80 +29,11 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "attention.cuh"
+#include "device_common.cuh"
 #include "slm_internal.h"
 
 namespace slm {
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
-                     smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void compute_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ int ld_volatile_int(const int *p) {
-    return *(const volatile int *)p;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 // ------------------------------------------------------------------ shared memory
 
@@ -539,39 +470,9 @@ __device__ void finish_argmax(const StepParams &P, Shared &S, float (&best_v)[NB
 // ------------------------------------------------------------------ attention phase
 
 template <bool KVBF16>
-__device__ __forceinline__ void load8(const uint8_t *row, int d0, float (&v)[8]) {
-    if constexpr (KVBF16) {
-        uint4 u = __ldcg((const uint4 *)(row + d0 * 2));
-        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-        v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
-    } else {
-        float4 a = __ldcg((const float4 *)(row + d0 * 4));
-        float4 b = __ldcg((const float4 *)(row + d0 * 4 + 16));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-}
-
-__device__ __forceinline__ float kv_round(float v, bool bf16) {
-    return bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
-}
-
-// Online-softmax merge of (m, l, o) pairs in the log2 domain.
-__device__ __forceinline__ void merge_state(float &m, float &l, float (&o)[8], float m2, float l2,
-                                            const float (&o2)[8]) {
-    float M = fmaxf(m, m2);
-    float a = (m == -INFINITY) ? 0.f : exp2f(m - M);
-    float b = (m2 == -INFINITY) ? 0.f : exp2f(m2 - M);
-    l = l * a + l2 * b;
-#pragma unroll
-    for (int d = 0; d < 8; d++) o[d] = o[d] * a + o2[d] * b;
-    m = M;
-}
-
-template <bool KVBF16>
 __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, Shared &S) {
     const Model &m = P.m;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int hd = m.head_dim, H = m.n_heads, KV = m.n_kv_heads, G = H / KV;
     const int half = hd / 2;
     const int pos = P.pos[b], ctx = pos + 1, seq = P.seq[b];
@@ -584,7 +485,6 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
     uint8_t *vbase = m.vc + head_off;
     const float *qkv = m.qkv_out + (size_t)b * m.qkv.rows;
     const float *rope = m.rope + (size_t)pos * half * 2;
-    const float qscale = rsqrtf((float)hd) * 1.4426950408889634f;  // scores in log2 units
 
     // append k (rotated) and v at slot pos when this chunk ends at the new position
     if (t1 == ctx) {
@@ -611,150 +511,22 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
         }
     }
 
-    // shared scratch: q [kMaxGroupPass][hd], per-warp states [warps][kMaxGroupPass][hd + 2]
-    float *qs = S.xs;
-    float *ws = S.xs + kMaxGroupPass * hd;
-    const int LP = hd / 8;           // lanes holding data for one position
-    int LPP = 1;                     // lanes per position, rounded up to a power of two
-    while (LPP < LP) LPP <<= 1;
-    const int PP = 32 / LPP;         // positions per warp pass
-    const int grp = lane / LPP, sub = lane % LPP;
-    const bool lane_on = sub < LP;   // lanes past head_dim / 8 carry zeros
-    const int d0 = sub * 8;
-
-    for (int jp = 0; jp < G; jp += kMaxGroupPass) {
-        const int Gp = min(kMaxGroupPass, G - jp);
-        compute_sync();  // previous users of qs / ws are done; the append is visible
-        for (int e = tid; e < Gp * half; e += kComputeThreads) {
-            int j = e / half, i = e - j * half;
-            const float *qr = qkv + (size_t)(g * G + jp + j) * hd;
-            float cs = __ldg(rope + 2 * i), sn = __ldg(rope + 2 * i + 1);
-            float a = __ldcg(qr + i), bb = __ldcg(qr + i + half);
-            qs[j * hd + i] = (a * cs - bb * sn) * qscale;
-            qs[j * hd + i + half] = (a * sn + bb * cs) * qscale;
-        }
-        compute_sync();
-        float qv[kMaxGroupPass][8];
-#pragma unroll
-        for (int j = 0; j < kMaxGroupPass; j++)
-#pragma unroll
-            for (int d = 0; d < 8; d++) qv[j][d] = (j < Gp && lane_on) ? qs[j * hd + d0 + d] : 0.f;
-        float mx[kMaxGroupPass], ls[kMaxGroupPass], o[kMaxGroupPass][8];
-#pragma unroll
-        for (int j = 0; j < kMaxGroupPass; j++) {
-            mx[j] = -INFINITY;
-            ls[j] = 0.f;
-#pragma unroll
-            for (int d = 0; d < 8; d++) o[j][d] = 0.f;
-        }
-        for (int tb = t0 + warp * PP; tb < t1; tb += kComputeWarps * PP) {
-            const int t = tb + grp;
-            const bool valid = t < t1;
-            float kv8[8], vv8[8];
-            if (valid && lane_on) {
-                load8<KVBF16>(kbase + (size_t)t * rowbytes, d0, kv8);
-                load8<KVBF16>(vbase + (size_t)t * rowbytes, d0, vv8);
-            } else {
-#pragma unroll
-                for (int d = 0; d < 8; d++) kv8[d] = vv8[d] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < kMaxGroupPass; j++) {
-                if (j >= Gp) break;
-                float s = 0.f;
-#pragma unroll
-                for (int d = 0; d < 8; d++) s = fmaf(qv[j][d], kv8[d], s);
-                for (int off = 1; off < LPP; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (valid) {
-                    float mn = fmaxf(mx[j], s);
-                    float corr = exp2f(mx[j] - mn);  // exp2(-inf) = 0 on the first position
-                    float p = exp2f(s - mn);
-                    ls[j] = ls[j] * corr + p;
-#pragma unroll
-                    for (int d = 0; d < 8; d++) o[j][d] = fmaf(p, vv8[d], o[j][d] * corr);
-                    mx[j] = mn;
-                }
-            }
-        }
-        // merge the position groups of this warp (lanes with the same `sub`)
-#pragma unroll
-        for (int j = 0; j < kMaxGroupPass; j++) {
-            if (j >= Gp) break;
-            for (int off = LPP; off < LPP * PP; off <<= 1) {
-                float m2 = __shfl_xor_sync(0xffffffffu, mx[j], off);
-                float l2 = __shfl_xor_sync(0xffffffffu, ls[j], off);
-                float o2[8];
-#pragma unroll
-                for (int d = 0; d < 8; d++) o2[d] = __shfl_xor_sync(0xffffffffu, o[j][d], off);
-                merge_state(mx[j], ls[j], o[j], m2, l2, o2);
-            }
-            if (grp == 0 && lane_on) {
-                float *w = ws + ((size_t)warp * kMaxGroupPass + j) * (hd + 2);
-#pragma unroll
-                for (int d = 0; d < 8; d++) w[2 + d0 + d] = o[j][d];
-                if (sub == 0) {
-                    w[0] = mx[j];
-                    w[1] = ls[j];
-                }
-            }
-        }
-        compute_sync();
-        // merge the warps: thread e handles (head j, dim d)
-        for (int e = tid; e < Gp * hd; e += kComputeThreads) {
-            int j = e / hd, d = e - j * hd;
-            float M = -INFINITY;
-            for (int w = 0; w < kComputeWarps; w++)
-                M = fmaxf(M, ws[((size_t)w * kMaxGroupPass + j) * (hd + 2)]);
-            float L = 0.f, O = 0.f;
-            for (int w = 0; w < kComputeWarps; w++) {
-                const float *st = ws + ((size_t)w * kMaxGroupPass + j) * (hd + 2);
-                if (st[0] == -INFINITY) continue;
-                float sc = exp2f(st[0] - M);
-                L = fmaf(st[1], sc, L);
-                O = fmaf(st[2 + d], sc, O);
-            }
-            const int h = g * G + jp + j;
-            if (nc == 1) {
-                m.attn_out[(size_t)b * H * hd + (size_t)h * hd + d] = O / L;
-            } else {
-                float *pp = m.part + (((size_t)b * H + h) * kMaxChunksPerSeq + c) * (hd + 2);
-                pp[2 + d] = O;
-                if (d == 0) {
-                    pp[0] = M;
-                    pp[1] = L;
-                }
-            }
-        }
-    }
-    if (nc == 1) return;
-    // split-K: the last CTA to finish a (row, kv head) merges its chunks
-    compute_sync();
-    if (tid == 0) {
-        __threadfence();
-        int prev = atomicAdd(m.part_count + (size_t)b * KV + g, 1);
-        S.flags[0] = (prev == nc - 1);
-    }
-    compute_sync();
-    if (!S.flags[0]) return;
-    __threadfence();
-    for (int e = tid; e < G * hd; e += kComputeThreads) {
-        int j = e / hd, d = e - j * hd;
-        const int h = g * G + j;
-        const float *pp = m.part + (((size_t)b * H + h) * kMaxChunksPerSeq) * (hd + 2);
-        float M = -INFINITY;
-        for (int cc = 0; cc < nc; cc++) M = fmaxf(M, __ldcg(pp + (size_t)cc * (hd + 2)));
-        float L = 0.f, O = 0.f;
-        for (int cc = 0; cc < nc; cc++) {
-            const float *st = pp + (size_t)cc * (hd + 2);
-            float mc = __ldcg(st);
-            if (mc == -INFINITY) continue;
-            float sc = exp2f(mc - M);
-            L = fmaf(__ldcg(st + 1), sc, L);
-            O = fmaf(__ldcg(st + 2 + d), sc, O);
-        }
-        m.attn_out[(size_t)b * H * hd + (size_t)h * hd + d] = O / L;
-    }
-    if (tid == 0) *(volatile int *)(m.part_count + (size_t)b * KV + g) = 0;
+    AttnTask T;
+    T.q = qkv + (size_t)g * G * hd;
+    T.rope = rope;
+    T.kbase = kbase;
+    T.vbase = vbase;
+    T.out = m.attn_out + ((size_t)b * H + (size_t)g * G) * hd;
+    T.part = m.part + ((size_t)b * H + (size_t)g * G) * kMaxChunksPerSeq * (hd + 2);
+    T.counter = m.part_count + (size_t)b * KV + g;
+    T.hd = hd;
+    T.G = G;
+    T.t0 = t0;
+    T.t1 = t1;
+    T.nc = nc;
+    T.c = c;
+    // the appended row must be visible to every thread before the chunk is read
+    attn_core<KVBF16>(T, S.xs, &S.flags[0]);
 }
 
 template <bool KVBF16>

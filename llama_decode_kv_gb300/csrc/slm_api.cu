@@ -46,6 +46,8 @@ struct slm_ctx {
 
 static thread_local std::string g_create_err;
 
+void slm::set_detached_error(const char *msg) { g_create_err = msg; }
+
 static int fail(slm_ctx *c, int code, const char *fmt, ...) {
     char buf[512];
     va_list ap;

@@ -90,6 +90,9 @@ struct StepParams {
     int n_barriers;
 };
 
+// Record the error text of a failed call that has no context (slm_last_error(NULL)).
+void set_detached_error(const char *msg);
+
 // Per-CTA slice of a matrix: units [u0, u1) in tile-major order.
 __host__ __device__ inline void unit_range(int units_total, int grid, int cta, int &u0, int &u1) {
     long long t = units_total;
