@@ -211,6 +211,31 @@ int slm_attention_decode(int32_t batch, int32_t n_heads, int32_t n_kv_heads, int
                          const void *v_cache, const int32_t *ctx_len, float *out, void *workspace,
                          size_t workspace_bytes, void *stream);
 
+/*
+ * slm_attention_decode_noalloc -- slm_attention_decode without a workspace argument,
+ * for callers that cannot allocate device memory: code running where cudaMalloc is not
+ * allowed or not wanted (an application whose own allocator reserves all device memory
+ * up front, or a latency-critical loop that must not call an allocator, which can
+ * synchronise the device).  The pages describe no such entry point; it has no
+ * counterpart there.
+ *   Arguments, layouts and results are those of slm_attention_decode.  The split-K
+ *   scratch lives in one fixed array compiled into the library,
+ *   slm_attention_noalloc_max_bytes() bytes (4 MiB), which every GPU that loads the
+ *   library holds until the process exits.  Shapes whose scratch
+ *   (slm_attention_workspace_bytes) exceeds it fail with SLM_EINVAL and a message.
+ *   The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *   routine.  The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any stream
+ *   capture.  Every call shares the array and it keeps the last call's contents: the
+ *   call clears the arrival counters itself, but calls whose work overlaps on the GPU
+ *   (e.g. on two unordered streams) race on the array.
+ */
+size_t slm_attention_noalloc_max_bytes(void);
+int slm_attention_decode_noalloc(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t capacity, int32_t kv_dtype,
+                                 const float *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *ctx_len, float *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,9 @@ _SIGS = {
     "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
                                             _P, ctypes.c_size_t, _P]),
+    "slm_attention_noalloc_max_bytes": (ctypes.c_size_t, []),
+    "slm_attention_decode_noalloc": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P,
+                                                    _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -110,6 +113,15 @@ def attention_decode(q, k_cache, v_cache, ctx_len, out, workspace, kv_dtype: int
     return slm_attention_decode(B, H, KV, hd, cap, kv_dtype, _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                 lens, _ptr(out), _ptr(workspace), workspace.numel(),
                                 _stream_ptr(stream))
+
+
+def attention_decode_noalloc(q, k_cache, v_cache, ctx_len, out, kv_dtype: int, stream=None) -> int:
+    """slm_attention_decode_noalloc over torch tensors (no workspace argument)."""
+    B, H, hd = q.shape
+    KV, cap = k_cache.shape[1], k_cache.shape[2]
+    lens = (ctypes.c_int32 * B)(*[int(x) for x in ctx_len])
+    return slm_attention_decode_noalloc(B, H, KV, hd, cap, kv_dtype, _ptr(q), _ptr(k_cache),
+                                        _ptr(v_cache), lens, _ptr(out), _stream_ptr(stream))
 
 
 class Engine:

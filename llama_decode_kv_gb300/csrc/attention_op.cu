@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 
 #include "attention.cuh"
 #include "slm_internal.h"
@@ -156,5 +157,66 @@ extern "C" int slm_attention_decode(int32_t batch, int32_t n_heads, int32_t n_kv
     P.out = out;
     P.part = (float *)workspace;
     P.counters = (int *)((uint8_t *)workspace + attn_partials_bytes(batch, n_heads, head_dim));
+    return attn_launch(P, kv_dtype, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ allocation-free variant
+//
+// For callers that cannot allocate device memory: the split-K partial states and the
+// arrival counters live in one fixed array compiled into the library instead of a
+// caller-provided workspace.  Every GPU that loads the library holds this array until
+// the process exits.
+
+static constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_scratch_mu;
+static void *g_scratch_ptr[64];  // device address of g_attn_scratch, per device ordinal
+
+// The host cannot use g_attn_scratch's name as a device address; look the address up
+// once per device, with that device current.
+static int scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return attn_fail(SLM_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return attn_fail(SLM_EUNSUPPORTED, "device ordinal %d above 63", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess || !p)
+            return attn_fail(SLM_ECUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return SLM_OK;
+}
+
+extern "C" size_t slm_attention_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" int slm_attention_decode_noalloc(int32_t batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                            int32_t capacity, int32_t kv_dtype, const float *q, const void *k_cache,
+                                            const void *v_cache, const int32_t *ctx_len, float *out, void *stream) {
+    AttnOpParams P{};
+    int rc = attn_plan(batch, n_heads, n_kv_heads, head_dim, capacity, kv_dtype, ctx_len, P);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !out)
+        return attn_fail(SLM_EINVAL, "q, k_cache, v_cache and out must be non-NULL");
+    size_t need = slm_attention_workspace_bytes(batch, n_heads, n_kv_heads, head_dim);
+    if (need > kNoAllocScratchBytes)
+        return attn_fail(SLM_EINVAL,
+                         "this shape needs %zu bytes of scratch; the fixed scratch array holds %zu "
+                         "(use slm_attention_decode with a workspace)",
+                         need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if ((rc = scratch_address(&scratch))) return rc;
+    P.q = q;
+    P.k = (const uint8_t *)k_cache;
+    P.v = (const uint8_t *)v_cache;
+    P.out = out;
+    P.part = (float *)scratch;
+    P.counters = (int *)((uint8_t *)scratch + attn_partials_bytes(batch, n_heads, head_dim));
+    // attn_launch clears the arrival counters before the kernel runs; the partial
+    // states need no clearing (each is written before it is read)
     return attn_launch(P, kv_dtype, (cudaStream_t)stream);
 }
