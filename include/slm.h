@@ -170,6 +170,17 @@ int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, f
                       float *v_host);
 
 /*
+ * slm_debug_trace -- timeline hook (in the spirit of kasahare's "--timing" and
+ * forward_traced): with enable != 0, every following step records, for each CTA of
+ * the decode kernel and each phase (5 per layer: QKV, attention, Wo, W1/W3, W2; then
+ * logits and argmax), three %globaltimer readings in ns: entered, inputs ready, done
+ * (0 where a CTA had no work).  out_host: NULL, or host uint64 [grid][5 * n_layers + 2][3]
+ * receiving the last step's record (out_len entries, synchronous).  enable = 0 turns
+ * recording off.  Returns the grid size, or a negative SLM_E* code.
+ */
+int slm_debug_trace(slm_ctx *ctx, int32_t enable, unsigned long long *out_host, size_t out_len);
+
+/*
  * slm_debug_fill_kv -- test hook: fill the whole KV cache (every layer, slot and
  * position) with the fp32 value `value` (rounded to the cache type), so that a test
  * can check that a step writes exactly the slots it should.  Synchronous.

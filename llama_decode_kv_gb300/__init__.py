@@ -55,6 +55,7 @@ _SIGS = {
     "slm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "slm_debug_copy_kv": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
     "slm_debug_fill_kv": (ctypes.c_int, [_P, ctypes.c_float]),
+    "slm_debug_trace": (ctypes.c_int, [_P, _I32, _P, ctypes.c_size_t]),
     "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
                                             _P, ctypes.c_size_t, _P]),
@@ -191,6 +192,23 @@ class Engine:
         if rc < 0:
             raise SlmError(rc, "slm_debug_copy_kv", self.last_error())
         return k, v
+
+    def trace(self, enable: bool = True, fetch: bool = False):
+        """Turn the phase timeline on/off; with fetch, return the last step's record as
+        uint64 [grid][5 * n_layers + 2][3] (entered, inputs ready, done) in ns."""
+        if not fetch:
+            rc = slm_debug_trace(self.ctx, int(enable), None, 0)
+            if rc < 0:
+                raise SlmError(rc, "slm_debug_trace", self.last_error())
+            return None
+        grid = slm_debug_trace(self.ctx, int(enable), None, 0)
+        if grid < 0:
+            raise SlmError(grid, "slm_debug_trace", self.last_error())
+        out = np.zeros((grid, 5 * self.shape.n_layers + 2, 3), dtype=np.uint64)
+        rc = slm_debug_trace(self.ctx, int(enable), out.ctypes.data, out.size)
+        if rc < 0:
+            raise SlmError(rc, "slm_debug_trace", self.last_error())
+        return out
 
     def fill_kv(self, value: float):
         self._check(slm_debug_fill_kv(self.ctx, float(value)), "slm_debug_fill_kv")

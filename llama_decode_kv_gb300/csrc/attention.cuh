@@ -13,15 +13,16 @@
 
 namespace slm {
 
+// Eight consecutive elements of a cached key or value row (global or shared memory).
 template <bool KVBF16>
 __device__ __forceinline__ void load8(const uint8_t *row, int d0, float (&v)[8]) {
     if constexpr (KVBF16) {
-        uint4 u = __ldcg((const uint4 *)(row + d0 * 2));
+        uint4 u = *(const uint4 *)(row + d0 * 2);
         v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
         v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
     } else {
-        float4 a = __ldcg((const float4 *)(row + d0 * 4));
-        float4 b = __ldcg((const float4 *)(row + d0 * 4 + 16));
+        float4 a = *(const float4 *)(row + d0 * 4);
+        float4 b = *(const float4 *)(row + d0 * 4 + 16);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
@@ -46,13 +47,20 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float (&o)[8], f
 
 // One work item: G query heads x positions [t0, t1) of one (row, kv head).
 struct AttnTask {
-    const float *q;              // query rows of the group: head j at q + j * hd
+    const float *q;              // query rows of the group: head j at q + j * hd (shared
+                                 //   or global memory, complete before the call)
     const float *rope;           // (cos, sin) pairs of the position, or null: q is rotated
-    const uint8_t *kbase;        // cached keys of the (row, kv head): position t at t * hd
-    const uint8_t *vbase;        // cached values, same layout
+    const uint8_t *kbase;        // keys of the (row, kv head): position t at t * hd elements
+    const uint8_t *vbase;        //   (global cache, or a shared-memory copy of the chunk
+                                 //   addressed as if it started at position 0)
     float *out;                  // final output rows: head j at out + j * hd
     float *part;                 // partials: head j, chunk c at (j * kMaxChunksPerSeq + c) * (hd + 2)
     int *counter;                // arrivals of this (row, kv head)'s chunks
+    uint64_t *ll_part;           // if set: publish this chunk's states as tagged words
+                                 //   (head j at (j * ncap + c) * (hd + 2)); no merge here
+    uint64_t *ll_out;            // if set: publish the merged output as tagged words
+    uint32_t tag;
+    int ncap;                    // chunk capacity of ll_part
     int hd, G, t0, t1, nc, c;
 };
 
@@ -82,7 +90,7 @@ __device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
         for (int e = tid; e < Gp * half; e += kComputeThreads) {
             int j = e / half, i = e - j * half;
             const float *qr = T.q + (size_t)(jp + j) * hd;
-            float a = __ldcg(qr + i), bb = __ldcg(qr + i + half);
+            float a = qr[i], bb = qr[i + half];  // q may sit in shared or global memory
             if (T.rope) {
                 float cs = __ldg(T.rope + 2 * i), sn = __ldg(T.rope + 2 * i + 1);
                 qs[j * hd + i] = (a * cs - bb * sn) * qscale;
@@ -172,8 +180,18 @@ __device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
                 L = fmaf(st[1], sc, L);
                 O = fmaf(st[2 + d], sc, O);
             }
-            if (nc == 1) {
-                T.out[(size_t)(jp + j) * hd + d] = O / L;
+            if (T.ll_part) {
+                uint64_t *pp = T.ll_part + ((size_t)(jp + j) * T.ncap + c) * (hd + 2);
+                ll_store(pp + 2 + d, O, T.tag);
+                if (d == 0) {
+                    ll_store(pp, M, T.tag);
+                    ll_store(pp + 1, L, T.tag);
+                }
+            } else if (nc == 1) {
+                if (T.ll_out)
+                    ll_store(T.ll_out + (size_t)(jp + j) * hd + d, O / L, T.tag);
+                else
+                    T.out[(size_t)(jp + j) * hd + d] = O / L;
             } else {
                 float *pp = T.part + ((size_t)(jp + j) * kMaxChunksPerSeq + c) * (hd + 2);
                 pp[2 + d] = O;
@@ -184,7 +202,7 @@ __device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
             }
         }
     }
-    if (nc == 1) return;
+    if (T.ll_part || nc == 1) return;
     // split-K: the last CTA to finish a (row, kv head) merges its chunks
     compute_sync();
     if (tid == 0) {
@@ -209,7 +227,10 @@ __device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
             L = fmaf(__ldcg(st + 1), sc, L);
             O = fmaf(__ldcg(st + 2 + d), sc, O);
         }
-        T.out[(size_t)j * hd + d] = O / L;
+        if (T.ll_out)
+            ll_store(T.ll_out + (size_t)j * hd + d, O / L, T.tag);
+        else
+            T.out[(size_t)j * hd + d] = O / L;
     }
     if (tid == 0) *(volatile int *)T.counter = 0;
 }

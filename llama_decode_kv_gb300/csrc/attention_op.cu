@@ -47,6 +47,10 @@ __global__ void __launch_bounds__(kComputeThreads) attention_decode_kernel(const
     T.out = P.out + ((size_t)b * P.H + (size_t)g * G) * hd;
     T.part = P.part + ((size_t)b * P.H + (size_t)g * G) * kMaxChunksPerSeq * (hd + 2);
     T.counter = P.counters + (size_t)b * P.KV + g;
+    T.ll_part = nullptr;
+    T.ll_out = nullptr;
+    T.tag = 0;
+    T.ncap = 0;
     T.hd = hd;
     T.G = G;
     T.t0 = c * P.chunk;

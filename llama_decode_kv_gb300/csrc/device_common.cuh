@@ -82,4 +82,27 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Tagged 8-byte exchange word: value bits in the low half, tag in the high half.  One
+// aligned 64-bit store / load is single-copy atomic, so a reader never sees a value with
+// another write's tag.  Relaxed at GPU scope: no fence, the L1 is bypassed.
+__device__ __forceinline__ void ll_store(uint64_t *p, float v, uint32_t tag) {
+    uint64_t w = ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ll_load(const uint64_t *p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
 }  // namespace slm

@@ -20,9 +20,9 @@
 #include "slm_internal.h"
 
 namespace slm {
-cudaError_t launch_decode_step(const StepParams &P, size_t smem, cudaStream_t stream);
-cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm);
-size_t decode_smem_bytes(size_t xs_bytes);
+cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream);
+cudaError_t decode_occupancy(int weight_bf16, int *blocks_per_sm);
+size_t decode_smem_bytes();
 }  // namespace slm
 
 using namespace slm;
@@ -35,8 +35,9 @@ struct slm_ctx {
     Model m{};
     std::vector<void *> allocs;
     std::vector<int> len;
-    unsigned long long bar_base = 0;
-    int n_barriers = 0;
+    uint32_t launch_seq = 0;     // exchange tag of the last launch
+    unsigned long long *d_trace = nullptr;  // phase timeline, when tracing is on
+    bool trace_on = false;
     int *d_tokens = nullptr;     // staging for host-provided tokens [max(max_seq, max_batch)]
     float *d_logits = nullptr;   // staging for host-requested logits [max_batch][vocab]
     int *d_ids = nullptr;        // staging for host-requested ids [max_batch]
@@ -270,16 +271,21 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
                     "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
     m.emb.layer_stride = 0;
 
-    // attention scratch shares the activation tile region
-    size_t xs = (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2)) * 4;
-    for (const Mat *M : {&m.emb, &m.qkv, &m.wo, &m.w13, &m.w2})
-        xs = std::max(xs, (size_t)B * M->KBp * 4);
-    c->smem = decode_smem_bytes(round_up(xs, 128));
+    // shared-memory limits of the decode kernel
+    c->smem = decode_smem_bytes();
     int per_sm = 0;
-    CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
+    CK(c, decode_occupancy(m.weight_bf16, &per_sm));
     if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
     c->grid = sms * per_sm;
-    c->n_barriers = 5 * L;
+    if ((dim + c->grid - 1) / c->grid > kMaxOwn)
+        return fail(c, SLM_EUNSUPPORTED, "dim %d too large for %d CTAs", dim, c->grid);
+    {
+        const int G = H / KV;
+        size_t attn = (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) + (G + 2) * hd) * 4 +
+                      kAttnStageBytes;
+        if (attn > kXsBudget) return fail(c, SLM_EUNSUPPORTED, "attention scratch of %zu B too large", attn);
+        if ((size_t)B * c->grid * 2 * 4 > kXsBudget) return fail(c, SLM_EUNSUPPORTED, "argmax scratch too large");
+    }
 
     // ---- weights: repack on the host, then one copy to the device
     std::vector<uint8_t> src;
@@ -320,10 +326,16 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     for (int l = 0; l < L; l++) {
         const uint8_t *an = take(dim);
         for (int i = 0; i < dim; i++) norms[(size_t)l * 2 * dim + i] = widen(an, esz, i);
+        // QKV rows grouped by kv head: [q heads g*G .. g*G+G-1; k head g; v head g]
         uint8_t *qkv = h.data() + off_qkv + (size_t)l * m.qkv.layer_stride;
-        pack_rows(qkv, m.qkv, 0, take((size_t)qd * dim), qd, esz);
-        pack_rows(qkv, m.qkv, qd, take((size_t)kvd * dim), kvd, esz);
-        pack_rows(qkv, m.qkv, qd + kvd, take((size_t)kvd * dim), kvd, esz);
+        const uint8_t *wq = take((size_t)qd * dim), *wk = take((size_t)kvd * dim), *wv = take((size_t)kvd * dim);
+        const int G = H / KV;
+        for (int g = 0; g < KV; g++) {
+            const int r0 = g * (G + 2) * hd;
+            pack_rows(qkv, m.qkv, r0, wq + (size_t)g * G * hd * dim * esz, G * hd, esz);
+            pack_rows(qkv, m.qkv, r0 + G * hd, wk + (size_t)g * hd * dim * esz, hd, esz);
+            pack_rows(qkv, m.qkv, r0 + (G + 1) * hd, wv + (size_t)g * hd * dim * esz, hd, esz);
+        }
         pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, take((size_t)dim * qd), dim, esz);
         const uint8_t *fn = take(dim);
         for (int i = 0; i < dim; i++) norms[(size_t)l * 2 * dim + dim + i] = widen(fn, esz, i);
@@ -370,20 +382,20 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     m.vc = (uint8_t *)p;
     CK(c, cudaMemset(m.kc, 0, kv_bytes));
     CK(c, cudaMemset(m.vc, 0, kv_bytes));
+    const size_t Lz = L;
     struct {
         void **dst;
         size_t bytes;
     } bufs[] = {
-        {(void **)&m.x, (size_t)B * dim * 4},
-        {(void **)&m.qkv_out, (size_t)B * qkv_rows * 4},
-        {(void **)&m.attn_out, (size_t)B * qd * 4},
-        {(void **)&m.hbuf, (size_t)B * hid * 4},
-        {(void **)&m.part, (size_t)B * H * kMaxChunksPerSeq * (hd + 2) * 4},
-        {(void **)&m.part_count, (size_t)B * KV * 4},
-        {(void **)&m.amax_val, (size_t)B * c->grid * 4},
-        {(void **)&m.amax_idx, (size_t)B * c->grid * 4},
-        {(void **)&m.amax_count, 4},
-        {(void **)&m.bar, 8},
+        {(void **)&m.ll_x, (Lz + 1) * B * dim * 8},
+        {(void **)&m.ll_qkv, Lz * B * qkv_rows * 8},
+        {(void **)&m.ll_part, Lz * B * H * kMaxChunksA * (hd + 2) * 8},
+        {(void **)&m.ll_o, Lz * B * qd * 8},
+        {(void **)&m.ll_xa, Lz * B * dim * 8},
+        {(void **)&m.ll_h, Lz * B * hid * 8},
+        {(void **)&m.ll_amax, (size_t)B * c->grid * 2 * 8},
+        {(void **)&m.part, Lz * B * H * kMaxChunksPerSeq * (hd + 2) * 4},
+        {(void **)&m.part_count, Lz * B * KV * 4},
         {(void **)&m.status, 4},
         {(void **)&m.abort_flag, 4},
         {(void **)&c->d_tokens, (size_t)std::max(cfg->max_seq, B) * 4},
@@ -418,8 +430,12 @@ extern "C" int slm_create(const slm_config *config, const void *weights, size_t 
 
 // Split-K geometry of the attention phase for this step: about two items per CTA, at
 // least kMinAttnChunk positions per chunk, at most kMaxChunksPerSeq chunks per row.
+// When every row's chunk states fit the Wo consumers' shared-memory tile (and at most
+// kMaxChunksA chunks per row), the consumers merge them; otherwise the last CTA to
+// finish a (row, kv head) merges and publishes the output.
 static void plan_attention(const slm_ctx *c, StepParams &P) {
-    const int KV = c->m.n_kv_heads;
+    const Model &m = c->m;
+    const int KV = m.n_kv_heads, H = m.n_heads, hd = m.head_dim;
     long long work = 0;
     int max_ctx = 1;
     for (int b = 0; b < P.batch; b++) {
@@ -430,6 +446,19 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
     ch = std::max<long long>(ch, kMinAttnChunk);
     ch = std::max<long long>(ch, (max_ctx + kMaxChunksPerSeq - 1) / kMaxChunksPerSeq);
     ch = (ch + 31) / 32 * 32;
+    // consumer merge: batch * (KBp(Wo) + H * nc * (hd + 2)) floats must fit the tile
+    const long long tile = (long long)(kXsBudget / 4) / P.batch - m.wo.KBp;
+    long long nc_fit = tile > 0 ? tile / ((long long)H * (hd + 2)) : 0;
+    nc_fit = std::min<long long>(nc_fit, kMaxChunksA);
+    P.attn_consumer_merge = 0;
+    if (nc_fit >= 1) {
+        long long ch_a = std::max<long long>(ch, (max_ctx + nc_fit - 1) / nc_fit);
+        ch_a = (ch_a + 31) / 32 * 32;
+        if (ch_a <= 4 * std::max<long long>(ch, 128)) {
+            ch = ch_a;
+            P.attn_consumer_merge = 1;
+        }
+    }
     P.attn_chunk = (int)ch;
     P.item_start[0] = 0;
     for (int b = 0; b < P.batch; b++) {
@@ -441,15 +470,15 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
 static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
     P.m = c->m;
     P.grid = c->grid;
-    P.n_barriers = c->n_barriers;
-    P.bar_base = c->bar_base;
+    if (++c->launch_seq == 0) c->launch_seq = 1;  // tag 0 marks never-written words
+    P.tag = c->launch_seq;
+    P.trace = c->trace_on ? c->d_trace : nullptr;
     plan_attention(c, P);
-    cudaError_t e = launch_decode_step(P, c->smem, s);
+    cudaError_t e = launch_decode_step(P, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(c, SLM_ECUDA, "decode launch failed: %s", cudaGetErrorString(e));
     }
-    c->bar_base += (unsigned long long)c->n_barriers * c->grid;
     return SLM_OK;
 }
 
@@ -575,12 +604,9 @@ extern "C" int slm_sync(slm_ctx *c, void *stream) {
     // clear the sticky state so that the next step starts clean
     CK(c, cudaMemset(c->m.status, 0, 4));
     CK(c, cudaMemset(c->m.abort_flag, 0, 4));
-    CK(c, cudaMemset(c->m.bar, 0, 8));
-    CK(c, cudaMemset(c->m.part_count, 0, (size_t)c->cfg.max_batch * c->cfg.n_kv_heads * 4));
-    CK(c, cudaMemset(c->m.amax_count, 0, 4));
+    CK(c, cudaMemset(c->m.part_count, 0, (size_t)c->cfg.n_layers * c->cfg.max_batch * c->cfg.n_kv_heads * 4));
     CK(c, cudaDeviceSynchronize());
-    c->bar_base = 0;
-    if (st & (kStBarrierTimeout | kStRingTimeout))
+    if (st & (kStExchangeTimeout | kStRingTimeout))
         return fail(c, SLM_ETIMEOUT, "device wait timed out (status 0x%x)", st);
     return fail(c, SLM_EDEVICE, "device status 0x%x (NaN logits or token out of range)", st);
 }
@@ -596,6 +622,26 @@ __global__ void fill_kv_kernel(uint8_t *p, size_t n, float v, int bf16) {
     } else {
         for (; i < n; i += stride) ((float *)p)[i] = v;
     }
+}
+
+extern "C" int slm_debug_trace(slm_ctx *c, int32_t enable, unsigned long long *out_host, size_t out_len) {
+    if (!c) return SLM_EINVAL;
+    const size_t n = (size_t)c->grid * trace_slots(c->cfg.n_layers) * 3;
+    if (enable && !c->d_trace) {
+        void *p;
+        int rc = dev_alloc(c, &p, n * 8);
+        if (rc) return rc;
+        c->d_trace = (unsigned long long *)p;
+    }
+    if (enable && !c->trace_on) CK(c, cudaMemset(c->d_trace, 0, n * 8));
+    c->trace_on = enable != 0;
+    if (out_host) {
+        if (!c->d_trace) return fail(c, SLM_ESTATE, "tracing was never enabled");
+        if (out_len < n) return fail(c, SLM_EINVAL, "trace needs %zu entries", n);
+        CK(c, cudaDeviceSynchronize());
+        CK(c, cudaMemcpy(out_host, c->d_trace, n * 8, cudaMemcpyDeviceToHost));
+    }
+    return (int)c->grid;
 }
 
 extern "C" int slm_debug_fill_kv(slm_ctx *c, float value) {

@@ -18,12 +18,15 @@ constexpr int kChunkBytes = 16384;                    // one ring slot
 constexpr int kMaxBatch = 16;
 constexpr int kMaxGroupPass = 4;                      // query heads per attention pass
 constexpr int kMaxChunksPerSeq = 64;                  // split-K chunks per (row, kv head)
+constexpr int kMaxChunksA = 16;                       // chunks when consumers merge them
 constexpr int kMinAttnChunk = 32;                     // positions
-constexpr size_t kXsBudget = 120 * 1024;              // activation tile in shared memory
+constexpr size_t kXsBudget = 112 * 1024;              // activation tile in shared memory
+constexpr size_t kAttnStageBytes = 64 * 1024;         // K + V chunk copy in shared memory
+constexpr int kMaxOwn = 64;                           // residual rows one CTA may own
 constexpr int kPadElems = 8;                          // K tiles are padded to 8 elements
 
 // status word bits (device side)
-constexpr int kStBarrierTimeout = 1;
+constexpr int kStExchangeTimeout = 1;
 constexpr int kStRingTimeout = 2;
 constexpr int kStNanLogits = 4;
 constexpr int kStBadToken = 8;
@@ -51,25 +54,26 @@ struct Model {
     int weight_bf16;   // 1 = bf16 weights, 0 = fp32
     int kv_bf16;       // 1 = bf16 cache, 0 = fp32
     Mat emb;           // [vocab][dim], also the tied output projection
-    Mat qkv;           // [(H + 2 KV) hd][dim]
+    Mat qkv;           // [(H + 2 KV) hd][dim]: per kv group g, its G q heads, k, v rows
     Mat wo;            // [dim][H hd]
     Mat w13;           // [2 hidden][dim], rows 2j / 2j+1 = W1 row j / W3 row j
     Mat w2;            // [dim][hidden]
     const float *norms;      // [n_layers][2][dim] (attn, ffn) then [dim] output norm
     const float *rope;       // [max_seq][head_dim/2][2] = (cos, sin)
     uint8_t *kc, *vc;        // [n_layers][max_batch][KV][max_seq][hd]
-    // scratch
-    float *x;          // [max_batch][dim] residual stream
-    float *qkv_out;    // [max_batch][(H + 2 KV) hd]
-    float *attn_out;   // [max_batch][H hd]
-    float *hbuf;       // [max_batch][hidden]
-    float *part;       // [max_batch][H][kMaxChunksPerSeq][hd + 2] split-K partials
-    int *part_count;   // [max_batch][KV] arrival counters
-    float *amax_val;   // [max_batch][grid] per-CTA argmax partials
-    int *amax_idx;
-    int *amax_count;   // [1]
-    unsigned long long *bar;  // grid barrier counter
-    int *status;       // device status word
+    // Exchange buffers.  Every element is a tagged 8-byte word (value in the low half,
+    // the launch's tag in the high half) so that consumers poll the data itself.  They
+    // are per layer: nothing is rewritten within one launch.
+    uint64_t *ll_x;     // [n_layers + 1][max_batch][dim]: residual entering layer l
+    uint64_t *ll_qkv;   // [n_layers][max_batch][(H + 2 KV) hd]
+    uint64_t *ll_part;  // [n_layers][max_batch][H][kMaxChunksA][hd + 2] chunk states
+    uint64_t *ll_o;     // [n_layers][max_batch][H hd] merged attention output
+    uint64_t *ll_xa;    // [n_layers][max_batch][dim]: residual after the attention block
+    uint64_t *ll_h;     // [n_layers][max_batch][hidden] SwiGLU output
+    uint64_t *ll_amax;  // [max_batch][grid][2] per-CTA argmax (value, index)
+    float *part;        // [n_layers][max_batch][H][kMaxChunksPerSeq][hd + 2] (producer merge)
+    int *part_count;    // [n_layers][max_batch][KV] arrival counters (producer merge)
+    int *status;        // device status word
     int *abort_flag;
 };
 
@@ -81,14 +85,21 @@ struct StepParams {
     int item_start[kMaxBatch + 1];  // attention work items per row: KV * nchunks
     int nchunk[kMaxBatch];
     int attn_chunk;                 // positions per split-K chunk
+    int attn_consumer_merge;        // 1: Wo consumers merge chunk states; 0: last CTA merges
     const int *tokens;              // device [batch]
     float *logits;                  // device [batch][vocab] or null
     int *next_ids;                  // device [batch] or null
     int do_logits;                  // 0: skip the vocabulary projection (prefill)
-    unsigned long long bar_base;    // barrier counter value at launch
+    uint32_t tag;                   // this launch's exchange tag (never 0)
     int grid;
-    int n_barriers;
+    unsigned long long *trace;      // null, or [grid][trace_slots][3] phase timestamps
 };
+
+// Phase timeline of one step (slm_debug_trace): per CTA and phase, three %globaltimer
+// readings (ns): phase entered, inputs ready, phase done.  Phases: 5 per layer (QKV,
+// attention, Wo, W1/W3, W2), then logits and argmax.
+constexpr int kTracePerLayer = 5;
+__host__ __device__ inline int trace_slots(int n_layers) { return kTracePerLayer * n_layers + 2; }
 
 // Record the error text of a failed call that has no context (slm_last_error(NULL)).
 void set_detached_error(const char *msg);
