@@ -66,7 +66,7 @@ enum {
  * Embeddings are always tied (kasahare "Optimisations").  weight_dtype: SLM_F32 or
  * SLM_BF16.  kv_dtype: the cache element type, SLM_F32 or SLM_BF16 (rounded to
  * nearest-even on append).
- * Requirements: all counts > 0, n_heads % n_kv_heads == 0, head_dim a multiple of 8
+ * Requirements: all counts > 0, dim a multiple of 4, n_heads % n_kv_heads == 0, head_dim a multiple of 8
  * and <= 256, max_batch <= 16, norm_eps >= 0, rope_theta > 0.  Shapes whose fp32
  * activation tile (max_batch x input width) cannot fit in shared memory give
  * SLM_EUNSUPPORTED.

@@ -98,11 +98,26 @@ __device__ bool wait_slot(const StepParams &P, uint64_t *bar, uint32_t parity) {
     }
 }
 
+// Shared-memory position of element k of a staged activation row.  With bf16 weights
+// a lane multiplies the 8 elements 8p..8p+7 of piece p; storing elements 8p+e at plane
+// e/4, offset 4p + e%4 makes every lane's two float4 reads contiguous across the warp
+// (no bank conflicts).  fp32 weights keep the natural order.
+__device__ __forceinline__ int xpos(int k, int KBp, bool perm) {
+    return perm ? ((k & 4) ? (KBp >> 1) : 0) + ((k >> 3) << 2) + (k & 3) : k;
+}
+
+__device__ __forceinline__ int xinv(int q, int KBp, bool perm) {
+    if (!perm) return q;
+    const int h = q >= (KBp >> 1) ? 1 : 0, r = q - h * (KBp >> 1);
+    return ((r >> 2) << 3) + (h << 2) + (r & 3);
+}
+
 // Poll rows x len tagged words (row stride src_ld) into shared memory (row stride
-// dst_ld) until every tag equals `tag`.  Each thread keeps up to 8 loads in flight.
-// All compute threads call it; it ends with a CTA barrier.
+// dst_ld; element j of a row at xpos(j, perm_ld) when perm_ld > 0) until every tag
+// equals `tag`.  Each thread keeps up to 8 loads in flight.  All compute threads call
+// it; it ends with a CTA barrier.
 __device__ void ll_poll(const StepParams &P, const uint64_t *src, int src_ld, int rows, int len,
-                        float *dst, int dst_ld, uint32_t tag) {
+                        float *dst, int dst_ld, uint32_t tag, int perm_ld = 0) {
     constexpr int kBatch = 8;
     const int tid = threadIdx.x;
     const int n = rows * len;
@@ -115,7 +130,7 @@ __device__ void ll_poll(const StepParams &P, const uint64_t *src, int src_ld, in
             need[k] = i < n;
             int r = need[k] ? i / len : 0, j = need[k] ? i - r * len : 0;
             so[k] = r * src_ld + j;
-            dof[k] = r * dst_ld + j;
+            dof[k] = r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j);
         }
         unsigned long long t0 = 0;
         for (int it = 0;; it++) {
@@ -188,34 +203,94 @@ __device__ __forceinline__ void for_each_chunk(const Mat &M, int layer, int esz,
 }
 
 // ------------------------------------------------------------------ streaming warp
+// A cursor over the same chunk sequence as the compute warps walk: per layer QKV, Wo,
+// W1/W3, W2, then the embedding (logits) when requested.
 
-__device__ void producer(const StepParams &P, Shared &S) {
+struct Cursor {
+    int phase, layer, kt, u, u0, u1;
+    bool done;
+};
+
+__device__ __forceinline__ const Mat &phase_mat(const Model &m, int phase) {
+    return phase == 0 ? m.qkv : phase == 1 ? m.wo : phase == 2 ? m.w13 : phase == 3 ? m.w2 : m.emb;
+}
+
+__device__ void cursor_enter(const StepParams &P, Cursor &c) {
+    const Mat &M = phase_mat(P.m, c.phase);
+    unit_range(M.rows / M.rows_per_unit, P.grid, blockIdx.x, c.u0, c.u1);
+    c.kt = 0;
+    c.u = c.u0;
+}
+
+__device__ void cursor_init(const StepParams &P, Cursor &c) {
+    c.phase = 0;
+    c.layer = 0;
+    c.done = false;
+    cursor_enter(P, c);
+}
+
+// Next chunk of the sequence; false at the end.
+__device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
     const Model &m = P.m;
     const int esz = m.weight_bf16 ? 2 : 4;
-    const int cta = blockIdx.x, grid = P.grid;
+    while (!c.done) {
+        const Mat &M = phase_mat(m, c.phase);
+        if (c.u < c.u1) {
+            const int cu = M.rows_per_chunk / M.rows_per_unit;
+            const long long rowbytes = (long long)M.KBp * esz;
+            out.kt = c.kt;
+            out.unit0 = c.u - c.u0;
+            out.nunits = min(cu, c.u1 - c.u);
+            out.src = M.base + (long long)(c.phase == 4 ? 0 : c.layer) * M.layer_stride +
+                      ((long long)c.kt * M.rows + (long long)c.u * M.rows_per_unit) * rowbytes;
+            out.bytes = (uint32_t)((long long)out.nunits * M.rows_per_unit * rowbytes);
+            c.u += out.nunits;
+            return true;
+        }
+        if (++c.kt < M.nkt) {
+            c.u = c.u0;
+            continue;
+        }
+        if (c.phase < 3) {
+            c.phase++;
+        } else if (c.phase == 3 && c.layer + 1 < m.n_layers) {
+            c.layer++;
+            c.phase = 0;
+        } else if (c.phase == 3 && P.do_logits) {
+            c.phase = 4;
+        } else {
+            c.done = true;
+            break;
+        }
+        cursor_enter(P, c);
+    }
+    return false;
+}
+
+// Copies this CTA's chunks into the ring, and keeps up to kL2Lookahead bytes of the
+// chunks after them on their way into L2, so that ring refills hit L2 rather than HBM.
+__device__ void producer(const StepParams &P, Shared &S) {
+    Cursor ic, pc;
+    cursor_init(P, ic);
+    cursor_init(P, pc);
+    long long ahead = 0;  // bytes prefetched into L2 and not yet copied into the ring
     uint32_t issued = 0;
-    bool dead = false;
-    auto issue = [&](const Chunk &c) {
-        if (dead) return;
-        uint32_t slot = issued % kRingSlots;
+    Chunk c, q;
+    while (cursor_next(P, ic, c)) {
+        while (ahead < kL2Lookahead && cursor_next(P, pc, q)) {
+            bulk_prefetch_l2(q.src, q.bytes);
+            ahead += q.bytes;
+        }
+        ahead -= c.bytes;
+        const uint32_t slot = issued % kRingSlots;
         if (issued >= (uint32_t)kRingSlots) {
-            uint32_t parity = ((issued / kRingSlots) - 1) & 1;
-            if (!wait_slot(P, &S.empty[slot], parity)) {
-                dead = true;
-                return;
-            }
+            const uint32_t parity = ((issued / kRingSlots) - 1) & 1;
+            if (!wait_slot(P, &S.empty[slot], parity)) break;
         }
         mbar_expect_tx(&S.full[slot], c.bytes);
         bulk_g2s(S.ring + (size_t)slot * kChunkBytes, c.src, c.bytes, &S.full[slot]);
         issued++;
-    };
-    for (int l = 0; l < m.n_layers; l++) {
-        for_each_chunk(m.qkv, l, esz, cta, grid, issue);
-        for_each_chunk(m.wo, l, esz, cta, grid, issue);
-        for_each_chunk(m.w13, l, esz, cta, grid, issue);
-        for_each_chunk(m.w2, l, esz, cta, grid, issue);
     }
-    if (P.do_logits) for_each_chunk(m.emb, 0, esz, cta, grid, issue);
     // Never leave with a copy in flight: wait (bounded, ignoring the abort flag) for the
     // completion of every slot that may still be filling.
     uint32_t first = issued > (uint32_t)kRingSlots ? issued - kRingSlots : 0;
@@ -270,14 +345,15 @@ __device__ void init_residual(const StepParams &P, Shared &S) {
     }
 }
 
-// RMSNorm of the staged rows in place: xs[b][k] = xs[b][k] * rsqrt(mean + eps) * g[k].
-__device__ void norm_in_place(const StepParams &P, float *xs, int ld, const float *g, Shared &S) {
+// RMSNorm of the staged rows in place: x[k] = x[k] * rsqrt(mean + eps) * g[k] for the
+// dim logical elements; the padding past dim must already be zero.
+__device__ void norm_in_place(const StepParams &P, float *xs, int ld, const float *g, bool perm, Shared &S) {
     const Model &m = P.m;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int b = warp; b < P.batch; b += kComputeWarps) {
         const float *r = xs + (size_t)b * ld;
         float ss = 0.f;
-        for (int k = lane; k < m.dim; k += 32) ss = fmaf(r[k], r[k], ss);
+        for (int q = lane; q < ld; q += 32) ss = fmaf(r[q], r[q], ss);
         ss = warp_sum(ss);
         if (lane == 0) S.rs[b] = 1.0f / sqrtf(ss / (float)m.dim + m.norm_eps);
     }
@@ -285,20 +361,24 @@ __device__ void norm_in_place(const StepParams &P, float *xs, int ld, const floa
     for (int b = 0; b < P.batch; b++) {
         float *r = xs + (size_t)b * ld;
         const float rs = S.rs[b];
-        for (int k = tid; k < m.dim; k += kComputeThreads) r[k] = (r[k] * rs) * __ldg(g + k);
+        for (int q = tid; q < ld; q += kComputeThreads) {
+            const int k = xinv(q, ld, perm);
+            if (k < m.dim) r[q] = (r[q] * rs) * g[k];
+        }
     }
     compute_sync();
 }
 
-__device__ void zero_pad(const StepParams &P, float *xs, int ld, int from) {
+__device__ void zero_pad(const StepParams &P, float *xs, int ld, int from, bool perm) {
     for (int b = 0; b < P.batch; b++)
-        for (int k = from + (int)threadIdx.x; k < ld; k += kComputeThreads) xs[(size_t)b * ld + k] = 0.f;
+        for (int k = from + (int)threadIdx.x; k < ld; k += kComputeThreads) xs[(size_t)b * ld + xpos(k, ld, perm)] = 0.f;
 }
 
 // Merge the chunk states of every (row, head) published by the attention items into
 // the Wo input tile: o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 __device__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M, Shared &S) {
     const Model &m = P.m;
+    const bool perm = m.weight_bf16;
     const int H = m.n_heads, hd = m.head_dim, st = hd + 2;
     int ncmax = 1;
     for (int b = 0; b < P.batch; b++) ncmax = max(ncmax, P.nchunk[b]);
@@ -325,198 +405,240 @@ __device__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M,
                 L = fmaf(sp[(size_t)c * st + 1], sc, L);
                 O = fmaf(sp[(size_t)c * st + 2 + d], sc, O);
             }
-            S.xs[(size_t)b * M.KBp + e] = O / L;
+            S.xs[(size_t)b * M.KBp + xpos(e, M.KBp, perm)] = O / L;
         }
     }
-    zero_pad(P, S.xs, M.KBp, H * hd);
+    zero_pad(P, S.xs, M.KBp, H * hd, perm);
     compute_sync();
 }
 
-// Stage the input of phase `epi` (K tile kt) into S.xs as fp32 [batch][KBp].
+// Stage the input of phase `epi` (K tile kt) into S.xs as fp32 [batch][KBp] (element
+// order given by xpos).
 __device__ void stage_input(const StepParams &P, int epi, int layer, const Mat &M, int kt, Shared &S) {
     const Model &m = P.m;
     const int tid = threadIdx.x;
+    const bool perm = m.weight_bf16;
+    const int pl = perm ? M.KBp : 0;
     compute_sync();  // everyone is done with the previous tile
     if (epi == EPI_QKV || epi == EPI_W13 || epi == EPI_LOGITS) {
-        if (epi == EPI_QKV && layer == 0) {
-            for (int b = 0; b < P.batch; b++) {
-                int tok = token_of(P, b);
-                for (int k = tid; k < m.dim; k += kComputeThreads) S.xs[(size_t)b * M.KBp + k] = emb_elem(m, tok, k);
-            }
-            compute_sync();
-        } else {
-            const uint64_t *src = epi == EPI_W13 ? m.ll_xa + ll_layer(P, layer, m.dim)
-                                                 : m.ll_x + ll_layer(P, epi == EPI_QKV ? layer : m.n_layers, m.dim);
-            ll_poll(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, P.tag);
-        }
+        // the gains do not depend on this step: fetch them while waiting for x
         const float *g = epi == EPI_QKV   ? m.norms + (size_t)layer * 2 * m.dim
                          : epi == EPI_W13 ? m.norms + (size_t)layer * 2 * m.dim + m.dim
                                           : m.norms + (size_t)m.n_layers * 2 * m.dim;
-        norm_in_place(P, S.xs, M.KBp, g, S);
-        zero_pad(P, S.xs, M.KBp, m.dim);
+        float *gs = S.xs + (size_t)P.batch * M.KBp;
+        for (int k = tid * 4; k < m.dim; k += kComputeThreads * 4) cp_async16(gs + k, g + k);
+        if (epi == EPI_QKV && layer == 0) {
+            for (int b = 0; b < P.batch; b++) {
+                int tok = token_of(P, b);
+                for (int k = tid; k < m.dim; k += kComputeThreads)
+                    S.xs[(size_t)b * M.KBp + xpos(k, M.KBp, perm)] = emb_elem(m, tok, k);
+            }
+        } else {
+            const uint64_t *src = epi == EPI_W13 ? m.ll_xa + ll_layer(P, layer, m.dim)
+                                                 : m.ll_x + ll_layer(P, epi == EPI_QKV ? layer : m.n_layers, m.dim);
+            ll_poll(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, P.tag, pl);
+        }
+        zero_pad(P, S.xs, M.KBp, m.dim, perm);
+        cp_async_wait_all();
         compute_sync();
+        norm_in_place(P, S.xs, M.KBp, gs, perm, S);
     } else if (epi == EPI_WO) {
         if (P.attn_consumer_merge) {
             merge_chunk_states(P, layer, M, S);
         } else {
             const int qd = m.n_heads * m.head_dim;
-            ll_poll(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, P.tag);
-            zero_pad(P, S.xs, M.KBp, qd);
+            ll_poll(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, P.tag, pl);
+            zero_pad(P, S.xs, M.KBp, qd, perm);
             compute_sync();
         }
     } else {  // W2: tile kt of the SwiGLU output
         const int k0 = kt * M.KB, kn = min(M.K - k0, M.KB);
-        ll_poll(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, P.tag);
-        zero_pad(P, S.xs, M.KBp, kn);
+        ll_poll(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, P.tag, pl);
+        zero_pad(P, S.xs, M.KBp, kn, perm);
         compute_sync();
     }
 }
 
 // ------------------------------------------------------------------ GEMV arithmetic
 
-// dot of one 16-byte weight piece with the matching activations of every row
-template <int NB, bool WBF16>
-__device__ __forceinline__ void piece_fma(const uint4 w, const float *xs, int KBp, int p, int batch,
-                                          float (&acc)[NB]) {
-    if constexpr (WBF16) {
-        float wf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                       bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+// A warp works on RG rows at once: RG independent accumulator chains per batch row,
+// one activation load per piece shared by all of them.
+template <int NB> struct GemvShape {
+    static constexpr int R = NB == 1 ? 4 : NB <= 4 ? 2 : 1;
+};
+
+template <int V> struct Log2 {
+    static constexpr int value = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : V >= 2 ? 1 : 0;
+};
+
+// Sum each of the V per-lane values over the warp (V a power of two <= 32) with a
+// transposing butterfly: V - 1 + 5 - log2(V) shuffles instead of 5 V.  Afterwards lane
+// l holds the total of value (l >> (5 - log2 V)).
+template <int V>
+__device__ __forceinline__ float reduce_scatter(float (&v)[V]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int b = 0; b < NB; b++) {
-            if (NB > 1 && b >= batch) break;
-            const float4 *xp = (const float4 *)(xs + (size_t)b * KBp + p * 8);
-            float4 x0 = xp[0], x1 = xp[1];
-            float a = acc[b];
-            a = fmaf(wf[0], x0.x, a);
-            a = fmaf(wf[1], x0.y, a);
-            a = fmaf(wf[2], x0.z, a);
-            a = fmaf(wf[3], x0.w, a);
-            a = fmaf(wf[4], x1.x, a);
-            a = fmaf(wf[5], x1.y, a);
-            a = fmaf(wf[6], x1.z, a);
-            a = fmaf(wf[7], x1.w, a);
-            acc[b] = a;
-        }
-    } else {
-        float wf[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                       __uint_as_float(w.w)};
+    for (int half = V / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
 #pragma unroll
-        for (int b = 0; b < NB; b++) {
-            if (NB > 1 && b >= batch) break;
-            float4 x0 = *(const float4 *)(xs + (size_t)b * KBp + p * 4);
-            float a = acc[b];
-            a = fmaf(wf[0], x0.x, a);
-            a = fmaf(wf[1], x0.y, a);
-            a = fmaf(wf[2], x0.z, a);
-            a = fmaf(wf[3], x0.w, a);
-            acc[b] = a;
+        for (int i = 0; i < half; i++) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
+#pragma unroll
+    for (int off = 16 >> Log2<V>::value; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    return v[0];
 }
 
-// One row of a ring slot against every batch row; returns the sums in every lane.
-template <int NB, bool WBF16>
-__device__ __forceinline__ void row_dot(const uint8_t *wrow, const float *xs, int KBp, int batch,
-                                        float (&acc)[NB]) {
+// Dots of RG weight rows with every staged batch row.  Group row r lives at
+// base + (r / RPU) * unit_stride + (r % RPU) * rowbytes; rows r >= nr are skipped.
+// Value index r * NB + b.
+template <int NB, int RG, int RPU, bool WBF16>
+__device__ __forceinline__ void rows_dot(const uint8_t *base, size_t unit_stride, size_t rowbytes, int nr,
+                                         const float *xs, int KBp, int batch, float (&acc)[RG * NB]) {
     const int lane = threadIdx.x & 31;
     constexpr int EPP = WBF16 ? 8 : 4;
     const int pieces = KBp / EPP;
 #pragma unroll
-    for (int b = 0; b < NB; b++) acc[b] = 0.f;
-    const uint4 *w4 = (const uint4 *)wrow;
-    int p = lane;
-    for (; p + 32 < pieces; p += 64) {
-        uint4 wa = w4[p], wb = w4[p + 32];
-        piece_fma<NB, WBF16>(wa, xs, KBp, p, batch, acc);
-        piece_fma<NB, WBF16>(wb, xs, KBp, p + 32, batch, acc);
-    }
-    if (p < pieces) piece_fma<NB, WBF16>(w4[p], xs, KBp, p, batch, acc);
+    for (int v = 0; v < RG * NB; v++) acc[v] = 0.f;
+    for (int p = lane; p < pieces; p += 32) {
+        float wf[RG][EPP];
 #pragma unroll
-    for (int b = 0; b < NB; b++) {
-        if (NB > 1 && b >= batch) break;
-        acc[b] = warp_sum(acc[b]);
+        for (int r = 0; r < RG; r++) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (r < nr) w = ((const uint4 *)(base + (size_t)(r / RPU) * unit_stride + (size_t)(r % RPU) * rowbytes))[p];
+            if constexpr (WBF16) {
+                wf[r][0] = bf16_lo(w.x); wf[r][1] = bf16_hi(w.x); wf[r][2] = bf16_lo(w.y); wf[r][3] = bf16_hi(w.y);
+                wf[r][4] = bf16_lo(w.z); wf[r][5] = bf16_hi(w.z); wf[r][6] = bf16_lo(w.w); wf[r][7] = bf16_hi(w.w);
+            } else {
+                wf[r][0] = __uint_as_float(w.x); wf[r][1] = __uint_as_float(w.y);
+                wf[r][2] = __uint_as_float(w.z); wf[r][3] = __uint_as_float(w.w);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; b++) {
+            if (NB > 1 && b >= batch) break;
+            float x[EPP];
+            if constexpr (WBF16) {
+                const float *xr = xs + (size_t)b * KBp + p * 4;  // planes of xpos()
+                const float4 x0 = *(const float4 *)xr, x1 = *(const float4 *)(xr + (KBp >> 1));
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+            } else {
+                const float4 x0 = *(const float4 *)(xs + (size_t)b * KBp + p * 4);
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+            }
+#pragma unroll
+            for (int r = 0; r < RG; r++)
+#pragma unroll
+                for (int e = 0; e < EPP; e++) acc[r * NB + b] = fmaf(wf[r][e], x[e], acc[r * NB + b]);
+        }
     }
 }
 
 // ------------------------------------------------------------------ GEMV phases
 
+// One group of a warp's units: finish the dots and run the phase's epilogue.
+template <int NB, int RG, int RPU, bool WBF16>
+__device__ __forceinline__ void gemv_group(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
+                                           const uint8_t *buf, int j0, int ng, int c_unit0, int c_kt, int u0,
+                                           float (&best_v)[NB], int (&best_i)[NB]) {
+    constexpr int V = RG * NB;
+    constexpr int SHIFT = 5 - Log2<V>::value;
+    const Model &m = P.m;
+    const int lane = threadIdx.x & 31;
+    const int batch = P.batch;
+    const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
+    const size_t unit_stride = (size_t)RPU * rowbytes;  // the group's units are consecutive
+    float acc[V];
+    rows_dot<NB, RG, RPU, WBF16>(buf + (size_t)j0 * RPU * rowbytes, unit_stride, rowbytes, ng * RPU, S.xs, M.KBp,
+                                 batch, acc);
+    const float val = reduce_scatter<V>(acc);
+    const int idx = lane >> SHIFT;              // value held by this lane
+    const bool holder = (lane & ((1 << SHIFT) - 1)) == 0;
+    const int r = idx / NB, b = idx - r * NB;   // group row, batch row
+    const uint32_t tag = P.tag;
+    if (epi == EPI_W13) {  // rows (2u, 2u + 1) = (gate, up) of group unit u
+        const float up = __shfl_sync(0xffffffffu, val, ((idx + NB) << SHIFT) & 31);
+        const int u = r >> 1;
+        if (holder && (r & 1) == 0 && u < ng && b < batch) {
+            const int unit = u0 + c_unit0 + j0 + u;
+            const float s = val / (1.0f + __expf(-val));
+            ll_store(m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit, s * up, tag);
+        }
+        return;
+    }
+    if (!holder || r >= ng || b >= batch) return;
+    const int i = c_unit0 + j0 + r;  // unit within the CTA's slice
+    const int unit = u0 + i;
+    float v = val;
+    if (M.nkt > 1) {  // accumulate this K tile; finish after the last one
+        float *a = S.accs + (size_t)i * kMaxBatch + b;
+        v = (c_kt == 0 ? 0.f : *a) + v;
+        *a = v;
+        if (c_kt != M.nkt - 1) return;
+    }
+    if (epi == EPI_QKV) {
+        ll_store(m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + unit, v, tag);
+    } else if (epi == EPI_WO || epi == EPI_W2) {
+        float *own = S.xown + b * kMaxOwn + i;
+        const float xn = *own + v;
+        *own = xn;
+        uint64_t *dst = epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim) : m.ll_x + ll_layer(P, layer + 1, m.dim);
+        ll_store(dst + (size_t)b * m.dim + unit, xn, tag);
+    } else {  // logits: rows of one lane's value increase, so a strict > keeps the lowest index
+        if (P.logits) P.logits[(size_t)b * m.vocab + unit] = v;
+        if (v != v) {
+            atomicOr(m.status, kStNanLogits);
+        } else {
+#pragma unroll
+            for (int bb = 0; bb < NB; bb++)
+                if (bb == b && (v > best_v[bb] || (v == best_v[bb] && unit < best_i[bb]))) {
+                    best_v[bb] = v;
+                    best_i[bb] = unit;
+                }
+        }
+    }
+}
+
 template <int NB, bool WBF16>
 __device__ void gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                            uint32_t &chunk_i, float (&best_v)[NB], int (&best_i)[NB], int tslot) {
-    const Model &m = P.m;
-    const int esz = WBF16 ? 2 : 4;
+    constexpr int R = GemvShape<NB>::R;
+    constexpr int RW = R < 2 ? 2 : R;  // W1/W3: whole (gate, up) pairs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int batch = P.batch;
-    const uint32_t tag = P.tag;
     int u0, u1;
     unit_range(M.rows / M.rows_per_unit, P.grid, blockIdx.x, u0, u1);
     trace_mark(P, tslot, 0);
     if (u0 == u1) return;
-    const bool split = M.nkt > 1;
     int cur_kt = -1;
-    for_each_chunk(M, layer, esz, blockIdx.x, P.grid, [&](const Chunk &c) {
+    for_each_chunk(M, layer, WBF16 ? 2 : 4, blockIdx.x, P.grid, [&](const Chunk &c) {
         if (c.kt != cur_kt) {
             stage_input(P, epi, layer, M, c.kt, S);
             if (cur_kt < 0) trace_mark(P, tslot, 1);
             cur_kt = c.kt;
         }
-        const uint32_t slot = chunk_i % kRingSlots, parity = (chunk_i / kRingSlots) & 1;
-        wait_slot(P, &S.full[slot], parity);
-        const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
-        const size_t rowbytes = (size_t)M.KBp * esz;
-        const bool last_tile = c.kt == M.nkt - 1;
-        // unit i of the CTA's slice always belongs to warp i % 8 (accumulators stay put)
-        const int first = (warp - c.unit0 % kComputeWarps + kComputeWarps) % kComputeWarps;
-        for (int j = first; j < c.nunits; j += kComputeWarps) {
-            const int i = c.unit0 + j;          // unit within the CTA's slice
-            const int unit = u0 + i;            // global unit
+        // chunk i belongs to warp i % 8, which double-buffers slots i % 16 and (i + 8) % 16
+        if ((int)(chunk_i % kComputeWarps) == warp) {
+            const uint32_t slot = chunk_i % kRingSlots, parity = (chunk_i / kRingSlots) & 1;
+            wait_slot(P, &S.full[slot], parity);
+            const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
             if (epi == EPI_W13) {
-                float a[NB], g[NB];
-                row_dot<NB, WBF16>(buf + (size_t)(2 * j) * rowbytes, S.xs, M.KBp, batch, a);
-                row_dot<NB, WBF16>(buf + (size_t)(2 * j + 1) * rowbytes, S.xs, M.KBp, batch, g);
-#pragma unroll
-                for (int b = 0; b < NB; b++) {
-                    if (b < batch && lane == b) {
-                        float s = a[b] / (1.0f + __expf(-a[b]));
-                        ll_store(m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit, s * g[b], tag);
-                    }
-                }
-                continue;
+                for (int j = 0; j < c.nunits; j += RW / 2)
+                    gemv_group<NB, RW, 2, WBF16>(P, epi, layer, M, S, buf, j, min(RW / 2, c.nunits - j), c.unit0,
+                                                 c.kt, u0, best_v, best_i);
+            } else {
+                int j = 0;
+                for (; j + R <= c.nunits; j += R)
+                    gemv_group<NB, R, 1, WBF16>(P, epi, layer, M, S, buf, j, R, c.unit0, c.kt, u0, best_v, best_i);
+                for (; j < c.nunits; j++)  // leftover rows one at a time (no idle accumulators)
+                    gemv_group<NB, 1, 1, WBF16>(P, epi, layer, M, S, buf, j, 1, c.unit0, c.kt, u0, best_v, best_i);
             }
-            float acc[NB];
-            row_dot<NB, WBF16>(buf + (size_t)j * rowbytes, S.xs, M.KBp, batch, acc);
-#pragma unroll
-            for (int b = 0; b < NB; b++) {
-                if (b >= batch || lane != b) continue;
-                float v = acc[b];
-                if (split) {  // accumulate this K tile; finish after the last one
-                    float *a = S.accs + (size_t)i * kMaxBatch + b;
-                    v = (c.kt == 0 ? 0.f : *a) + v;
-                    *a = v;
-                    if (!last_tile) continue;
-                }
-                if (epi == EPI_QKV) {
-                    ll_store(m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + unit, v, tag);
-                } else if (epi == EPI_WO || epi == EPI_W2) {
-                    float *own = S.xown + b * kMaxOwn + i;
-                    const float xn = *own + v;
-                    *own = xn;
-                    uint64_t *dst = epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim)
-                                                  : m.ll_x + ll_layer(P, layer + 1, m.dim);
-                    ll_store(dst + (size_t)b * m.dim + unit, xn, tag);
-                } else {  // logits
-                    if (P.logits) P.logits[(size_t)b * m.vocab + unit] = v;
-                    if (v != v)
-                        atomicOr(m.status, kStNanLogits);
-                    else if (v > best_v[b] || (v == best_v[b] && unit < best_i[b])) {
-                        best_v[b] = v;
-                        best_i[b] = unit;
-                    }
-                }
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[slot]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty[slot]);
         chunk_i++;
     });
     trace_mark(P, tslot, 2);
@@ -529,11 +651,23 @@ __device__ void finish_argmax(const StepParams &P, Shared &S, float (&best_v)[NB
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int batch = P.batch;
     compute_sync();  // the logits phase is done with S.xs
+    // each lane holds candidates for some rows: reduce over the warp (lowest index on ties)
 #pragma unroll
     for (int b = 0; b < NB; b++) {
-        if (b < batch && lane == b) {
-            S.wbest_v[warp * kMaxBatch + b] = best_v[b];
-            S.wbest_i[warp * kMaxBatch + b] = best_i[b];
+        float v = best_v[b];
+        int i = best_i[b];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+            const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
+            if (v2 > v || (v2 == v && i2 < i)) {
+                v = v2;
+                i = i2;
+            }
+        }
+        if (b < batch && lane == 0) {
+            S.wbest_v[warp * kMaxBatch + b] = v;
+            S.wbest_i[warp * kMaxBatch + b] = i;
         }
     }
     compute_sync();
@@ -696,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     if (tid == 0) {
         for (int i = 0; i < kRingSlots; i++) {
             mbar_init(&S.full[i], 1);
-            mbar_init(&S.empty[i], kComputeWarps);
+            mbar_init(&S.empty[i], 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }

@@ -103,10 +103,11 @@ static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Choose the K tiling of a [rows][K] matrix: one tile when the fp32 activation tile of
 // every batch row fits in shared memory and a unit of rows fits in one ring slot;
-// otherwise split K (only for residual-add epilogues, where split-K partial sums can be
-// accumulated).
+// otherwise split K (only for residual-add epilogues, where the tiles' partial sums are
+// accumulated).  A chunk (one warp's piece of work) holds whole units: enough that a
+// CTA's share splits into about one chunk per warp or more, at most one slot.
 static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int max_batch,
-                     bool allow_split) {
+                     bool allow_split, int grid) {
     for (int nkt = 1; nkt <= 64; nkt++) {
         int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), kPadElems);
         int real_nkt = (K + KB - 1) / KB;
@@ -121,9 +122,11 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
             M.nkt = real_nkt;
             M.rows_per_unit = rows_per_unit;
             M.units = real_nkt * (rows / rows_per_unit);
-            int rpc = (int)(kChunkBytes / ((size_t)KB * esz));
-            rpc = rpc / rows_per_unit * rows_per_unit;
-            M.rows_per_chunk = std::max(rpc, rows_per_unit);
+            const int units = rows / rows_per_unit;
+            const int per_cta = (units + grid - 1) / grid;
+            const int fit = (int)(kChunkBytes / unit_bytes);
+            const int upc = std::max(1, std::min(fit, (per_cta + kComputeWarps - 1) / kComputeWarps));
+            M.rows_per_chunk = upc * rows_per_unit;
             M.layer_stride = (long long)real_nkt * rows * KB * esz;
             return true;
         }
@@ -169,6 +172,11 @@ static bool config_ok(const slm_config *c, std::string &why) {
     }
     if (c->n_heads % c->n_kv_heads) {
         why = "n_heads must be a multiple of n_kv_heads";
+        return false;
+    }
+    if (c->dim % 4) {
+        snprintf(buf, sizeof buf, "dim %d must be a multiple of 4", c->dim);
+        why = buf;
         return false;
     }
     if (c->head_dim % 8 || c->head_dim > 256) {
@@ -264,12 +272,6 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     m.norm_eps = cfg->norm_eps;
     m.weight_bf16 = cfg->weight_dtype == SLM_BF16;
     m.kv_bf16 = cfg->kv_dtype == SLM_BF16;
-    if (!plan_mat(m.emb, V, dim, 1, esz, B, false) || !plan_mat(m.qkv, qkv_rows, dim, 1, esz, B, false) ||
-        !plan_mat(m.wo, dim, qd, 1, esz, B, true) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false) ||
-        !plan_mat(m.w2, dim, hid, 1, esz, B, true))
-        return fail(c, SLM_EUNSUPPORTED,
-                    "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
-    m.emb.layer_stride = 0;
 
     // shared-memory limits of the decode kernel
     c->smem = decode_smem_bytes();
@@ -277,6 +279,13 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     CK(c, decode_occupancy(m.weight_bf16, &per_sm));
     if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
     c->grid = sms * per_sm;
+    const int grid = c->grid;
+    if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) || !plan_mat(m.qkv, qkv_rows, dim, 1, esz, B, false, grid) ||
+        !plan_mat(m.wo, dim, qd, 1, esz, B, true, grid) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, grid) ||
+        !plan_mat(m.w2, dim, hid, 1, esz, B, true, grid))
+        return fail(c, SLM_EUNSUPPORTED,
+                    "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
+    m.emb.layer_stride = 0;
     if ((dim + c->grid - 1) / c->grid > kMaxOwn)
         return fail(c, SLM_EUNSUPPORTED, "dim %d too large for %d CTAs", dim, c->grid);
     {
@@ -285,6 +294,9 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
                       kAttnStageBytes;
         if (attn > kXsBudget) return fail(c, SLM_EUNSUPPORTED, "attention scratch of %zu B too large", attn);
         if ((size_t)B * c->grid * 2 * 4 > kXsBudget) return fail(c, SLM_EUNSUPPORTED, "argmax scratch too large");
+        for (const Mat *M : {&m.emb, &m.qkv, &m.w13})
+            if (((size_t)B * M->KBp + dim) * 4 > kXsBudget)
+                return fail(c, SLM_EUNSUPPORTED, "activation tile plus gains too large for shared memory");
     }
 
     // ---- weights: repack on the host, then one copy to the device

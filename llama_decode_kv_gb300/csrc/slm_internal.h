@@ -13,15 +13,16 @@ namespace slm {
 constexpr int kComputeWarps = 8;                      // warps that do the arithmetic
 constexpr int kThreads = (kComputeWarps + 1) * 32;     // + one weight-streaming warp
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kRingSlots = 6;                         // weight ring depth per CTA
-constexpr int kChunkBytes = 16384;                    // one ring slot
+constexpr int kRingSlots = 16;                        // weight ring depth per CTA (2 per warp)
+constexpr int kChunkBytes = 8192;                     // one ring slot = one warp's chunk
+constexpr long long kL2Lookahead = 192 * 1024;        // weight bytes prefetched into L2 ahead
 constexpr int kMaxBatch = 16;
 constexpr int kMaxGroupPass = 4;                      // query heads per attention pass
 constexpr int kMaxChunksPerSeq = 64;                  // split-K chunks per (row, kv head)
 constexpr int kMaxChunksA = 16;                       // chunks when consumers merge them
 constexpr int kMinAttnChunk = 32;                     // positions
-constexpr size_t kXsBudget = 112 * 1024;              // activation tile in shared memory
-constexpr size_t kAttnStageBytes = 64 * 1024;         // K + V chunk copy in shared memory
+constexpr size_t kXsBudget = 80 * 1024;               // activation tile in shared memory
+constexpr size_t kAttnStageBytes = 48 * 1024;         // K + V chunk copy in shared memory
 constexpr int kMaxOwn = 64;                           // residual rows one CTA may own
 constexpr int kPadElems = 8;                          // K tiles are padded to 8 elements
 

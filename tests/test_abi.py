@@ -39,6 +39,7 @@ def _cfg(**kw):
 
 @pytest.mark.parametrize("kw,why", [
     (dict(n_kv_heads=3), "multiple"),
+    (dict(dim=66), "dim 66"),
     (dict(head_dim=12), "head_dim"),
     (dict(head_dim=0), "positive"),
     (dict(max_batch=17), "max_batch"),
