@@ -40,34 +40,34 @@ namespace slm {
 // ------------------------------------------------------------------ shared memory
 
 struct Shared {
-    uint8_t *ring;      // [kRingSlots][kChunkBytes]
-    uint64_t *full;     // [kRingSlots]
-    uint64_t *empty;    // [kRingSlots]
+    uint64_t *full;     // [kMaxRingSlots]
+    uint64_t *empty;    // [kMaxRingSlots]
     float *rs;          // [kMaxBatch] 1 / rms
     float *wbest_v;     // [kComputeWarps][kMaxBatch]
     int *wbest_i;       // [kComputeWarps][kMaxBatch]
     int *flags;         // [4]: 0 = last-arriver flag
     float *xown;        // [kMaxBatch][kMaxOwn] residual rows this CTA owns
     float *accs;        // [kMaxOwn][kMaxBatch] accumulators across K tiles
-    float *xs;          // activation tile / attention scratch, kXsBudget bytes
+    float *xs;          // activation tile / attention scratch, P.xs_bytes
+    uint8_t *ring;      // [P.ring_slots][kChunkBytes]
 };
 
-constexpr int kRingBytes = kRingSlots * kChunkBytes;
-constexpr int kMiscBytes = 2 * kRingSlots * 8 + kMaxBatch * 4 + 2 * kComputeWarps * kMaxBatch * 4 + 16;
-constexpr int kOwnOffset = ((kRingBytes + kMiscBytes + 127) / 128) * 128;
+// Layout: barriers and small arrays, owned residual rows, K-tile accumulators, the
+// activation tile, then the weight ring (sized at create time from what is left).
+constexpr int kMiscBytes = 2 * kMaxRingSlots * 8 + kMaxBatch * 4 + 2 * kComputeWarps * kMaxBatch * 4 + 16;
+constexpr int kOwnOffset = ((kMiscBytes + 127) / 128) * 128;
 constexpr int kAccOffset = kOwnOffset + kMaxBatch * kMaxOwn * 4;
 constexpr int kXsOffset = kAccOffset + kMaxOwn * kMaxBatch * 4;
-constexpr int kSmemBytes = kXsOffset + (int)kXsBudget;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-__device__ __forceinline__ Shared carve(uint8_t *base) {
+__host__ __device__ inline size_t ring_offset(int xs_bytes) { return ((size_t)kXsOffset + xs_bytes + 1023) / 1024 * 1024; }
+
+__device__ __forceinline__ Shared carve(uint8_t *base, const StepParams &P) {
     Shared s;
-    s.ring = base;
-    uint8_t *p = base + kRingBytes;
+    uint8_t *p = base;
     s.full = (uint64_t *)p;
-    p += kRingSlots * 8;
+    p += kMaxRingSlots * 8;
     s.empty = (uint64_t *)p;
-    p += kRingSlots * 8;
+    p += kMaxRingSlots * 8;
     s.rs = (float *)p;
     p += kMaxBatch * 4;
     s.wbest_v = (float *)p;
@@ -78,6 +78,7 @@ __device__ __forceinline__ Shared carve(uint8_t *base) {
     s.xown = (float *)(base + kOwnOffset);
     s.accs = (float *)(base + kAccOffset);
     s.xs = (float *)(base + kXsOffset);
+    s.ring = base + ring_offset(P.xs_bytes);
     return s;
 }
 
@@ -267,24 +268,17 @@ __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
     return false;
 }
 
-// Copies this CTA's chunks into the ring, and keeps up to kL2Lookahead bytes of the
-// chunks after them on their way into L2, so that ring refills hit L2 rather than HBM.
+// Copies this CTA's chunks into the ring, in the order the compute warps use them.
 __device__ void producer(const StepParams &P, Shared &S) {
-    Cursor ic, pc;
+    const uint32_t slots = (uint32_t)P.ring_slots;
+    Cursor ic;
     cursor_init(P, ic);
-    cursor_init(P, pc);
-    long long ahead = 0;  // bytes prefetched into L2 and not yet copied into the ring
     uint32_t issued = 0;
-    Chunk c, q;
+    Chunk c;
     while (cursor_next(P, ic, c)) {
-        while (ahead < kL2Lookahead && cursor_next(P, pc, q)) {
-            bulk_prefetch_l2(q.src, q.bytes);
-            ahead += q.bytes;
-        }
-        ahead -= c.bytes;
-        const uint32_t slot = issued % kRingSlots;
-        if (issued >= (uint32_t)kRingSlots) {
-            const uint32_t parity = ((issued / kRingSlots) - 1) & 1;
+        const uint32_t slot = issued % slots;
+        if (issued >= slots) {
+            const uint32_t parity = ((issued / slots) - 1) & 1;
             if (!wait_slot(P, &S.empty[slot], parity)) break;
         }
         mbar_expect_tx(&S.full[slot], c.bytes);
@@ -293,9 +287,9 @@ __device__ void producer(const StepParams &P, Shared &S) {
     }
     // Never leave with a copy in flight: wait (bounded, ignoring the abort flag) for the
     // completion of every slot that may still be filling.
-    uint32_t first = issued > (uint32_t)kRingSlots ? issued - kRingSlots : 0;
+    uint32_t first = issued > slots ? issued - slots : 0;
     for (uint32_t i = first; i < issued; i++) {
-        uint32_t slot = i % kRingSlots, parity = (i / kRingSlots) & 1;
+        uint32_t slot = i % slots, parity = (i / slots) & 1;
         unsigned long long t0 = global_ns();
         while (!mbar_try_wait(&S.full[slot], parity)) {
             if (global_ns() - t0 > kWaitLimitNs) {
@@ -492,49 +486,85 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[V]) {
     return v[0];
 }
 
+// Independent accumulator chains per (row, batch row): enough to keep the FMA pipe and
+// the shared-memory loads busy with two warps per scheduler.
+template <int NB, int RG> struct Unroll {
+    static constexpr int value = RG * NB >= 8 ? 1 : RG * NB >= 4 ? 2 : 4;
+};
+
 // Dots of RG weight rows with every staged batch row.  Group row r lives at
 // base + (r / RPU) * unit_stride + (r % RPU) * rowbytes; rows r >= nr are skipped.
-// Value index r * NB + b.
+// Value index r * NB + b.  Pieces are taken U at a time into U separate accumulators.
 template <int NB, int RG, int RPU, bool WBF16>
 __device__ __forceinline__ void rows_dot(const uint8_t *base, size_t unit_stride, size_t rowbytes, int nr,
-                                         const float *xs, int KBp, int batch, float (&acc)[RG * NB]) {
-    const int lane = threadIdx.x & 31;
+                                         const float *xs, int KBp, int batch, float (&out)[RG * NB]) {
+    constexpr int U = Unroll<NB, RG>::value;
     constexpr int EPP = WBF16 ? 8 : 4;
+    const int lane = threadIdx.x & 31;
     const int pieces = KBp / EPP;
+    float acc[U][RG * NB];
 #pragma unroll
-    for (int v = 0; v < RG * NB; v++) acc[v] = 0.f;
-    for (int p = lane; p < pieces; p += 32) {
-        float wf[RG][EPP];
+    for (int u = 0; u < U; u++)
 #pragma unroll
-        for (int r = 0; r < RG; r++) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (r < nr) w = ((const uint4 *)(base + (size_t)(r / RPU) * unit_stride + (size_t)(r % RPU) * rowbytes))[p];
-            if constexpr (WBF16) {
-                wf[r][0] = bf16_lo(w.x); wf[r][1] = bf16_hi(w.x); wf[r][2] = bf16_lo(w.y); wf[r][3] = bf16_hi(w.y);
-                wf[r][4] = bf16_lo(w.z); wf[r][5] = bf16_hi(w.z); wf[r][6] = bf16_lo(w.w); wf[r][7] = bf16_hi(w.w);
-            } else {
-                wf[r][0] = __uint_as_float(w.x); wf[r][1] = __uint_as_float(w.y);
-                wf[r][2] = __uint_as_float(w.z); wf[r][3] = __uint_as_float(w.w);
-            }
-        }
+        for (int v = 0; v < RG * NB; v++) acc[u][v] = 0.f;
+    const uint4 *rows[RG];
 #pragma unroll
-        for (int b = 0; b < NB; b++) {
-            if (NB > 1 && b >= batch) break;
-            float x[EPP];
-            if constexpr (WBF16) {
-                const float *xr = xs + (size_t)b * KBp + p * 4;  // planes of xpos()
-                const float4 x0 = *(const float4 *)xr, x1 = *(const float4 *)(xr + (KBp >> 1));
-                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-            } else {
-                const float4 x0 = *(const float4 *)(xs + (size_t)b * KBp + p * 4);
-                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-            }
+    for (int r = 0; r < RG; r++)
+        rows[r] = (const uint4 *)(base + (size_t)((r < nr ? r : 0) / RPU) * unit_stride +
+                                  (size_t)((r < nr ? r : 0) % RPU) * rowbytes);
+    for (int p0 = lane; p0 < pieces; p0 += 32 * U) {
+        uint4 w[U][RG];
+#pragma unroll
+        for (int u = 0; u < U; u++)
 #pragma unroll
             for (int r = 0; r < RG; r++)
+                w[u][r] = (p0 + 32 * u < pieces && r < nr) ? rows[r][p0 + 32 * u] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int e = 0; e < EPP; e++) acc[r * NB + b] = fmaf(wf[r][e], x[e], acc[r * NB + b]);
+        for (int u = 0; u < U; u++) {
+            const int p = p0 + 32 * u;
+            if (p >= pieces) break;
+#pragma unroll
+            for (int b = 0; b < NB; b++) {
+                if (NB > 1 && b >= batch) break;
+                float x[EPP];
+                if constexpr (WBF16) {
+                    const float *xr = xs + (size_t)b * KBp + p * 4;  // planes of xpos()
+                    const float4 x0 = *(const float4 *)xr, x1 = *(const float4 *)(xr + (KBp >> 1));
+                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                    x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+                } else {
+                    const float4 x0 = *(const float4 *)(xs + (size_t)b * KBp + p * 4);
+                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                }
+#pragma unroll
+                for (int r = 0; r < RG; r++) {
+                    const uint4 q = w[u][r];
+                    float &a = acc[u][r * NB + b];
+                    if constexpr (WBF16) {
+                        a = fmaf(bf16_lo(q.x), x[0], a);
+                        a = fmaf(bf16_hi(q.x), x[1], a);
+                        a = fmaf(bf16_lo(q.y), x[2], a);
+                        a = fmaf(bf16_hi(q.y), x[3], a);
+                        a = fmaf(bf16_lo(q.z), x[4], a);
+                        a = fmaf(bf16_hi(q.z), x[5], a);
+                        a = fmaf(bf16_lo(q.w), x[6], a);
+                        a = fmaf(bf16_hi(q.w), x[7], a);
+                    } else {
+                        a = fmaf(__uint_as_float(q.x), x[0], a);
+                        a = fmaf(__uint_as_float(q.y), x[1], a);
+                        a = fmaf(__uint_as_float(q.z), x[2], a);
+                        a = fmaf(__uint_as_float(q.w), x[3], a);
+                    }
+                }
+            }
         }
+    }
+#pragma unroll
+    for (int v = 0; v < RG * NB; v++) {
+        float t = acc[0][v];
+#pragma unroll
+        for (int u = 1; u < U; u++) t += acc[u][v];
+        out[v] = t;
     }
 }
 
@@ -620,20 +650,25 @@ __device__ void gemv_phase(const StepParams &P, int epi, int layer, const Mat &M
             if (cur_kt < 0) trace_mark(P, tslot, 1);
             cur_kt = c.kt;
         }
-        // chunk i belongs to warp i % 8, which double-buffers slots i % 16 and (i + 8) % 16
+        // chunk i belongs to warp i % 8; with a multiple of 8 slots every use of a slot
+        // belongs to the same warp, which takes them in order
         if ((int)(chunk_i % kComputeWarps) == warp) {
-            const uint32_t slot = chunk_i % kRingSlots, parity = (chunk_i / kRingSlots) & 1;
+            const uint32_t slot = chunk_i % (uint32_t)P.ring_slots, parity = (chunk_i / (uint32_t)P.ring_slots) & 1;
             wait_slot(P, &S.full[slot], parity);
             const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
             if (epi == EPI_W13) {
                 for (int j = 0; j < c.nunits; j += RW / 2)
                     gemv_group<NB, RW, 2, WBF16>(P, epi, layer, M, S, buf, j, min(RW / 2, c.nunits - j), c.unit0,
                                                  c.kt, u0, best_v, best_i);
-            } else {
+            } else {  // groups of R rows, then of 2, then single rows: no idle accumulators
                 int j = 0;
                 for (; j + R <= c.nunits; j += R)
                     gemv_group<NB, R, 1, WBF16>(P, epi, layer, M, S, buf, j, R, c.unit0, c.kt, u0, best_v, best_i);
-                for (; j < c.nunits; j++)  // leftover rows one at a time (no idle accumulators)
+                if constexpr (R > 2) {
+                    for (; j + 2 <= c.nunits; j += 2)
+                        gemv_group<NB, 2, 1, WBF16>(P, epi, layer, M, S, buf, j, 2, c.unit0, c.kt, u0, best_v, best_i);
+                }
+                for (; j < c.nunits; j++)
                     gemv_group<NB, 1, 1, WBF16>(P, epi, layer, M, S, buf, j, 1, c.unit0, c.kt, u0, best_v, best_i);
             }
             __syncwarp();
@@ -731,7 +766,7 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
     float *raw = S.xs + kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2);
     uint8_t *kst = (uint8_t *)(raw + (size_t)(G + 2) * hd);
     const int tc = appends ? pos : t1;  // cached positions [t0, tc) of this chunk
-    const bool stage = (size_t)(t1 - t0) * rowbytes * 2 <= kAttnStageBytes;
+    const bool stage = (size_t)(t1 - t0) * rowbytes * 2 <= (size_t)P.attn_stage_bytes;
     uint8_t *vst = kst + (size_t)(t1 - t0) * rowbytes;
     compute_sync();  // the previous item is done with the scratch
     if (stage) {
@@ -825,10 +860,10 @@ __device__ void attention_phase(const StepParams &P, int layer, Shared &S) {
 template <int NB, bool WBF16>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    Shared S = carve(smem_raw);
+    Shared S = carve(smem_raw, P);
     const int tid = threadIdx.x;
     if (tid == 0) {
-        for (int i = 0; i < kRingSlots; i++) {
+        for (int i = 0; i < P.ring_slots; i++) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], 1);
         }
@@ -871,15 +906,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
 // ------------------------------------------------------------------ host-side launch
 
-size_t decode_smem_bytes() { return (size_t)kSmemBytes; }
+size_t decode_smem_bytes(int xs_bytes, int ring_slots) {
+    return ring_offset(xs_bytes) + (size_t)ring_slots * kChunkBytes;
+}
 
 template <int NB, bool WBF16>
 static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
     auto fn = decode_step_kernel<NB, WBF16>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const size_t smem = decode_smem_bytes(P.xs_bytes, P.ring_slots);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void *args[] = {(void *)&P};
-    return cudaLaunchCooperativeKernel((const void *)fn, dim3(P.grid), dim3(kThreads), args, kSmemBytes, stream);
+    return cudaLaunchCooperativeKernel((const void *)fn, dim3(P.grid), dim3(kThreads), args, smem, stream);
 }
 
 template <bool WBF16>
@@ -894,11 +932,11 @@ cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream) {
     return P.m.weight_bf16 ? launch_w<true>(P, stream) : launch_w<false>(P, stream);
 }
 
-cudaError_t decode_occupancy(int weight_bf16, int *blocks_per_sm) {
+cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm) {
     auto fn = weight_bf16 ? decode_step_kernel<1, true> : decode_step_kernel<1, false>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kThreads, kSmemBytes);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kThreads, smem);
 }
 
 }  // namespace slm

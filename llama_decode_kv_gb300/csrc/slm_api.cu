@@ -21,8 +21,8 @@
 
 namespace slm {
 cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream);
-cudaError_t decode_occupancy(int weight_bf16, int *blocks_per_sm);
-size_t decode_smem_bytes();
+cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm);
+size_t decode_smem_bytes(int xs_bytes, int ring_slots);
 }  // namespace slm
 
 using namespace slm;
@@ -32,6 +32,7 @@ struct slm_ctx {
     int device = 0;
     int grid = 0;
     size_t smem = 0;
+    int ring_slots = 0, xs_bytes = 0, attn_stage = 0;
     Model m{};
     std::vector<void *> allocs;
     std::vector<int> len;
@@ -273,12 +274,10 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     m.weight_bf16 = cfg->weight_dtype == SLM_BF16;
     m.kv_bf16 = cfg->kv_dtype == SLM_BF16;
 
-    // shared-memory limits of the decode kernel
-    c->smem = decode_smem_bytes();
-    int per_sm = 0;
-    CK(c, decode_occupancy(m.weight_bf16, &per_sm));
-    if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
-    c->grid = sms * per_sm;
+    // Shared memory of the decode kernel: the activation tile / attention scratch region
+    // takes what this shape needs, the weight ring (8 KB slots, a multiple of 8, at
+    // least 16) takes the rest.  The grid is one CTA per SM.
+    c->grid = sms;
     const int grid = c->grid;
     if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) || !plan_mat(m.qkv, qkv_rows, dim, 1, esz, B, false, grid) ||
         !plan_mat(m.wo, dim, qd, 1, esz, B, true, grid) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, grid) ||
@@ -286,18 +285,28 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         return fail(c, SLM_EUNSUPPORTED,
                     "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
     m.emb.layer_stride = 0;
-    if ((dim + c->grid - 1) / c->grid > kMaxOwn)
-        return fail(c, SLM_EUNSUPPORTED, "dim %d too large for %d CTAs", dim, c->grid);
+    if ((dim + grid - 1) / grid > kMaxOwn) return fail(c, SLM_EUNSUPPORTED, "dim %d too large for %d CTAs", dim, grid);
     {
         const int G = H / KV;
-        size_t attn = (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) + (G + 2) * hd) * 4 +
-                      kAttnStageBytes;
-        if (attn > kXsBudget) return fail(c, SLM_EUNSUPPORTED, "attention scratch of %zu B too large", attn);
-        if ((size_t)B * c->grid * 2 * 4 > kXsBudget) return fail(c, SLM_EUNSUPPORTED, "argmax scratch too large");
-        for (const Mat *M : {&m.emb, &m.qkv, &m.w13})
-            if (((size_t)B * M->KBp + dim) * 4 > kXsBudget)
-                return fail(c, SLM_EUNSUPPORTED, "activation tile plus gains too large for shared memory");
+        size_t need = 0;
+        for (const Mat *M : {&m.emb, &m.qkv, &m.w13}) need = std::max(need, ((size_t)B * M->KBp + dim) * 4);
+        for (const Mat *M : {&m.wo, &m.w2}) need = std::max(need, (size_t)B * M->KBp * 4);
+        c->attn_stage = B <= 2 ? 16 * 1024 : 32 * 1024;
+        need = std::max(need, (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) + (G + 2) * hd) * 4 +
+                                  c->attn_stage);
+        need = std::max(need, (size_t)B * grid * 2 * 4);  // argmax candidates
+        c->xs_bytes = (int)round_up(need, 1024);
+        const size_t base = decode_smem_bytes(c->xs_bytes, 0);
+        int slots = base < kSmemLimit ? (int)((kSmemLimit - base) / kChunkBytes) : 0;
+        slots = std::min(kMaxRingSlots, slots / 8 * 8);
+        if (slots < kMinRingSlots)
+            return fail(c, SLM_EUNSUPPORTED, "shared memory too small: %zu B of scratch leaves %d ring slots", need, slots);
+        c->ring_slots = slots;
+        c->smem = decode_smem_bytes(c->xs_bytes, slots);
     }
+    int per_sm = 0;
+    CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
+    if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
 
     // ---- weights: repack on the host, then one copy to the device
     std::vector<uint8_t> src;
@@ -459,9 +468,12 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
     ch = std::max<long long>(ch, (max_ctx + kMaxChunksPerSeq - 1) / kMaxChunksPerSeq);
     ch = (ch + 31) / 32 * 32;
     // consumer merge: batch * (KBp(Wo) + H * nc * (hd + 2)) floats must fit the tile
-    const long long tile = (long long)(kXsBudget / 4) / P.batch - m.wo.KBp;
+    const long long tile = (long long)(c->xs_bytes / 4) / P.batch - m.wo.KBp;
     long long nc_fit = tile > 0 ? tile / ((long long)H * (hd + 2)) : 0;
     nc_fit = std::min<long long>(nc_fit, kMaxChunksA);
+    // consumers poll batch * H * nc * (hd + 2) words: beyond ~8K words the polling rounds
+    // cost more than letting the last CTA of each (row, kv head) merge
+    nc_fit = std::min<long long>(nc_fit, 8192 / ((long long)P.batch * H * (hd + 2)));
     P.attn_consumer_merge = 0;
     if (nc_fit >= 1) {
         long long ch_a = std::max<long long>(ch, (max_ctx + nc_fit - 1) / nc_fit);
@@ -485,6 +497,9 @@ static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
     if (++c->launch_seq == 0) c->launch_seq = 1;  // tag 0 marks never-written words
     P.tag = c->launch_seq;
     P.trace = c->trace_on ? c->d_trace : nullptr;
+    P.ring_slots = c->ring_slots;
+    P.xs_bytes = c->xs_bytes;
+    P.attn_stage_bytes = c->attn_stage;
     plan_attention(c, P);
     cudaError_t e = launch_decode_step(P, s);
     if (e != cudaSuccess) {

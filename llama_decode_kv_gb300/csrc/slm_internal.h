@@ -13,17 +13,17 @@ namespace slm {
 constexpr int kComputeWarps = 8;                      // warps that do the arithmetic
 constexpr int kThreads = (kComputeWarps + 1) * 32;     // + one weight-streaming warp
 constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kRingSlots = 16;                        // weight ring depth per CTA (2 per warp)
+constexpr int kMaxRingSlots = 32;                     // weight ring depth per CTA (a multiple
+constexpr int kMinRingSlots = 16;                     //   of 8: slot s is always warp s % 8's)
 constexpr int kChunkBytes = 8192;                     // one ring slot = one warp's chunk
-constexpr long long kL2Lookahead = 192 * 1024;        // weight bytes prefetched into L2 ahead
 constexpr int kMaxBatch = 16;
 constexpr int kMaxGroupPass = 4;                      // query heads per attention pass
 constexpr int kMaxChunksPerSeq = 64;                  // split-K chunks per (row, kv head)
 constexpr int kMaxChunksA = 16;                       // chunks when consumers merge them
 constexpr int kMinAttnChunk = 32;                     // positions
-constexpr size_t kXsBudget = 80 * 1024;               // activation tile in shared memory
-constexpr size_t kAttnStageBytes = 48 * 1024;         // K + V chunk copy in shared memory
-constexpr int kMaxOwn = 64;                           // residual rows one CTA may own
+constexpr size_t kXsBudget = 88 * 1024;               // activation tile, at most (16-slot ring)
+constexpr size_t kSmemLimit = 227 * 1024;             // dynamic shared memory per CTA
+constexpr int kMaxOwn = 32;                           // residual rows one CTA may own
 constexpr int kPadElems = 8;                          // K tiles are padded to 8 elements
 
 // status word bits (device side)
@@ -93,6 +93,9 @@ struct StepParams {
     int do_logits;                  // 0: skip the vocabulary projection (prefill)
     uint32_t tag;                   // this launch's exchange tag (never 0)
     int grid;
+    int ring_slots;                 // weight ring depth (multiple of 8)
+    int xs_bytes;                   // activation tile / scratch region
+    int attn_stage_bytes;           // K + V chunk copy budget within it
     unsigned long long *trace;      // null, or [grid][trace_slots][3] phase timestamps
 };
 

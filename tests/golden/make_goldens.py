@@ -1,16 +1,19 @@
-"""Write the oracle's expected values for the Llama-3.2-1B-shaped workload.
+"""Write the oracle's expected values for the large workloads.
 
-The single-threaded fp32 oracle needs about 2 s per token position at this shape, so a
-2048-token prompt plus 256 greedy decode steps takes over an hour per row: too slow to
-recompute inside a test.  This script runs it once per row (rows in parallel, spawned
-processes) and stores, for the prefill's last position and for every decode step:
+The single-threaded fp32 oracle needs about 1 s per token position at the Llama-3.2-1B
+shape (0.2 s at the SmolLM2 shape), so a 2048-token prompt plus 256 greedy decode steps
+takes about half an hour per row: too slow to recompute inside a test.  This script runs
+it once per row (rows in parallel, spawned processes) and stores, for the prefill's last
+position and for every decode step:
 the oracle's greedy id, its top-2 logit gap, max|logit|, its 8 largest logits with their
 indices, and the logits at 64 fixed vocabulary indices.  It calls only `oracle` and
 `synth`.  The first 2048 tokens of the long-context workload's row 0 equal this row 0
 prompt (the prompt generator draws sequentially), so the same file also pins that
 workload's prefix.
 
-Usage: python tests/golden/make_llama1b_goldens.py [rows...]   (default rows 0 1)
+Usage: python tests/golden/make_goldens.py WORKLOAD [rows...]
+  llama1b_b8 0 1   -> llama1b_row0.npz, llama1b_row1.npz (also the llama1b_b1 row 0)
+  smol_b16 0 7 15  -> smol_b16_row{0,7,15}.npz
 """
 import multiprocessing as mp
 import os
@@ -25,7 +28,7 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-WORKLOAD = "llama1b_b8"
+PREFIX = {"llama1b_b8": "llama1b", "smol_b16": "smol_b16"}
 SAMPLE_SEED = 4242
 N_SAMPLE = 64
 TOPK = 8
@@ -35,9 +38,10 @@ def sample_indices(vocab):
     return np.sort(np.random.default_rng(SAMPLE_SEED).choice(vocab, N_SAMPLE, replace=False)).astype(np.int32)
 
 
-def run_row(row):
+def run_row(args):
+    workload, row = args
     import oracle
-    wl = synth.WORKLOADS[WORKLOAD]
+    wl = synth.WORKLOADS[workload]
     s = wl.shape.replace(max_batch=1)
     W = synth.make_weights(s)
     prompt = synth.make_prompt(s, row, wl.prompt_len)
@@ -69,13 +73,14 @@ def run_row(row):
     res["sample_idx"] = idx
     res["weights_sha256"] = np.array(synth.digest(W))
     res["prompt"] = prompt
-    path = os.path.join(HERE, f"llama1b_row{row}.npz")
+    path = os.path.join(HERE, f"{PREFIX[workload]}_row{row}.npz")
     np.savez_compressed(path, **res)
     return path
 
 
 if __name__ == "__main__":
-    rows = [int(r) for r in sys.argv[1:]] or [0, 1]
+    workload = sys.argv[1]
+    rows = [int(r) for r in sys.argv[2:]] or [0]
     with mp.get_context("spawn").Pool(len(rows)) as pool:
-        for p in pool.map(run_row, rows):
+        for p in pool.map(run_row, [(workload, r) for r in rows]):
             print("wrote", p)

@@ -1,0 +1,131 @@
+"""The full-size workloads on the GPU against the oracle's stored values.
+
+The oracle needs too long at these sizes to run inside a test (about half an hour per
+Llama-3.2-1B-shaped row), so `tests/golden/make_goldens.py` (which calls only the
+oracle) stored, per checked row and step, the greedy id, the top-2 gap, max|logit|, the
+top-8 logits and the logits at 64 fixed vocabulary indices.  The GPU runs the whole
+workload -- every row of the batch, full prompt, every decode step, in the launch
+configuration the benchmark uses -- with the checked rows fed the oracle's ids (teacher
+forcing) and the others their own, and is compared on those stored values:
+logits within tol * max|logit| (tol 2e-2: bf16 KV cache), ids equal wherever the
+oracle's top-2 gap exceeds 1e-2.
+"""
+import functools
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+GAP = 1e-2
+
+
+@pytest.fixture(scope="module")
+def slm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import llama_decode_kv_gb300 as m
+    return m
+
+
+@functools.lru_cache(maxsize=2)
+def weights_for(kind: str):
+    shape = synth.SMOL if kind == "smol" else synth.LLAMA1B
+    return synth.make_weights(shape)
+
+
+def golden(prefix, row):
+    path = os.path.join(GOLDEN, f"{prefix}_row{row}.npz")
+    if not os.path.exists(path):
+        pytest.fail(f"missing {path}: run tests/golden/make_goldens.py")
+    return dict(np.load(path))
+
+
+def check_step(gpu_logits_sampled, gpu_top_vals, gpu_id, g, s, tol, what):
+    """gpu_logits_sampled: GPU logits at g['sample_idx']; gpu_top_vals: GPU logits at the
+    oracle's top-8 indices."""
+    scale = float(g["maxabs"][s])
+    err = max(float(np.abs(gpu_logits_sampled - g["sampled"][s]).max()),
+              float(np.abs(gpu_top_vals - g["top_val"][s]).max()))
+    assert err <= tol * scale, f"{what}: max|d logit| {err:.3e} > {tol} * {scale:.3e}"
+    want = int(g["ids"][s])
+    if g["gap"][s] > GAP:
+        assert gpu_id == want, f"{what}: id {gpu_id} != oracle {want} (gap {g['gap'][s]:.3g})"
+    else:
+        top = list(g["top_idx"][s])
+        ok = (gpu_id in top and g["top_val"][s][top.index(gpu_id)] >= g["top_val"][s][0] - GAP) or \
+             (gpu_id not in top and g["top_val"][s][-1] >= g["top_val"][s][0] - GAP)
+        assert ok, f"{what}: id {gpu_id} is not within the gap of the oracle's best"
+    return err / scale
+
+
+def run_workload(slm, wl, kind, prefix, checked_rows, shape=None):
+    s = shape or wl.shape
+    W = weights_for(kind)
+    gold = {r: golden(prefix, r) for r in checked_rows}
+    for r, g in gold.items():
+        assert str(g["weights_sha256"]) == synth.digest(W), "synthetic weights differ from the golden run's"
+    prompts = [synth.make_prompt(s, r, wl.prompt_len) for r in range(wl.batch)]
+    for r, g in gold.items():
+        assert np.array_equal(g["prompt"][: wl.prompt_len], prompts[r])
+    eng = slm.Engine(s, W)
+    dev = torch.device("cuda")
+    worst = 0.0
+    cur = {}
+    sidx = {r: torch.as_tensor(gold[r]["sample_idx"], device=dev, dtype=torch.long) for r in gold}
+    tidx = {r: torch.as_tensor(gold[r]["top_idx"], device=dev, dtype=torch.long) for r in gold}
+    for r in range(wl.batch):
+        lg, nid = eng.prefill_checked(r, prompts[r], want_logits=r in gold)
+        g_id = int(nid.item())
+        if r in gold:
+            worst = max(worst, check_step(lg[sidx[r]].cpu().numpy(), lg[tidx[r][0]].cpu().numpy(), g_id,
+                                          gold[r], 0, 2e-2, f"{prefix} row {r} prefill"))
+            cur[r] = int(gold[r]["ids"][0])
+        else:
+            cur[r] = g_id
+    seqs = list(range(wl.batch))
+    for step in range(wl.decode_steps):
+        toks = torch.tensor([cur[r] for r in seqs], dtype=torch.int32, device=dev)
+        lg, ids = eng.decode_checked(seqs, toks, [wl.prompt_len + step] * wl.batch, want_logits=True)
+        ids_h = ids.cpu().numpy()
+        for i, r in enumerate(seqs):
+            if r in gold:
+                worst = max(worst, check_step(lg[i][sidx[r]].cpu().numpy(), lg[i][tidx[r][step + 1]].cpu().numpy(),
+                                              int(ids_h[i]), gold[r], step + 1, 2e-2,
+                                              f"{prefix} row {r} step {step}"))
+                cur[r] = int(gold[r]["ids"][step + 1])
+            else:
+                cur[r] = int(ids_h[i])
+    assert eng.sync() == 0, eng.last_error()
+    eng.close()
+    return worst
+
+
+@pytest.mark.slow
+def test_smol_b16_workload(slm):
+    """SmolLM2-135M shape, bf16 KV, 16 rows x (512-token prompt + 512 greedy steps)."""
+    wl = synth.WORKLOADS["smol_b16"]
+    worst = run_workload(slm, wl, "smol", "smol_b16", [0, 7, 15])
+    assert worst < 2e-2
+
+
+@pytest.mark.slow
+def test_llama1b_b1_workload(slm):
+    """Llama-3.2-1B shape, bf16 KV, 2048-token prompt + 256 greedy steps, batch 1."""
+    wl = synth.WORKLOADS["llama1b_b1"]
+    worst = run_workload(slm, wl, "llama", "llama1b", [0])
+    assert worst < 2e-2
+
+
+@pytest.mark.slow
+def test_llama1b_b8_workload(slm):
+    """Llama-3.2-1B shape, bf16 KV, 8 rows x (2048-token prompt + 256 greedy steps)."""
+    wl = synth.WORKLOADS["llama1b_b8"]
+    worst = run_workload(slm, wl, "llama", "llama1b", [0, 1])
+    assert worst < 2e-2
