@@ -181,6 +181,14 @@ int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, f
 int slm_debug_trace(slm_ctx *ctx, int32_t enable, unsigned long long *out_host, size_t out_len);
 
 /*
+ * slm_debug_gemm_bf16 -- test hook for the tensor-core GEMM tile used by the prefill:
+ * C[m][n] = sum_k A[m][k] * B[n][k] in fp32, A device bf16 [M][K], B device bf16 [N][K]
+ * (both 16-byte aligned), C device fp32 [M][N].  K must be a multiple of 64.
+ * Synchronous.  SLM_ETIMEOUT if a bounded wait inside the kernel ran out.
+ */
+int slm_debug_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *A, const void *B, float *C, void *stream);
+
+/*
  * slm_debug_fill_kv -- test hook: fill the whole KV cache (every layer, slot and
  * position) with the fp32 value `value` (rounded to the cache type), so that a test
  * can check that a step writes exactly the slots it should.  Synchronous.

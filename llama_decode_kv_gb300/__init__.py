@@ -56,6 +56,7 @@ _SIGS = {
     "slm_debug_copy_kv": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
     "slm_debug_fill_kv": (ctypes.c_int, [_P, ctypes.c_float]),
     "slm_debug_trace": (ctypes.c_int, [_P, _I32, _P, ctypes.c_size_t]),
+    "slm_debug_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
                                             _P, ctypes.c_size_t, _P]),

@@ -1,0 +1,312 @@
+// gemm_tc.cu -- bf16 x bf16 -> fp32 GEMM tile on the 5th-generation tensor cores.
+//
+// One CTA computes a 128 x 128 output tile.  The activation operand may come as two bf16
+// parts (hi + lo, ~16 mantissa bits together): each K step then issues two MMAs into the
+// same accumulator against the one weight tile.
+//   warp 4 (one lane)  : TMA producer, cp.async.bulk.tensor.2d of the A and B K-blocks
+//                        (128 rows x 64 bf16 = one 128-byte swizzle atom wide) into a
+//                        4-stage ring, completion on mbarriers;
+//   warp 5 (one lane)  : tcgen05.mma.cta_group::1.kind::f16 (M 128, N 128, K 16) issuer,
+//                        accumulating in tensor memory; tcgen05.commit frees each stage
+//                        and finally signals the epilogue;
+//   warps 0-3          : allocate the 128 TMEM columns, then read the accumulator back
+//                        with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = tile rows)
+//                        and apply the fused epilogue.
+// Every wait is bounded; TMEM is always freed.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "gemm_tc.cuh"
+#include "slm_internal.h"
+
+namespace slm {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4;
+constexpr int kTileBytes = kBM * kBK * 2;            // 16 KB per operand per stage
+constexpr int kGemmThreads = 192;
+constexpr int kGemmSmem = 1024 + kStages * 3 * kTileBytes + 256;
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_addr(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows 128 bytes
+// apart, 8-row groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(const void *p) {
+    const uint32_t a = smem_addr(p);
+    uint64_t d = (uint64_t)((a & 0x3FFFF) >> 4);
+    d |= (uint64_t)(16 >> 4) << 16;     // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;             // version
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ bool gemm_wait(uint64_t *bar, uint32_t parity, int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __grid_constant__ GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);  // 1024-B aligned stages
+    uint8_t *sa = base;                                 // [kStages][128 rows][128 B]
+    uint8_t *sl = base + kStages * kTileBytes;          // low parts of A (split operand)
+    uint8_t *sb = base + 2 * kStages * kTileBytes;      // [kStages][128 rows][128 B]
+    uint64_t *full = (uint64_t *)(sb + kStages * kTileBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *done = empty + kStages;
+    uint32_t *tmem_slot = (uint32_t *)(done + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+    const int nk = g.K / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {  // 128 fp32 accumulator columns
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kBN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4 && lane == 0) {
+        // producer: A rows m0.., B rows n0.., K block kb
+        for (int kb = 0; kb < nk; kb++) {
+            const int s = kb % kStages, u = kb / kStages;
+            if (kb >= kStages && !gemm_wait(&empty[s], (u - 1) & 1, g.status)) break;
+            mbar_expect_tx(&full[s], (g.a_split ? 3 : 2) * kTileBytes);
+            tma_load_2d(sa + s * kTileBytes, &g.a_map, kb * kBK, m0, &full[s]);
+            if (g.a_split) tma_load_2d(sl + s * kTileBytes, &g.a_lo_map, kb * kBK, m0, &full[s]);
+            if (g.b_tile_k > 0) {
+                const int k = kb * kBK, z = k / g.b_tile_k;
+                tma_load_3d(sb + s * kTileBytes, &g.b_map, k - z * g.b_tile_k, n0, z, &full[s]);
+            } else {
+                tma_load_2d(sb + s * kTileBytes, &g.b_map, kb * kBK, n0, &full[s]);
+            }
+        }
+    } else if (warp == 5 && lane == 0) {
+        // MMA issuer: 4 K-steps of 16 per stage; the descriptor advances 32 bytes per step
+        const uint32_t idesc = idesc_bf16(kBM, kBN);
+        for (int kb = 0; kb < nk; kb++) {
+            const int s = kb % kStages, u = kb / kStages;
+            if (!gemm_wait(&full[s], u & 1, g.status)) break;
+            tc_fence_after();
+            const uint64_t ad = sdesc_sw128(sa + s * kTileBytes), bd = sdesc_sw128(sb + s * kTileBytes);
+            const uint64_t ld = sdesc_sw128(sl + s * kTileBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; k++) {
+                umma_bf16(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, (kb | k) != 0);
+                if (g.a_split) umma_bf16(tmem, ld + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), idesc, 1);
+            }
+            umma_commit(&empty[s]);
+        }
+        umma_commit(done);
+    } else if (warp < 4) {
+        // epilogue: wait for the accumulator, then 16 columns at a time
+        gemm_wait(done, 0, g.status);
+        __syncwarp();  // tcgen05.ld is warp-collective
+        tc_fence_after();
+        const int row = m0 + warp * 32 + lane;
+        for (int c = 0; c < kBN; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
+            if (row >= g.M) continue;
+            if (g.epi == GEMM_SWIGLU) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const int n = n0 + c + j;
+                    if (n + 1 >= g.N) continue;
+                    const float gt = __uint_as_float(r[j]), up = __uint_as_float(r[j + 1]);
+                    const float h = gt / (1.0f + __expf(-gt)) * up;
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+                    const __nv_bfloat16 lb = __float2bfloat16_rn(h - __bfloat162float(hb));
+                    g.out_bf16[(size_t)row * g.ldo + (n >> 1)] = *(const uint16_t *)&hb;
+                    if (g.out_bf16_lo) g.out_bf16_lo[(size_t)row * g.ldo + (n >> 1)] = *(const uint16_t *)&lb;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const int n = n0 + c + j;
+                    if (n >= g.N) continue;
+                    float *o = g.out_f32 + (size_t)row * g.ldo + n;
+                    const float v = __uint_as_float(r[j]);
+                    *o = g.epi == GEMM_ADD_F32 ? *o + v : v;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN) : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if (((uintptr_t)base & 15) || ((size_t)ld * 2) % 16) return cudaErrorInvalidValue;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_bf16_tiled_map(CUtensorMap *map, const void *base, int tiles, int rows, int tile_k) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if (((uintptr_t)base & 15) || tile_k % kBK) return cudaErrorInvalidValue;
+    cuuint64_t dims[3] = {(cuuint64_t)tile_k, (cuuint64_t)rows, (cuuint64_t)tiles};
+    cuuint64_t strides[2] = {(cuuint64_t)tile_k * 2, (cuuint64_t)rows * tile_k * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)kBM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t gemm_bf16_tn(const GemmArgs &args, cudaStream_t stream) {
+    if (args.K <= 0 || args.K % kBK || args.M <= 0 || args.N <= 0) return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid((args.N + kBN - 1) / kBN, (args.M + kBM - 1) / kBM);
+    gemm_bf16_tn_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace slm
+
+// ------------------------------------------------------------------ test hook
+
+using namespace slm;
+
+extern "C" int slm_debug_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *A, const void *B, float *C,
+                                   void *stream) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % kBK || !A || !B || !C) {
+        set_detached_error("slm_debug_gemm_bf16: M, N > 0, K a positive multiple of 64, non-NULL pointers");
+        return SLM_EINVAL;
+    }
+    static int *status = nullptr;
+    if (!status && cudaMalloc(&status, sizeof(int)) != cudaSuccess) return SLM_ENOMEM;
+    GemmArgs g{};
+    g.b_tile_k = 0;
+    g.a_split = 0;
+    if (make_bf16_map(&g.a_map, A, M, K, K) != cudaSuccess || make_bf16_map(&g.b_map, B, N, K, K) != cudaSuccess) {
+        set_detached_error("slm_debug_gemm_bf16: tensor map encoding failed (alignment?)");
+        return SLM_EINVAL;
+    }
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.epi = GEMM_STORE_F32;
+    g.out_f32 = C;
+    g.ldo = N;
+    g.status = status;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess || gemm_bf16_tn(g, s) != cudaSuccess) {
+        set_detached_error("slm_debug_gemm_bf16: launch failed");
+        return SLM_ECUDA;
+    }
+    int st = 0;
+    if (cudaMemcpyAsync(&st, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SLM_ECUDA;
+    return st ? SLM_ETIMEOUT : SLM_OK;
+}

@@ -17,6 +17,7 @@
 #include <string>
 #include <vector>
 
+#include "prefill.cuh"
 #include "slm_internal.h"
 
 namespace slm {
@@ -38,6 +39,8 @@ struct slm_ctx {
     std::vector<int> len;
     uint32_t launch_seq = 0;     // exchange tag of the last launch
     unsigned long long *d_trace = nullptr;  // phase timeline, when tracing is on
+    bool prefill_tc = false;     // long prompts go through the tensor-core prefill
+    PrefillPlan plan;
     bool trace_on = false;
     int *d_tokens = nullptr;     // staging for host-provided tokens [max(max_seq, max_batch)]
     float *d_logits = nullptr;   // staging for host-requested logits [max_batch][vocab]
@@ -428,6 +431,25 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         CK(c, cudaMemset(*b.dst, 0, b.bytes));
     }
     CK(c, cudaMallocHost((void **)&c->h_ids, (size_t)B * 4));
+    // tensor-core prefill buffers (blocks of up to 2048 prompt positions)
+    if (prefill_supported(m)) {
+        PrefillPlan &pp = c->plan;
+        const int rows = std::min(2048, cfg->max_seq);
+        struct {
+            void **dst;
+            size_t bytes;
+        } pb[] = {
+            {(void **)&pp.x, (size_t)rows * dim * 4},        {(void **)&pp.xn, (size_t)rows * dim * 2 * 2},
+            {(void **)&pp.qkv, (size_t)rows * qkv_rows * 4}, {(void **)&pp.o, (size_t)rows * qd * 2 * 2},
+            {(void **)&pp.h, (size_t)rows * hid * 2 * 2},    {(void **)&pp.logits, (size_t)V * 4},
+        };
+        for (auto &b : pb) {
+            if ((rc = dev_alloc(c, b.dst, b.bytes))) return rc;
+            CK(c, cudaMemset(*b.dst, 0, b.bytes));
+        }
+        CK(c, prefill_prepare(m, pp, rows));
+        c->prefill_tc = true;
+    }
     c->len.assign(B, 0);
     CK(c, cudaDeviceSynchronize());
     return SLM_OK;
@@ -579,6 +601,23 @@ extern "C" int slm_prefill(slm_ctx *c, int32_t seq, const int32_t *tokens, int32
                 return fail(c, SLM_EINVAL, "token %d out of range at %d", tokens[i], i);
         CK(c, cudaMemcpyAsync(c->d_tokens, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, s));
         dtok = c->d_tokens;
+    }
+    if (c->prefill_tc && n >= kTensorPrefillMin) {
+        const bool ids_dev2 = ids_dev;
+        cudaError_t e = prefill_run(c->m, c->plan, seq, dtok, n, last_logits ? (log_dev ? last_logits : c->d_logits) : nullptr,
+                                    ids_dev2 ? next_id : c->d_ids, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, SLM_ECUDA, "tensor-core prefill failed: %s", cudaGetErrorString(e));
+        }
+        c->len[seq] = n;
+        if (!log_dev) CK(c, cudaMemcpyAsync(last_logits, c->d_logits, (size_t)c->cfg.vocab * 4, cudaMemcpyDeviceToHost, s));
+        if (!ids_dev) CK(c, cudaMemcpyAsync(c->h_ids, c->d_ids, 4, cudaMemcpyDeviceToHost, s));
+        if (!tok_dev || !log_dev || !ids_dev) {
+            CK(c, cudaStreamSynchronize(s));
+            if (!ids_dev) *next_id = c->h_ids[0];
+        }
+        return SLM_OK;
     }
     for (int p = 0; p < n; p++) {
         StepParams P{};

@@ -21,10 +21,12 @@ constexpr int kMaxGroupPass = 4;                      // query heads per attenti
 constexpr int kMaxChunksPerSeq = 64;                  // split-K chunks per (row, kv head)
 constexpr int kMaxChunksA = 16;                       // chunks when consumers merge them
 constexpr int kMinAttnChunk = 32;                     // positions
+constexpr int kTensorPrefillMin = 16;                 // prompts this long use the GEMM prefill
 constexpr size_t kXsBudget = 88 * 1024;               // activation tile, at most (16-slot ring)
 constexpr size_t kSmemLimit = 227 * 1024;             // dynamic shared memory per CTA
 constexpr int kMaxOwn = 32;                           // residual rows one CTA may own
-constexpr int kPadElems = 8;                          // K tiles are padded to 8 elements
+constexpr int kPadElems = 64;                         // K tiles are padded to 64 elements
+                                                      //   (one tensor-core K block)
 
 // status word bits (device side)
 constexpr int kStExchangeTimeout = 1;

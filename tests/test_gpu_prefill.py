@@ -1,0 +1,75 @@
+"""The tensor-core prefill (tcgen05 GEMMs + causal attention) against the oracle.
+
+It is taken for prompts of 16 tokens or more when weights and KV cache are bf16; its
+GEMM operands are bf16, so it is held to the bf16-cache tolerance (2e-2 * max|logit|).
+Prompts longer than one 2048-position block exercise the chunked path, and decode
+steps run on top of the cache it wrote.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity_util import check_id, check_logits
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+SHAPE = synth.Shape(dim=128, n_layers=2, n_heads=4, n_kv_heads=2, head_dim=64, hidden=256, vocab=512,
+                    max_seq=2304, max_batch=2, rope_theta=10000.0, weight_dtype=synth.DTYPE_BF16,
+                    kv_dtype=synth.DTYPE_BF16)
+
+
+@pytest.fixture(scope="module")
+def slm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import llama_decode_kv_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("n", [16, 100, 2100])
+def test_tensor_prefill_matches_oracle(slm, n):
+    s = SHAPE
+    W = synth.make_weights(s, seed=21)
+    prompt = synth.make_prompt(s, 3, n)
+    o = oracle.Model(s, W)
+    ref_logits, ref_id = o.prefill(0, prompt)
+    eng = slm.Engine(s, W)
+    lg, nid = eng.prefill_checked(0, prompt)
+    check_logits(lg.cpu().numpy(), ref_logits, 2e-2, f"prefill n={n}")
+    check_id(int(nid.item()), ref_logits, ref_id, f"prefill n={n}")
+    # decode on top of the prefilled cache, teacher-forced with the oracle's ids
+    tok = ref_id
+    for st in range(4):
+        rl, rid = o.decode_step([0], [tok], [n + st])
+        gl, gid = eng.decode_checked([0], torch.tensor([tok], dtype=torch.int32, device="cuda"), [n + st])
+        check_logits(gl[0].cpu().numpy(), rl[0], 2e-2, f"decode {st} after prefill n={n}")
+        check_id(int(gid.item()), rl[0], int(rid[0]), f"decode {st} after prefill n={n}")
+        tok = int(rid[0])
+    assert eng.sync() == 0, eng.last_error()
+    # the cache rows the prefill wrote, against the oracle's (bf16 values)
+    for layer in (0, s.n_layers - 1):
+        gk, gv = eng.kv(layer, 0)
+        ok, ov = o.kv(layer, 0)
+        assert gk.shape == ok.shape
+        tol = 2e-2 * max(1.0, float(np.abs(ok).max()))
+        assert np.abs(gk - ok).max() <= tol and np.abs(gv - ov).max() <= tol
+
+
+def test_tensor_prefill_equals_token_by_token_prefill_closely(slm):
+    # The same prompt through the tensor-core path (>= 16 tokens) and, token by token,
+    # through the decode kernel (15 tokens then 1 decode step per further token).
+    s = SHAPE
+    W = synth.make_weights(s, seed=22)
+    prompt = synth.make_prompt(s, 4, 40)
+    a = slm.Engine(s, W)
+    la, ia = a.prefill_checked(0, prompt)
+    b = slm.Engine(s, W)
+    b.prefill_checked(0, prompt[:15], want_logits=False)
+    lb = None
+    for p in range(15, 40):
+        lb, ib = b.decode_checked([0], torch.tensor([int(prompt[p])], dtype=torch.int32, device="cuda"), [p])
+    la, lb = la.cpu().numpy(), lb[0].cpu().numpy()
+    assert np.abs(la - lb).max() <= 2e-2 * np.abs(lb).max()
+    assert a.sync() == 0 and b.sync() == 0
