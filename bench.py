@@ -59,6 +59,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def peaks_tensor():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def kv_bytes_read(shape, ctx: int) -> int:
     """K and V bytes one row reads in one step at context length ctx (all layers)."""
     esz = 2 if shape.kv_dtype == synth.DTYPE_BF16 else 4
@@ -160,6 +168,35 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def prefill_measure(slm, torch, W, local: int, reps: int = 3):
+    """Tensor-core prefill of a 512-token prompt on the same weights with a bf16 KV cache
+    (the SmolLM2 batch-16 workload's prompt length); FLOPs counted once per MAC of the
+    linear layers and the logits row plus causal attention."""
+    s = synth.WORKLOADS["smol_b16"].shape.replace(max_batch=1)
+    eng = slm.Engine(s, W)
+    n = 512
+    prompt = torch.as_tensor(synth.make_prompt(s, 0, n)).to(torch.device("cuda", local))
+    nid = torch.empty(1, dtype=torch.int32, device=prompt.device)
+    times = []
+    for i in range(reps + 1):
+        eng.reset(0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        rc = eng.prefill(0, prompt, None, nid)
+        b.record()
+        torch.cuda.synchronize()
+        if rc != 0:
+            raise RuntimeError(f"slm_prefill: {eng.last_error()}")
+        if i:
+            times.append(a.elapsed_time(b) / 1e3)
+    assert eng.sync() == 0, eng.last_error()
+    eng.close()
+    t = statistics.median(times)
+    lin = synth.n_params(s) - s.vocab * s.dim  # matrices of the blocks
+    flops = 2.0 * lin * n + 2.0 * s.vocab * s.dim + 2.0 * 2 * s.head_dim * s.n_heads * s.n_layers * n * (n + 1) / 2
+    return t, flops
 
 
 def cpu_baseline(shape, W, prompt, budget_s: float):
@@ -300,6 +337,9 @@ def run_ours(args, world, rank, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = e2e_steps * wl.batch * world / e2e_s
 
+    pf_t, pf_flops = prefill_measure(slm, torch, W, local)
+    tflops_peak = peaks_tensor()
+
     if rank != 0:
         return
     line = {
@@ -327,6 +367,11 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * wl.batch,
                 "d2h_bytes_per_step": 4 * wl.batch},
         "gpu_launches": args.steps,
+        "prefill": {"workload": "512-token prompt, same SmolLM2-135M-shaped weights, bf16 KV cache",
+                    "tokens_per_s": 512 / pf_t, "ms": pf_t * 1e3,
+                    "tflops": pf_flops / pf_t / 1e12, "peak_tflops": tflops_peak,
+                    "frac": pf_flops / pf_t / 1e12 / tflops_peak, "bound": "tensor",
+                    "note": "activation operands split into bf16 hi + lo: the tensor cores execute 2x these FLOPs"},
         "clocks": clk,
     }
     if world == 1:
