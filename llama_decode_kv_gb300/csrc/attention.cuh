@@ -1,5 +1,6 @@
 // attention.cuh -- split-K GQA decode attention over one chunk of cached positions
 // (flash-decoding).  Shared by the decode kernel and the stand-alone attention op.
+// q arrives with RoPE applied; the cache holds rotated keys.
 //
 // softmax(q K^T / sqrt(d_head)) V for the G query heads that read one kv head
 // (kasahare 0.4.0 / simple-llm, "Architecture": GQA with n_kv_heads <= n_heads).  The
@@ -14,9 +15,8 @@
 namespace slm {
 
 // Eight consecutive elements of a cached key or value row (global or shared memory).
-template <bool KVBF16>
-__device__ __forceinline__ void load8(const uint8_t *row, int d0, float (&v)[8]) {
-    if constexpr (KVBF16) {
+__device__ __forceinline__ void load8(const uint8_t *row, int d0, bool kvbf16, float (&v)[8]) {
+    if (kvbf16) {
         uint4 u = *(const uint4 *)(row + d0 * 2);
         v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
         v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
@@ -47,12 +47,17 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float (&o)[8], f
 
 // One work item: G query heads x positions [t0, t1) of one (row, kv head).
 struct AttnTask {
-    const float *q;              // query rows of the group: head j at q + j * hd (shared
-                                 //   or global memory, complete before the call)
-    const float *rope;           // (cos, sin) pairs of the position, or null: q is rotated
+    const float *q;              // query rows of the group, head j at q + j * hd, RoPE applied;
+                                 //   complete before the call
+    bool q_ready;                // q already multiplied by log2(e) / sqrt(hd) and in shared
+                                 //   memory; otherwise scaled here into the scratch
+    bool kv_bf16;                // cache element type: bf16 or fp32
     const uint8_t *kbase;        // keys of the (row, kv head): position t at t * hd elements
     const uint8_t *vbase;        //   (global cache, or a shared-memory copy of the chunk
                                  //   addressed as if it started at position 0)
+    const uint8_t *tail_k;       // position tail_t is read from these rows instead (the
+    const uint8_t *tail_v;       //   step's own key and value); tail_t = -1: none
+    int tail_t;
     float *out;                  // final output rows: head j at out + j * hd
     float *part;                 // partials: head j, chunk c at (j * kMaxChunksPerSeq + c) * (hd + 2)
     int *counter;                // arrivals of this (row, kv head)'s chunks
@@ -66,12 +71,12 @@ struct AttnTask {
 
 // All kComputeThreads threads of the CTA call this.  `scratch` holds
 // kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) floats; `flag` one int.
-template <bool KVBF16>
-__device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
+__device__ __forceinline__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hd = T.hd, G = T.G, half = hd / 2;
+    const int hd = T.hd, G = T.G;
     const int t0 = T.t0, t1 = T.t1, nc = T.nc, c = T.c;
-    const size_t rowbytes = (size_t)hd * (KVBF16 ? 2 : 4);
+    const bool kvbf16 = T.kv_bf16;
+    const size_t rowbytes = (size_t)hd * (kvbf16 ? 2 : 4);
     const uint8_t *kbase = T.kbase, *vbase = T.vbase;
     const float qscale = rsqrtf((float)hd) * 1.4426950408889634f;  // scores in log2 units
     float *qs = scratch;
@@ -86,26 +91,18 @@ __device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
 
     for (int jp = 0; jp < G; jp += kMaxGroupPass) {
         const int Gp = min(kMaxGroupPass, G - jp);
-        compute_sync();  // previous users of qs / ws are done; the append is visible
-        for (int e = tid; e < Gp * half; e += kComputeThreads) {
-            int j = e / half, i = e - j * half;
-            const float *qr = T.q + (size_t)(jp + j) * hd;
-            float a = qr[i], bb = qr[i + half];  // q may sit in shared or global memory
-            if (T.rope) {
-                float cs = __ldg(T.rope + 2 * i), sn = __ldg(T.rope + 2 * i + 1);
-                qs[j * hd + i] = (a * cs - bb * sn) * qscale;
-                qs[j * hd + i + half] = (a * sn + bb * cs) * qscale;
-            } else {
-                qs[j * hd + i] = a * qscale;
-                qs[j * hd + i + half] = bb * qscale;
-            }
+        const float *qsrc = T.q + (size_t)jp * hd;
+        if (jp > 0 || !T.q_ready) compute_sync();  // previous users of qs / ws are done
+        if (!T.q_ready) {
+            for (int e = tid; e < Gp * hd; e += kComputeThreads) qs[e] = qsrc[e] * qscale;  // q may be global
+            compute_sync();
+            qsrc = qs;
         }
-        compute_sync();
         float qv[kMaxGroupPass][8];
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++)
 #pragma unroll
-            for (int d = 0; d < 8; d++) qv[j][d] = (j < Gp && lane_on) ? qs[j * hd + d0 + d] : 0.f;
+            for (int d = 0; d < 8; d++) qv[j][d] = (j < Gp && lane_on) ? qsrc[j * hd + d0 + d] : 0.f;
         float mx[kMaxGroupPass], ls[kMaxGroupPass], o[kMaxGroupPass][8];
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++) {
@@ -119,8 +116,9 @@ __device__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
             const bool valid = t < t1;
             float kv8[8], vv8[8];
             if (valid && lane_on) {
-                load8<KVBF16>(kbase + (size_t)t * rowbytes, d0, kv8);
-                load8<KVBF16>(vbase + (size_t)t * rowbytes, d0, vv8);
+                const bool tl = t == T.tail_t;
+                load8(tl ? T.tail_k : kbase + (size_t)t * rowbytes, d0, kvbf16, kv8);
+                load8(tl ? T.tail_v : vbase + (size_t)t * rowbytes, d0, kvbf16, vv8);
             } else {
 #pragma unroll
                 for (int d = 0; d < 8; d++) kv8[d] = vv8[d] = 0.f;

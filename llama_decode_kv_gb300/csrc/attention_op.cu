@@ -41,7 +41,10 @@ __global__ void __launch_bounds__(kComputeThreads) attention_decode_kernel(const
     const size_t rowbytes = (size_t)hd * (KVBF16 ? 2 : 4);
     AttnTask T;
     T.q = P.q + ((size_t)b * P.H + (size_t)g * G) * hd;
-    T.rope = nullptr;
+    T.q_ready = false;
+    T.kv_bf16 = KVBF16;
+    T.tail_k = T.tail_v = nullptr;
+    T.tail_t = -1;
     T.kbase = P.k + ((size_t)b * P.KV + g) * P.cap * rowbytes;
     T.vbase = P.v + ((size_t)b * P.KV + g) * P.cap * rowbytes;
     T.out = P.out + ((size_t)b * P.H + (size_t)g * G) * hd;
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(kComputeThreads) attention_decode_kernel(const
     T.t1 = min(P.ctx[b], T.t0 + P.chunk);
     T.nc = nc;
     T.c = c;
-    attn_core<KVBF16>(T, scratch, &flag);
+    attn_core(T, scratch, &flag);
 }
 
 // ------------------------------------------------------------------ host side

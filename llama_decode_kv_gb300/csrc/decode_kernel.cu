@@ -6,25 +6,28 @@
 // residual; then the final RMSNorm, the tied-embedding logits and the greedy argmax).
 //
 // Structure (one CTA per SM, 8 compute warps + 1 streaming warp):
-//  * Weights do not depend on activations, so the streaming warp walks this CTA's
-//    share of every matrix of the step (layer by layer, in consumption order) and
-//    copies it HBM -> shared memory with cp.async.bulk into a ring of 16 KB slots,
-//    signalled by mbarriers.  It runs ahead of the compute warps across phases.
-//  * Each GEMV phase splits its output rows evenly over the CTAs.  A phase's input is
-//    a vector produced by other CTAs; instead of grid barriers, producers publish every
-//    element as a tagged 8-byte word (value + this launch's tag, one atomic store) and
-//    consumers poll the words they need until the tags match: one L2 round trip per
-//    hand-off, no fence, no counter.  Exchange buffers are per layer, so nothing is
-//    rewritten within a launch.
+//  * Weights do not depend on activations: the streaming warp walks this CTA's share of
+//    every matrix of the step in consumption order and copies it HBM -> shared memory
+//    with cp.async.bulk into a ring of 8 KB slots signalled by mbarriers, running ahead
+//    of the compute warps across phases.
+//  * Each GEMV phase splits its output rows evenly over the CTAs.  Its input vector is
+//    produced by other CTAs: producers publish every element as a tagged 8-byte word
+//    (value + this launch's tag, one store) and consumers poll the words until the tags
+//    match -- no fence, no counter, no grid barrier.  Exchange buffers are per layer, so
+//    nothing is rewritten within a launch.
+//  * RMSNorm is folded into that poll: the squares are summed as the elements arrive,
+//    the gain is applied on arrival and 1/rms multiplies the finished dot products.
+//  * QKV rows are stored in RoPE pairs (dims i and i + d/2 of a head side by side), so
+//    the QKV epilogue rotates q and k, scales q for a base-2 softmax, rounds k and v to
+//    the cache type and appends them to the cache.
 //  * Each CTA keeps the residual rows it owns (the rows of Wo and W2 it computes) in
 //    shared memory, so the residual adds read nothing from memory.
-//  * GEMV: fp32 activations in shared memory, bf16 weights widened by shifts, fp32 FMA,
-//    butterfly warp reduction.  Epilogues are fused: QKV publish, residual add (Wo,
-//    W2), SwiGLU over interleaved W1/W3 rows, logits + argmax.
 //  * Attention: work item = (row, kv head, chunk of positions), flash-decoding with an
-//    online softmax per query head (attention.cuh); RoPE of q and k and the cache
-//    append happen here.  Chunk states are either merged by the Wo consumers (small
-//    batches) or by the last CTA to finish a (row, kv head).
+//    online softmax per query head (attention.cuh); chunk states are merged by the Wo
+//    consumers (small batches) or by the last CTA to finish a (row, kv head).
+//  * The code is kept small: the four GEMV phases of a layer run through one body with a
+//    run-time epilogue, so each helper is emitted once.  Every layer walks the whole
+//    step's code again, and it has to stay in the SM's instruction caches.
 //  * Every wait is bounded (1 s): on expiry the kernel records it in the status word,
 //    raises an abort flag and finishes the step without waiting any further.
 #include <cuda_runtime.h>
@@ -42,7 +45,8 @@ namespace slm {
 struct Shared {
     uint64_t *full;     // [kMaxRingSlots]
     uint64_t *empty;    // [kMaxRingSlots]
-    float *rs;          // [kMaxBatch] 1 / rms
+    float *ssp;         // [kComputeWarps][kMaxBatch] per-warp sums of squares of the
+                        //   current RMSNorm input (every warp stores all its entries)
     float *wbest_v;     // [kComputeWarps][kMaxBatch]
     int *wbest_i;       // [kComputeWarps][kMaxBatch]
     int *flags;         // [4]: 0 = last-arriver flag
@@ -54,7 +58,7 @@ struct Shared {
 
 // Layout: barriers and small arrays, owned residual rows, K-tile accumulators, the
 // activation tile, then the weight ring (sized at create time from what is left).
-constexpr int kMiscBytes = 2 * kMaxRingSlots * 8 + kMaxBatch * 4 + 2 * kComputeWarps * kMaxBatch * 4 + 16;
+constexpr int kMiscBytes = 2 * kMaxRingSlots * 8 + 3 * kComputeWarps * kMaxBatch * 4 + 16;
 constexpr int kOwnOffset = ((kMiscBytes + 127) / 128) * 128;
 constexpr int kAccOffset = kOwnOffset + kMaxBatch * kMaxOwn * 4;
 constexpr int kXsOffset = kAccOffset + kMaxOwn * kMaxBatch * 4;
@@ -68,8 +72,8 @@ __device__ __forceinline__ Shared carve(uint8_t *base, const StepParams &P) {
     p += kMaxRingSlots * 8;
     s.empty = (uint64_t *)p;
     p += kMaxRingSlots * 8;
-    s.rs = (float *)p;
-    p += kMaxBatch * 4;
+    s.ssp = (float *)p;
+    p += kComputeWarps * kMaxBatch * 4;
     s.wbest_v = (float *)p;
     p += kComputeWarps * kMaxBatch * 4;
     s.wbest_i = (int *)p;
@@ -107,43 +111,53 @@ __device__ __forceinline__ int xpos(int k, int KBp, bool perm) {
     return perm ? ((k & 4) ? (KBp >> 1) : 0) + ((k >> 3) << 2) + (k & 3) : k;
 }
 
-__device__ __forceinline__ int xinv(int q, int KBp, bool perm) {
-    if (!perm) return q;
-    const int h = q >= (KBp >> 1) ? 1 : 0, r = q - h * (KBp >> 1);
-    return ((r >> 2) << 3) + (h << 2) + (r & 3);
+// Timeline hook: thread 0 of each CTA stamps (phase, point) when tracing is on.
+__device__ __forceinline__ void trace_mark(const StepParams &P, int slot, int point) {
+    if (P.trace && threadIdx.x == 0)
+        P.trace[((size_t)blockIdx.x * trace_slots(P.m.n_layers) + slot) * 3 + point] = global_ns();
 }
 
-// Poll rows x len tagged words (row stride src_ld) into shared memory (row stride
-// dst_ld; element j of a row at xpos(j, perm_ld) when perm_ld > 0) until every tag
-// equals `tag`.  Each thread keeps up to 8 loads in flight.  All compute threads call
-// it; it ends with a CTA barrier.
-__device__ void ll_poll(const StepParams &P, const uint64_t *src, int src_ld, int rows, int len,
-                        float *dst, int dst_ld, uint32_t tag, int perm_ld = 0) {
-    constexpr int kBatch = 8;
+// ------------------------------------------------------------------ polling
+
+constexpr int kPollBatch = 8;  // loads each thread keeps in flight
+
+// Poll rows x len tagged words src[r * src_ld + j] into shared memory dst[r * dst_ld +
+// xpos(j)] (natural order when perm_ld is 0) until every tag equals the launch's tag.
+// With `gain` (a single row): element j is stored as x_j * gain_j and each warp stores
+// its sum of x_j^2 in ssp[warp * kMaxBatch].  All compute threads call it; it ends with
+// their barrier.
+__device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *src, int src_ld, int rows, int len,
+                                        float *dst, int dst_ld, int perm_ld, const float *gain, float *ssp) {
     const int tid = threadIdx.x;
     const int n = rows * len;
-    for (int base = 0; base < n; base += kComputeThreads * kBatch) {
-        int so[kBatch], dof[kBatch];
-        bool need[kBatch];
+    const uint32_t tag = P.tag;
+    float ss = 0.f;
+    for (int base = 0; base < n; base += kComputeThreads * kPollBatch) {
+        int so[kPollBatch], dof[kPollBatch];
+        float g[kPollBatch];
+        bool need[kPollBatch];
 #pragma unroll
-        for (int k = 0; k < kBatch; k++) {
-            int i = base + k * kComputeThreads + tid;
+        for (int k = 0; k < kPollBatch; k++) {
+            const int i = base + k * kComputeThreads + tid;
             need[k] = i < n;
-            int r = need[k] ? i / len : 0, j = need[k] ? i - r * len : 0;
+            const int r = need[k] ? i / len : 0, j = need[k] ? i - r * len : 0;
             so[k] = r * src_ld + j;
             dof[k] = r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j);
+            g[k] = (gain && need[k]) ? __ldg(gain + j) : 1.f;
         }
         unsigned long long t0 = 0;
         for (int it = 0;; it++) {
-            uint64_t w[kBatch];
+            uint64_t w[kPollBatch];
 #pragma unroll
-            for (int k = 0; k < kBatch; k++) w[k] = need[k] ? ll_load(src + so[k]) : 0;
+            for (int k = 0; k < kPollBatch; k++) w[k] = need[k] ? ll_load(src + so[k]) : 0;
             bool pending = false;
 #pragma unroll
-            for (int k = 0; k < kBatch; k++) {
+            for (int k = 0; k < kPollBatch; k++) {
                 if (!need[k]) continue;
                 if ((uint32_t)(w[k] >> 32) == tag) {
-                    dst[dof[k]] = __uint_as_float((uint32_t)w[k]);
+                    const float x = __uint_as_float((uint32_t)w[k]);
+                    ss = fmaf(x, x, ss);
+                    dst[dof[k]] = x * g[k];
                     need[k] = false;
                 } else {
                     pending = true;
@@ -161,47 +175,21 @@ __device__ void ll_poll(const StepParams &P, const uint64_t *src, int src_ld, in
             }
         }
     }
+    if (ssp) {
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) ssp[(tid >> 5) * kMaxBatch] = ss;
+    }
     compute_sync();
-}
-
-// Timeline hook: thread 0 of each CTA stamps (phase, point) when tracing is on.
-__device__ __forceinline__ void trace_mark(const StepParams &P, int slot, int point) {
-    if (P.trace && threadIdx.x == 0)
-        P.trace[((size_t)blockIdx.x * trace_slots(P.m.n_layers) + slot) * 3 + point] = global_ns();
 }
 
 // ------------------------------------------------------------------ chunk walk
 // The streaming warp and the compute warps enumerate exactly the same chunks: this
-// CTA's units [u0, u1) of the matrix, K tile by K tile.
+// CTA's units [u0, u1) of the matrix, K tile by K tile, rows_per_chunk rows at a time.
 
 struct Chunk {
-    int kt;
-    int unit0;       // first unit of the chunk, relative to the CTA's first unit
-    int nunits;
     const uint8_t *src;
     uint32_t bytes;
 };
-
-template <typename F>
-__device__ __forceinline__ void for_each_chunk(const Mat &M, int layer, int esz, int cta, int grid, F &&f) {
-    const int units = M.rows / M.rows_per_unit;
-    int u0, u1;
-    unit_range(units, grid, cta, u0, u1);
-    const int cu = M.rows_per_chunk / M.rows_per_unit;
-    const uint8_t *lbase = M.base + (long long)layer * M.layer_stride;
-    const long long rowbytes = (long long)M.KBp * esz;
-    for (int kt = 0; kt < M.nkt; kt++) {
-        for (int u = u0; u < u1; u += cu) {
-            Chunk c;
-            c.kt = kt;
-            c.unit0 = u - u0;
-            c.nunits = min(cu, u1 - u);
-            c.src = lbase + ((long long)kt * M.rows + (long long)u * M.rows_per_unit) * rowbytes;
-            c.bytes = (uint32_t)((long long)c.nunits * M.rows_per_unit * rowbytes);
-            f(c);
-        }
-    }
-}
 
 // ------------------------------------------------------------------ streaming warp
 // A cursor over the same chunk sequence as the compute warps walk: per layer QKV, Wo,
@@ -223,13 +211,6 @@ __device__ void cursor_enter(const StepParams &P, Cursor &c) {
     c.u = c.u0;
 }
 
-__device__ void cursor_init(const StepParams &P, Cursor &c) {
-    c.phase = 0;
-    c.layer = 0;
-    c.done = false;
-    cursor_enter(P, c);
-}
-
 // Next chunk of the sequence; false at the end.
 __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
     const Model &m = P.m;
@@ -239,13 +220,11 @@ __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
         if (c.u < c.u1) {
             const int cu = M.rows_per_chunk / M.rows_per_unit;
             const long long rowbytes = (long long)M.KBp * esz;
-            out.kt = c.kt;
-            out.unit0 = c.u - c.u0;
-            out.nunits = min(cu, c.u1 - c.u);
+            const int nunits = min(cu, c.u1 - c.u);
             out.src = M.base + (long long)(c.phase == 4 ? 0 : c.layer) * M.layer_stride +
                       ((long long)c.kt * M.rows + (long long)c.u * M.rows_per_unit) * rowbytes;
-            out.bytes = (uint32_t)((long long)out.nunits * M.rows_per_unit * rowbytes);
-            c.u += out.nunits;
+            out.bytes = (uint32_t)((long long)nunits * M.rows_per_unit * rowbytes);
+            c.u += nunits;
             return true;
         }
         if (++c.kt < M.nkt) {
@@ -269,10 +248,13 @@ __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
 }
 
 // Copies this CTA's chunks into the ring, in the order the compute warps use them.
-__device__ void producer(const StepParams &P, Shared &S) {
+__device__ __forceinline__ void producer(const StepParams &P, Shared &S) {
     const uint32_t slots = (uint32_t)P.ring_slots;
     Cursor ic;
-    cursor_init(P, ic);
+    ic.phase = 0;
+    ic.layer = 0;
+    ic.done = false;
+    cursor_enter(P, ic);
     uint32_t issued = 0;
     Chunk c;
     while (cursor_next(P, ic, c)) {
@@ -328,7 +310,7 @@ __device__ __forceinline__ size_t ll_layer(const StepParams &P, int layer, int p
 }
 
 // Residual rows this CTA owns (rows of Wo and W2 it computes) start as the embedding.
-__device__ void init_residual(const StepParams &P, Shared &S) {
+__device__ __forceinline__ void init_residual(const StepParams &P, Shared &S) {
     const Model &m = P.m;
     int r0, r1;
     unit_range(m.dim, P.grid, blockIdx.x, r0, r1);
@@ -339,26 +321,36 @@ __device__ void init_residual(const StepParams &P, Shared &S) {
     }
 }
 
-// RMSNorm of the staged rows in place: x[k] = x[k] * rsqrt(mean + eps) * g[k] for the
-// dim logical elements; the padding past dim must already be zero.
-__device__ void norm_in_place(const StepParams &P, float *xs, int ld, const float *g, bool perm, Shared &S) {
-    const Model &m = P.m;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int b = warp; b < P.batch; b += kComputeWarps) {
-        const float *r = xs + (size_t)b * ld;
-        float ss = 0.f;
-        for (int q = lane; q < ld; q += 32) ss = fmaf(r[q], r[q], ss);
-        ss = warp_sum(ss);
-        if (lane == 0) S.rs[b] = 1.0f / sqrtf(ss / (float)m.dim + m.norm_eps);
-    }
-    compute_sync();
-    for (int b = 0; b < P.batch; b++) {
+// RMSNorm statistics of staged raw rows: each warp stores its part of sum_j x_j^2 of
+// row b in ssp[warp * kMaxBatch + b] (0 for rows it does not hold) and every element is
+// multiplied by its gain.  Rows are spread over power-of-two groups of threads.  Ends
+// with a barrier.
+__device__ __forceinline__ void norm_pass(const StepParams &P, float *xs, int ld, bool perm, const float *gain, float *ssp) {
+    const int batch = P.batch, dim = P.m.dim;
+    int rp = 1;
+    while (rp < batch) rp <<= 1;
+    const int tpr = kComputeThreads / rp;  // threads per row, >= 16
+    const int tid = threadIdx.x, b = tid / tpr, t = tid - b * tpr;
+    float ss = 0.f;
+    if (b < batch) {
         float *r = xs + (size_t)b * ld;
-        const float rs = S.rs[b];
-        for (int q = tid; q < ld; q += kComputeThreads) {
-            const int k = xinv(q, ld, perm);
-            if (k < m.dim) r[q] = (r[q] * rs) * g[k];
+        for (int j = t; j < dim; j += tpr) {
+            const int q = xpos(j, ld, perm);
+            const float x = r[q];
+            ss = fmaf(x, x, ss);
+            r[q] = x * __ldg(gain + j);
         }
+    }
+    const int w = tpr < 32 ? tpr : 32;  // lanes of one row within a warp
+    for (int off = w >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const int warp = tid >> 5, lane = tid & 31;
+    const float s0 = __shfl_sync(0xffffffffu, ss, 0), s16 = __shfl_sync(0xffffffffu, ss, 16);
+    const int row_a = (warp * 32) / tpr, row_b = (warp * 32 + 16) / tpr;  // rows of lanes 0 and 16
+    if (lane < batch) {
+        float v = 0.f;
+        if (lane == row_a) v += s0;
+        if (row_b != row_a && lane == row_b) v += s16;
+        ssp[warp * kMaxBatch + lane] = v;
     }
     compute_sync();
 }
@@ -370,7 +362,7 @@ __device__ void zero_pad(const StepParams &P, float *xs, int ld, int from, bool 
 
 // Merge the chunk states of every (row, head) published by the attention items into
 // the Wo input tile: o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
-__device__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M, Shared &S) {
+__device__ __forceinline__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M, Shared &S) {
     const Model &m = P.m;
     const bool perm = m.weight_bf16;
     const int H = m.n_heads, hd = m.head_dim, st = hd + 2;
@@ -378,11 +370,12 @@ __device__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M,
     for (int b = 0; b < P.batch; b++) ncmax = max(ncmax, P.nchunk[b]);
     float *stage = S.xs + (size_t)P.batch * M.KBp;  // [batch][H][ncmax][hd + 2]
     const uint64_t *src = m.ll_part + ll_layer(P, layer, H * kMaxChunksA * st);
+    zero_pad(P, S.xs, M.KBp, H * hd, perm);
     for (int b = 0; b < P.batch; b++) {
         const int nc = P.nchunk[b];
         // rows (b, h) x (nc * st) words, source row stride kMaxChunksA * st
-        ll_poll(P, src + (size_t)b * H * kMaxChunksA * st, kMaxChunksA * st, H, nc * st,
-                stage + (size_t)b * H * ncmax * st, ncmax * st, P.tag);
+        poll_words(P, src + (size_t)b * H * kMaxChunksA * st, kMaxChunksA * st, H, nc * st,
+                   stage + (size_t)b * H * ncmax * st, ncmax * st, 0, nullptr, nullptr);
     }
     for (int b = 0; b < P.batch; b++) {
         const int nc = P.nchunk[b];
@@ -402,54 +395,58 @@ __device__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M,
             S.xs[(size_t)b * M.KBp + xpos(e, M.KBp, perm)] = O / L;
         }
     }
-    zero_pad(P, S.xs, M.KBp, H * hd, perm);
     compute_sync();
 }
 
 // Stage the input of phase `epi` (K tile kt) into S.xs as fp32 [batch][KBp] (element
-// order given by xpos).
-__device__ void stage_input(const StepParams &P, int epi, int layer, const Mat &M, int kt, Shared &S) {
+// order given by xpos).  An RMSNorm input is left as x * gain, with the per-warp sums
+// of x^2 in S.ssp.
+__device__ __forceinline__ void stage_input(const StepParams &P, int epi, int layer, const Mat &M, int kt, Shared &S) {
     const Model &m = P.m;
     const int tid = threadIdx.x;
     const bool perm = m.weight_bf16;
     const int pl = perm ? M.KBp : 0;
     compute_sync();  // everyone is done with the previous tile
     if (epi == EPI_QKV || epi == EPI_W13 || epi == EPI_LOGITS) {
-        // the gains do not depend on this step: fetch them while waiting for x
         const float *g = epi == EPI_QKV   ? m.norms + (size_t)layer * 2 * m.dim
                          : epi == EPI_W13 ? m.norms + (size_t)layer * 2 * m.dim + m.dim
                                           : m.norms + (size_t)m.n_layers * 2 * m.dim;
-        float *gs = S.xs + (size_t)P.batch * M.KBp;
-        for (int k = tid * 4; k < m.dim; k += kComputeThreads * 4) cp_async16(gs + k, g + k);
+        zero_pad(P, S.xs, M.KBp, m.dim, perm);
+        if (epi == EPI_QKV && tid < P.batch) {  // the QKV epilogue's RoPE rows, into L1 meanwhile
+            const float *rr = m.rope + (size_t)P.pos[tid] * m.head_dim;
+            for (int k = 0; k < m.head_dim; k += 32) prefetch_l1(rr + k);
+        }
         if (epi == EPI_QKV && layer == 0) {
             for (int b = 0; b < P.batch; b++) {
-                int tok = token_of(P, b);
+                const int tok = token_of(P, b);
                 for (int k = tid; k < m.dim; k += kComputeThreads)
                     S.xs[(size_t)b * M.KBp + xpos(k, M.KBp, perm)] = emb_elem(m, tok, k);
             }
+            compute_sync();
+            norm_pass(P, S.xs, M.KBp, perm, g, S.ssp);
         } else {
             const uint64_t *src = epi == EPI_W13 ? m.ll_xa + ll_layer(P, layer, m.dim)
                                                  : m.ll_x + ll_layer(P, epi == EPI_QKV ? layer : m.n_layers, m.dim);
-            ll_poll(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, P.tag, pl);
+            if (P.batch == 1) {
+                poll_words(P, src, m.dim, 1, m.dim, S.xs, M.KBp, pl, g, S.ssp);
+            } else {
+                poll_words(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, pl, nullptr, nullptr);
+                norm_pass(P, S.xs, M.KBp, perm, g, S.ssp);
+            }
         }
-        zero_pad(P, S.xs, M.KBp, m.dim, perm);
-        cp_async_wait_all();
-        compute_sync();
-        norm_in_place(P, S.xs, M.KBp, gs, perm, S);
     } else if (epi == EPI_WO) {
         if (P.attn_consumer_merge) {
             merge_chunk_states(P, layer, M, S);
         } else {
             const int qd = m.n_heads * m.head_dim;
-            ll_poll(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, P.tag, pl);
             zero_pad(P, S.xs, M.KBp, qd, perm);
-            compute_sync();
+            poll_words(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, pl, nullptr, nullptr);
         }
     } else {  // W2: tile kt of the SwiGLU output
         const int k0 = kt * M.KB, kn = min(M.K - k0, M.KB);
-        ll_poll(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, P.tag, pl);
         zero_pad(P, S.xs, M.KBp, kn, perm);
-        compute_sync();
+        poll_words(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, pl, nullptr,
+                   nullptr);
     }
 }
 
@@ -493,11 +490,10 @@ template <int NB, int RG> struct Unroll {
 };
 
 // Dots of RG weight rows with every staged batch row.  Group row r lives at
-// base + (r / RPU) * unit_stride + (r % RPU) * rowbytes; rows r >= nr are skipped.
-// Value index r * NB + b.  Pieces are taken U at a time into U separate accumulators.
-template <int NB, int RG, int RPU, bool WBF16>
-__device__ __forceinline__ void rows_dot(const uint8_t *base, size_t unit_stride, size_t rowbytes, int nr,
-                                         const float *xs, int KBp, int batch, float (&out)[RG * NB]) {
+// base + r * rowbytes; rows r >= nr are skipped.  Value index r * NB + b.
+template <int NB, int RG, bool WBF16>
+__device__ __forceinline__ void rows_dot(const uint8_t *base, size_t rowbytes, int nr, const float *xs, int KBp,
+                                         int batch, float (&out)[RG * NB]) {
     constexpr int U = Unroll<NB, RG>::value;
     constexpr int EPP = WBF16 ? 8 : 4;
     const int lane = threadIdx.x & 31;
@@ -509,9 +505,8 @@ __device__ __forceinline__ void rows_dot(const uint8_t *base, size_t unit_stride
         for (int v = 0; v < RG * NB; v++) acc[u][v] = 0.f;
     const uint4 *rows[RG];
 #pragma unroll
-    for (int r = 0; r < RG; r++)
-        rows[r] = (const uint4 *)(base + (size_t)((r < nr ? r : 0) / RPU) * unit_stride +
-                                  (size_t)((r < nr ? r : 0) % RPU) * rowbytes);
+    for (int r = 0; r < RG; r++) rows[r] = (const uint4 *)(base + (size_t)(r < nr ? r : 0) * rowbytes);
+#pragma unroll 1
     for (int p0 = lane; p0 < pieces; p0 += 32 * U) {
         uint4 w[U][RG];
 #pragma unroll
@@ -568,125 +563,237 @@ __device__ __forceinline__ void rows_dot(const uint8_t *base, size_t unit_stride
     }
 }
 
-// ------------------------------------------------------------------ GEMV phases
+// ------------------------------------------------------------------ epilogues
 
-// One group of a warp's units: finish the dots and run the phase's epilogue.
+// 1 / rms of batch row b from the per-warp sums of squares.
+__device__ __forceinline__ float inv_rms(const Model &m, const float *ssp, int b) {
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; w++) ss += ssp[w * kMaxBatch + b];
+    return 1.0f / sqrtf(ss / (float)m.dim + m.norm_eps);
+}
+
+// QKV epilogue of one RoPE pair unit: (a, c) = rows (dim i, dim i + d/2) of sub-head s
+// of kv group g (s < G: query head g G + s; s = G: key; s = G + 1: value), already
+// scaled by 1/rms.  q and k are rotated; q is multiplied by log2(e) / sqrt(d) (scores in
+// base-2 units); k and v are rounded to the cache type and appended at the row's
+// position.  Every value is published for the attention items.
+__device__ __forceinline__ void qkv_pair_epilogue(const StepParams &P, int layer, int b, int unit, float a, float c) {
+    const Model &m = P.m;
+    const int hd = m.head_dim, half = hd >> 1, G = m.n_heads / m.n_kv_heads;
+    const int per_group = (G + 2) * half;
+    const int g = unit / per_group, rem = unit - g * per_group;
+    const int s = rem / half, i = rem - s * half;
+    const int pos = P.pos[b];
+    float o0 = a, o1 = c;
+    if (s <= G) {
+        const float cs = m.rope[((size_t)pos * half + i) * 2], sn = m.rope[((size_t)pos * half + i) * 2 + 1];
+        o0 = a * cs - c * sn;
+        o1 = a * sn + c * cs;
+    }
+    if (s < G) {
+        const float qscale = rsqrtf((float)hd) * 1.4426950408889634f;
+        o0 *= qscale;
+        o1 *= qscale;
+    } else {
+        const bool bf = m.kv_bf16;
+        const size_t rowbytes = (size_t)hd * (bf ? 2 : 4);
+        uint8_t *row = (s == G ? m.kc : m.vc) +
+                       ((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + pos) * rowbytes;
+        if (bf) {
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(o0), h1 = __float2bfloat16_rn(o1);
+            ((__nv_bfloat16 *)row)[i] = h0;
+            ((__nv_bfloat16 *)row)[i + half] = h1;
+            o0 = __bfloat162float(h0);
+            o1 = __bfloat162float(h1);
+        } else {
+            ((float *)row)[i] = o0;
+            ((float *)row)[i + half] = o1;
+        }
+    }
+    uint64_t *dst = m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + ((size_t)g * (G + 2) + s) * hd;
+    ll_store(dst + i, o0, P.tag);
+    ll_store(dst + i + half, o1, P.tag);
+}
+
+// A logits candidate this lane holds after a group (v = -inf: none).
+struct Cand {
+    float v;
+    int i, b;
+};
+
+// One group of RG rows (RPU = 1) or RG / 2 pair units (RPU = 2) of a warp's chunk: the
+// dots, then the phase's epilogue.  j0 / ng: first unit and unit count of the group
+// within the chunk; c_unit0: the chunk's first unit within the CTA's slice.
 template <int NB, int RG, int RPU, bool WBF16>
-__device__ __forceinline__ void gemv_group(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
-                                           const uint8_t *buf, int j0, int ng, int c_unit0, int c_kt, int u0,
-                                           float (&best_v)[NB], int (&best_i)[NB]) {
+__device__ __forceinline__ Cand gemv_group(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
+                                        const uint8_t *buf, int j0, int ng, int c_unit0, int c_kt, int u0) {
     constexpr int V = RG * NB;
     constexpr int SHIFT = 5 - Log2<V>::value;
     const Model &m = P.m;
     const int lane = threadIdx.x & 31;
     const int batch = P.batch;
     const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
-    const size_t unit_stride = (size_t)RPU * rowbytes;  // the group's units are consecutive
+    Cand cd{-INFINITY, 0, 0};
     float acc[V];
-    rows_dot<NB, RG, RPU, WBF16>(buf + (size_t)j0 * RPU * rowbytes, unit_stride, rowbytes, ng * RPU, S.xs, M.KBp,
-                                 batch, acc);
+    rows_dot<NB, RG, WBF16>(buf + (size_t)j0 * RPU * rowbytes, rowbytes, ng * RPU, S.xs, M.KBp, batch, acc);
     const float val = reduce_scatter<V>(acc);
-    const int idx = lane >> SHIFT;              // value held by this lane
+    const int idx = lane >> SHIFT;  // value held by this lane
     const bool holder = (lane & ((1 << SHIFT) - 1)) == 0;
-    const int r = idx / NB, b = idx - r * NB;   // group row, batch row
+    const int r = idx / NB, b = idx - r * NB;  // group row, batch row
     const uint32_t tag = P.tag;
-    if (epi == EPI_W13) {  // rows (2u, 2u + 1) = (gate, up) of group unit u
-        const float up = __shfl_sync(0xffffffffu, val, ((idx + NB) << SHIFT) & 31);
+    if constexpr (RPU == 2) {  // pair units: (gate, up) of W1/W3; (dim i, dim i + d/2) of QKV
+        const float second = __shfl_sync(0xffffffffu, val, ((idx + NB) << SHIFT) & 31);
         const int u = r >> 1;
-        if (holder && (r & 1) == 0 && u < ng && b < batch) {
-            const int unit = u0 + c_unit0 + j0 + u;
-            const float s = val / (1.0f + __expf(-val));
-            ll_store(m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit, s * up, tag);
+        if (!holder || (r & 1) || u >= ng || b >= batch) return cd;
+        const int unit = u0 + c_unit0 + j0 + u;
+        const float rs = inv_rms(m, S.ssp, b);
+        const float x1 = val * rs, x2 = second * rs;
+        if (epi == EPI_W13) {
+            const float s = x1 / (1.0f + __expf(-x1));
+            ll_store(m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit, s * x2, tag);
+        } else {
+            qkv_pair_epilogue(P, layer, b, unit, x1, x2);
         }
-        return;
-    }
-    if (!holder || r >= ng || b >= batch) return;
-    const int i = c_unit0 + j0 + r;  // unit within the CTA's slice
-    const int unit = u0 + i;
-    float v = val;
-    if (M.nkt > 1) {  // accumulate this K tile; finish after the last one
-        float *a = S.accs + (size_t)i * kMaxBatch + b;
-        v = (c_kt == 0 ? 0.f : *a) + v;
-        *a = v;
-        if (c_kt != M.nkt - 1) return;
-    }
-    if (epi == EPI_QKV) {
-        ll_store(m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + unit, v, tag);
-    } else if (epi == EPI_WO || epi == EPI_W2) {
+        return cd;
+    } else {
+        if (!holder || r >= ng || b >= batch) return cd;
+        const int i = c_unit0 + j0 + r;  // unit within the CTA's slice
+        const int unit = u0 + i;
+        float v = val;
+        if (epi == EPI_LOGITS) {
+            v *= inv_rms(m, S.ssp, b);
+            if (P.logits) P.logits[(size_t)b * m.vocab + unit] = v;
+            if (v != v) {
+                atomicOr(m.status, kStNanLogits);
+            } else {
+                cd.v = v;
+                cd.i = unit;
+                cd.b = b;
+            }
+            return cd;
+        }
+        if (M.nkt > 1) {  // accumulate this K tile; finish after the last one
+            float *a = S.accs + (size_t)i * kMaxBatch + b;
+            v = (c_kt == 0 ? 0.f : *a) + v;
+            *a = v;
+            if (c_kt != M.nkt - 1) return cd;
+        }
+        // Wo / W2: residual add on the owned row, publish the new residual
         float *own = S.xown + b * kMaxOwn + i;
         const float xn = *own + v;
         *own = xn;
         uint64_t *dst = epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim) : m.ll_x + ll_layer(P, layer + 1, m.dim);
         ll_store(dst + (size_t)b * m.dim + unit, xn, tag);
-    } else {  // logits: rows of one lane's value increase, so a strict > keeps the lowest index
-        if (P.logits) P.logits[(size_t)b * m.vocab + unit] = v;
-        if (v != v) {
-            atomicOr(m.status, kStNanLogits);
-        } else {
-#pragma unroll
-            for (int bb = 0; bb < NB; bb++)
-                if (bb == b && (v > best_v[bb] || (v == best_v[bb] && unit < best_i[bb]))) {
-                    best_v[bb] = v;
-                    best_i[bb] = unit;
-                }
-        }
+        return cd;
     }
 }
 
-template <int NB, bool WBF16>
-__device__ void gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
-                           uint32_t &chunk_i, float (&best_v)[NB], int (&best_i)[NB], int tslot) {
-    constexpr int R = GemvShape<NB>::R;
-    constexpr int RW = R < 2 ? 2 : R;  // W1/W3: whole (gate, up) pairs
+// ------------------------------------------------------------------ GEMV phases
+
+template <int NB>
+__device__ __forceinline__ void keep_best(const Cand &cd, float (&best_v)[NB], int (&best_i)[NB]) {
+#pragma unroll
+    for (int bb = 0; bb < NB; bb++)
+        if (bb == cd.b && (cd.v > best_v[bb] || (cd.v == best_v[bb] && cd.i < best_i[bb]))) {
+            best_v[bb] = cd.v;
+            best_i[bb] = cd.i;
+        }
+}
+
+// The chunks of one matrix for this CTA, K tile by K tile: chunk i of the step belongs
+// to warp i % 8; with a multiple of 8 ring slots every use of a slot belongs to the same
+// warp, which takes them in order.  Each warp goes straight to its own chunks, and
+// waits for its first one's weights before the input is polled (the producer is far
+// enough ahead that they are normally resident).  Returns the updated chunk counter.
+// For the logits, each lane keeps the best (value, index) per batch row.
+template <int NB, bool WBF16, bool LOGITS>
+__device__ __forceinline__ uint32_t walk_chunks(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
+                                                uint32_t chunk_i, int tslot, float (&best_v)[NB], int (&best_i)[NB]) {
+    // Row groups: at batch 1 only the logits have chunks of several rows (a CTA's share
+    // of the layer matrices is a few rows, one per chunk), so the layer phases keep a
+    // single group shape there and the code stays small.
+    constexpr int R = (NB == 1 && !LOGITS) ? 1 : GemvShape<NB>::R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
     unit_range(M.rows / M.rows_per_unit, P.grid, blockIdx.x, u0, u1);
     trace_mark(P, tslot, 0);
-    if (u0 == u1) return;
-    int cur_kt = -1;
-    for_each_chunk(M, layer, WBF16 ? 2 : 4, blockIdx.x, P.grid, [&](const Chunk &c) {
-        if (c.kt != cur_kt) {
-            stage_input(P, epi, layer, M, c.kt, S);
-            if (cur_kt < 0) trace_mark(P, tslot, 1);
-            cur_kt = c.kt;
-        }
-        // chunk i belongs to warp i % 8; with a multiple of 8 slots every use of a slot
-        // belongs to the same warp, which takes them in order
-        if ((int)(chunk_i % kComputeWarps) == warp) {
-            const uint32_t slot = chunk_i % (uint32_t)P.ring_slots, parity = (chunk_i / (uint32_t)P.ring_slots) & 1;
-            wait_slot(P, &S.full[slot], parity);
+    if (u0 == u1) return chunk_i;
+    const int cu = M.rows_per_chunk / M.rows_per_unit;  // units per chunk
+    const int cpk = (u1 - u0 + cu - 1) / cu;            // chunks per K tile
+    const int nch = M.nkt * cpk;
+    const uint32_t slots = (uint32_t)P.ring_slots;
+    // this warp's chunks of the phase: j, j + 8, ...; j < 8 <= slots, so the first one
+    // never waits for a chunk consumed after the poll
+    int j = (warp - (int)(chunk_i & 7)) & 7;
+    if (j < nch) {
+        const uint32_t ci = chunk_i + (uint32_t)j;
+        wait_slot(P, &S.full[ci % slots], (ci / slots) & 1);
+    }
+#pragma unroll 1
+    for (int kt = 0; kt < M.nkt; kt++) {
+        stage_input(P, epi, layer, M, kt, S);
+        if (kt == 0) trace_mark(P, tslot, 1);
+#pragma unroll 1
+        for (; j < nch && j < (kt + 1) * cpk; j += kComputeWarps) {
+            const uint32_t ci = chunk_i + (uint32_t)j;
+            const uint32_t slot = ci % slots;
+            wait_slot(P, &S.full[slot], (ci / slots) & 1);
+            const int unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0);
             const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
-            if (epi == EPI_W13) {
-                for (int j = 0; j < c.nunits; j += RW / 2)
-                    gemv_group<NB, RW, 2, WBF16>(P, epi, layer, M, S, buf, j, min(RW / 2, c.nunits - j), c.unit0,
-                                                 c.kt, u0, best_v, best_i);
-            } else {  // groups of R rows, then of 2, then single rows: no idle accumulators
-                int j = 0;
-                for (; j + R <= c.nunits; j += R)
-                    gemv_group<NB, R, 1, WBF16>(P, epi, layer, M, S, buf, j, R, c.unit0, c.kt, u0, best_v, best_i);
-                if constexpr (R > 2) {
-                    for (; j + 2 <= c.nunits; j += 2)
-                        gemv_group<NB, 2, 1, WBF16>(P, epi, layer, M, S, buf, j, 2, c.unit0, c.kt, u0, best_v, best_i);
+            if (M.rows_per_unit == 2) {
+#pragma unroll 1
+                for (int g = 0; g < nunits; g++)
+                    gemv_group<NB, 2, 2, WBF16>(P, epi, layer, M, S, buf, g, 1, unit0, kt, u0);
+            } else {
+                int g = 0;
+#pragma unroll 1
+                for (; g + R <= nunits; g += R) {
+                    const Cand cd = gemv_group<NB, R, 1, WBF16>(P, epi, layer, M, S, buf, g, R, unit0, kt, u0);
+                    if constexpr (LOGITS) keep_best<NB>(cd, best_v, best_i);
                 }
-                for (; j < c.nunits; j++)
-                    gemv_group<NB, 1, 1, WBF16>(P, epi, layer, M, S, buf, j, 1, c.unit0, c.kt, u0, best_v, best_i);
+                if constexpr (R > 1) {
+#pragma unroll 1
+                    for (; g < nunits; g++) {
+                        const Cand cd = gemv_group<NB, 1, 1, WBF16>(P, epi, layer, M, S, buf, g, 1, unit0, kt, u0);
+                        if constexpr (LOGITS) keep_best<NB>(cd, best_v, best_i);
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.empty[slot]);
         }
-        chunk_i++;
-    });
+    }
+    if (P.trace) compute_sync();  // the timeline's "done" covers every warp
     trace_mark(P, tslot, 2);
+    return chunk_i + (uint32_t)nch;
 }
 
-// Per-warp, then per-CTA argmax candidates; CTA 0 collects every CTA's candidate.
-template <int NB>
-__device__ void finish_argmax(const StepParams &P, Shared &S, float (&best_v)[NB], int (&best_i)[NB]) {
+template <int NB, bool WBF16>
+__device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
+                                            uint32_t chunk_i, int tslot) {
+    float bv[NB];
+    int bi[NB];
+    return walk_chunks<NB, WBF16, false>(P, epi, layer, M, S, chunk_i, tslot, bv, bi);
+}
+
+// The logits and the greedy argmax: per lane, per warp, per CTA best candidates (lowest
+// index on ties); CTA 0 collects every CTA's candidate.
+template <int NB, bool WBF16>
+__device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uint32_t chunk_i, int tslot) {
     const Model &m = P.m;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int batch = P.batch;
+    float best_v[NB];
+    int best_i[NB];
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+        best_v[b] = -INFINITY;
+        best_i[b] = 0x7fffffff;
+    }
+    walk_chunks<NB, WBF16, true>(P, EPI_LOGITS, 0, m.emb, S, chunk_i, tslot, best_v, best_i);
+    trace_mark(P, tslot + 1, 0);
     compute_sync();  // the logits phase is done with S.xs
-    // each lane holds candidates for some rows: reduce over the warp (lowest index on ties)
 #pragma unroll
     for (int b = 0; b < NB; b++) {
         float v = best_v[b];
@@ -721,53 +828,58 @@ __device__ void finish_argmax(const StepParams &P, Shared &S, float (&best_v)[NB
         ll_store(dst, bv, P.tag);
         ll_store(dst + 1, __int_as_float(bi), P.tag);
     }
-    if (blockIdx.x != 0) return;
-    // CTA 0: poll [batch][grid][2] words into shared memory, reduce per row
-    ll_poll(P, m.ll_amax, P.grid * 2, batch, P.grid * 2, S.xs, P.grid * 2, P.tag);
-    if (tid < batch) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        const float *r = S.xs + (size_t)tid * P.grid * 2;
-        for (int c = 0; c < P.grid; c++) {
-            float v = r[2 * c];
-            int i = __float_as_int(r[2 * c + 1]);
-            if (v > bv || (v == bv && i < bi)) {
-                bv = v;
-                bi = i;
+    if (blockIdx.x == 0) {
+        // CTA 0: poll [batch][grid][2] words into shared memory, reduce per row
+        poll_words(P, m.ll_amax, P.grid * 2, batch, P.grid * 2, S.xs, P.grid * 2, 0, nullptr, nullptr);
+        if (tid < batch) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            const float *r = S.xs + (size_t)tid * P.grid * 2;
+            for (int c = 0; c < P.grid; c++) {
+                float v = r[2 * c];
+                int i = __float_as_int(r[2 * c + 1]);
+                if (v > bv || (v == bv && i < bi)) {
+                    bv = v;
+                    bi = i;
+                }
             }
+            if (bi == 0x7fffffff) bi = 0;  // all NaN: the status word already records it
+            if (P.next_ids) P.next_ids[tid] = bi;
         }
-        if (bi == 0x7fffffff) bi = 0;  // all NaN: the status word already records it
-        if (P.next_ids) P.next_ids[tid] = bi;
     }
+    trace_mark(P, tslot + 1, 2);
 }
 
 // ------------------------------------------------------------------ attention phase
 
-template <bool KVBF16>
-__device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, Shared &S) {
+// One work item: the query heads of kv group g of batch row b against positions
+// [t0, t1) of chunk c.  q arrives rotated and scaled from the QKV epilogue; the chunk
+// that ends at the new position also takes that position's key and value from the
+// exchange words (the cache copy written by the QKV epilogue is for later steps).
+__device__ __forceinline__ void attn_item(const StepParams &P, int layer, int b, int g, int c, Shared &S) {
     const Model &m = P.m;
     const int tid = threadIdx.x;
+    const bool kvbf16 = m.kv_bf16;
     const int hd = m.head_dim, H = m.n_heads, KV = m.n_kv_heads, G = H / KV;
-    const int half = hd / 2, qrows = m.qkv.rows;
+    const int qrows = m.qkv.rows;
     const int pos = P.pos[b], ctx = pos + 1, seq = P.seq[b];
     const int CH = P.attn_chunk, nc = P.nchunk[b];
     const int t0 = c * CH, t1 = min(ctx, t0 + CH);
-    const size_t rowbytes = (size_t)hd * (KVBF16 ? 2 : 4);
+    const size_t rowbytes = (size_t)hd * (kvbf16 ? 2 : 4);
     const size_t head_off = ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq) * rowbytes;
-    uint8_t *kbase = m.kc + head_off;
-    uint8_t *vbase = m.vc + head_off;
-    const float *rope = m.rope + (size_t)pos * half * 2;
-    const uint64_t *qkv = m.ll_qkv + ll_layer(P, layer, qrows) + (size_t)b * qrows;
+    const uint8_t *kbase = m.kc + head_off;
+    const uint8_t *vbase = m.vc + head_off;
+    const uint64_t *qkv = m.ll_qkv + ll_layer(P, layer, qrows) + (size_t)b * qrows + (size_t)g * (G + 2) * hd;
     const bool appends = t1 == ctx;  // this chunk ends at the new position
 
-    // Shared scratch after attn_core's: the group's raw [q heads; k; v] rows, then
-    // (when it fits) a copy of the chunk's cached keys and values.  The cached rows do
-    // not depend on this step, so their copy starts before waiting for q.
+    // Shared scratch after attn_core's: the group's [q heads; k; v] rows, then (when it
+    // fits) a copy of the chunk's cached keys and values, else the new position's row.
+    // The cached rows do not depend on this step, so their copy starts before the poll.
     float *raw = S.xs + kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2);
     uint8_t *kst = (uint8_t *)(raw + (size_t)(G + 2) * hd);
     const int tc = appends ? pos : t1;  // cached positions [t0, tc) of this chunk
     const bool stage = (size_t)(t1 - t0) * rowbytes * 2 <= (size_t)P.attn_stage_bytes;
-    uint8_t *vst = kst + (size_t)(t1 - t0) * rowbytes;
+    uint8_t *vst = kst + (size_t)(stage ? t1 - t0 : 1) * rowbytes;
     compute_sync();  // the previous item is done with the scratch
     if (stage) {
         const int per_row = (int)(rowbytes / 16), n16 = (tc - t0) * per_row;
@@ -777,50 +889,33 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
             cp_async16(vst + off, vbase + (size_t)t0 * rowbytes + off);
         }
     }
-    // one contiguous range: this group's q heads, then its k and v rows
-    ll_poll(P, qkv + (size_t)g * (G + 2) * hd, hd, G + 2, hd, raw, hd, P.tag);
-    if (appends) {
-        uint8_t *kd = kbase + (size_t)pos * rowbytes;
-        uint8_t *vd = vbase + (size_t)pos * rowbytes;
-        uint8_t *ks = kst + (size_t)(pos - t0) * rowbytes;
-        uint8_t *vs = vst + (size_t)(pos - t0) * rowbytes;
+    poll_words(P, qkv, hd, appends ? G + 2 : G, hd, raw, hd, 0, nullptr, nullptr);
+    trace_mark(P, layer * kTracePerLayer + 1, 1);
+    if (appends) {  // the new row, in the cache type (already rounded by the producer)
+        uint8_t *kd = kst + (size_t)(stage ? pos - t0 : 0) * rowbytes;
+        uint8_t *vd = vst + (size_t)(stage ? pos - t0 : 0) * rowbytes;
         const float *kr = raw + (size_t)G * hd, *vr = raw + (size_t)(G + 1) * hd;
-        for (int i = tid; i < half; i += kComputeThreads) {
-            float cs = __ldg(rope + 2 * i), sn = __ldg(rope + 2 * i + 1);
-            float a = kr[i], bb = kr[i + half];
-            float k0 = kv_round(a * cs - bb * sn, KVBF16), k1 = kv_round(a * sn + bb * cs, KVBF16);
-            float v0 = kv_round(vr[i], KVBF16), v1 = kv_round(vr[i + half], KVBF16);
-            if (KVBF16) {
-                ((__nv_bfloat16 *)kd)[i] = __float2bfloat16_rn(k0);
-                ((__nv_bfloat16 *)kd)[i + half] = __float2bfloat16_rn(k1);
-                ((__nv_bfloat16 *)vd)[i] = __float2bfloat16_rn(v0);
-                ((__nv_bfloat16 *)vd)[i + half] = __float2bfloat16_rn(v1);
-                if (stage) {
-                    ((__nv_bfloat16 *)ks)[i] = __float2bfloat16_rn(k0);
-                    ((__nv_bfloat16 *)ks)[i + half] = __float2bfloat16_rn(k1);
-                    ((__nv_bfloat16 *)vs)[i] = __float2bfloat16_rn(v0);
-                    ((__nv_bfloat16 *)vs)[i + half] = __float2bfloat16_rn(v1);
-                }
+        for (int i = tid; i < hd; i += kComputeThreads) {
+            if (kvbf16) {
+                ((__nv_bfloat16 *)kd)[i] = __float2bfloat16_rn(kr[i]);
+                ((__nv_bfloat16 *)vd)[i] = __float2bfloat16_rn(vr[i]);
             } else {
-                ((float *)kd)[i] = k0;
-                ((float *)kd)[i + half] = k1;
-                ((float *)vd)[i] = v0;
-                ((float *)vd)[i + half] = v1;
-                if (stage) {
-                    ((float *)ks)[i] = k0;
-                    ((float *)ks)[i + half] = k1;
-                    ((float *)vs)[i] = v0;
-                    ((float *)vs)[i + half] = v1;
-                }
+                ((float *)kd)[i] = kr[i];
+                ((float *)vd)[i] = vr[i];
             }
         }
     }
-    if (stage) cp_async_wait_all();  // attn_core's first barrier publishes the copies
+    if (stage) cp_async_wait_all();
+    compute_sync();  // staged rows and the new row are visible to every warp
     AttnTask T;
-    T.q = raw;  // read by attn_core after its first barrier
-    T.rope = rope;
+    T.q = raw;
+    T.q_ready = true;
+    T.kv_bf16 = kvbf16;
     T.kbase = stage ? kst - (size_t)t0 * rowbytes : kbase;
     T.vbase = stage ? vst - (size_t)t0 * rowbytes : vbase;
+    T.tail_k = kst;
+    T.tail_v = vst;
+    T.tail_t = (appends && !stage) ? pos : -1;
     T.out = nullptr;
     const size_t pl = (size_t)layer * m.max_batch + b;
     T.part = m.part + (pl * H + (size_t)g * G) * kMaxChunksPerSeq * (hd + 2);
@@ -835,11 +930,10 @@ __device__ void attn_item(const StepParams &P, int layer, int b, int g, int c, S
     T.t1 = t1;
     T.nc = nc;
     T.c = c;
-    attn_core<KVBF16>(T, S.xs, &S.flags[0]);
+    attn_core(T, S.xs, &S.flags[0]);
 }
 
-template <bool KVBF16>
-__device__ void attention_phase(const StepParams &P, int layer, Shared &S) {
+__device__ __forceinline__ void attention_phase(const StepParams &P, int layer, Shared &S) {
     const int tslot = layer * kTracePerLayer + 1;
     trace_mark(P, tslot, 0);
     const int total = P.item_start[P.batch];
@@ -850,8 +944,9 @@ __device__ void attention_phase(const StepParams &P, int layer, Shared &S) {
         const int local = item - P.item_start[b];
         const int nc = P.nchunk[b];
         const int g = local / nc, c = local - g * nc;
-        if (g < KV) attn_item<KVBF16>(P, layer, b, g, c, S);
+        if (g < KV) attn_item(P, layer, b, g, c, S);
     }
+    if (P.trace) compute_sync();
     trace_mark(P, tslot, 2);
 }
 
@@ -876,32 +971,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
     const Model &m = P.m;
     uint32_t chunk_i = 0;
-    float best_v[NB];
-    int best_i[NB];
-#pragma unroll
-    for (int b = 0; b < NB; b++) {
-        best_v[b] = -INFINITY;
-        best_i[b] = 0x7fffffff;
-    }
     init_residual(P, S);
+#pragma unroll 1
     for (int l = 0; l < m.n_layers; l++) {
-        const int t = l * kTracePerLayer;
-        gemv_phase<NB, WBF16>(P, EPI_QKV, l, m.qkv, S, chunk_i, best_v, best_i, t);
-        if (m.kv_bf16)
-            attention_phase<true>(P, l, S);
-        else
-            attention_phase<false>(P, l, S);
-        gemv_phase<NB, WBF16>(P, EPI_WO, l, m.wo, S, chunk_i, best_v, best_i, t + 2);
-        gemv_phase<NB, WBF16>(P, EPI_W13, l, m.w13, S, chunk_i, best_v, best_i, t + 3);
-        gemv_phase<NB, WBF16>(P, EPI_W2, l, m.w2, S, chunk_i, best_v, best_i, t + 4);
+        // phases: QKV, attention, Wo, W1/W3, W2; the four GEMV phases share one body
+#pragma unroll 1
+        for (int ph = 0; ph < kTracePerLayer; ph++) {
+            const int t = l * kTracePerLayer + ph;
+            if (ph == 1) {
+                attention_phase(P, l, S);
+                continue;
+            }
+            const int epi = ph == 0 ? EPI_QKV : ph == 2 ? EPI_WO : ph == 3 ? EPI_W13 : EPI_W2;
+            const Mat M = ph == 0 ? m.qkv : ph == 2 ? m.wo : ph == 3 ? m.w13 : m.w2;
+            chunk_i = gemv_phase<NB, WBF16>(P, epi, l, M, S, chunk_i, t);
+        }
     }
-    if (P.do_logits) {
-        const int t = m.n_layers * kTracePerLayer;
-        gemv_phase<NB, WBF16>(P, EPI_LOGITS, 0, m.emb, S, chunk_i, best_v, best_i, t);
-        trace_mark(P, t + 1, 0);
-        finish_argmax<NB>(P, S, best_v, best_i);
-        trace_mark(P, t + 1, 2);
-    }
+    if (P.do_logits) logits_phase<NB, WBF16>(P, S, chunk_i, m.n_layers * kTracePerLayer);
 }
 
 // ------------------------------------------------------------------ host-side launch

@@ -62,6 +62,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Hint: bring the line holding p into L1.
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Named barrier 1 over the kComputeThreads arithmetic threads (the streaming warp of
 // the decode kernel never joins it).
 __device__ __forceinline__ void compute_sync() {

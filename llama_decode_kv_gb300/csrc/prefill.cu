@@ -78,20 +78,26 @@ __global__ void rmsnorm_bf16_kernel(const float *x, const float *g, uint16_t *ou
 }
 
 // RoPE of q (in place) and k; k and v of positions p0 + t appended to the cache.
-// qkv rows are grouped per kv head: [q heads g*G .. g*G+G-1; k; v].
+// qkv rows are grouped per kv head, [q heads g*G .. g*G+G-1; k; v], each head's columns
+// in RoPE pairs (column 2i = dim i, column 2i + 1 = dim i + hd/2, the weights' stored
+// order).  The row is read into shared memory first and written back in natural order.
 template <bool KVBF16>
 __global__ void rope_append_kernel(const Model m, float *qkv, int layer, int seq, int p0) {
+    extern __shared__ float rowbuf[];  // [qkv.rows]
     const int t = blockIdx.x, pos = p0 + t;
     const int hd = m.head_dim, half = hd / 2, KV = m.n_kv_heads, G = m.n_heads / KV;
     const float *rope = m.rope + (size_t)pos * half * 2;
     float *row = qkv + (size_t)t * m.qkv.rows;
     const size_t rowbytes = (size_t)hd * (KVBF16 ? 2 : 4);
+    for (int e = threadIdx.x; e < m.qkv.rows; e += blockDim.x) rowbuf[e] = row[e];
+    __syncthreads();
     for (int e = threadIdx.x; e < KV * (G + 2) * half; e += blockDim.x) {
         const int g = e / ((G + 2) * half), r = e - g * (G + 2) * half;
         const int j = r / half, i = r - j * half;  // head slot j in the group: q (< G), k (= G), v (= G + 1)
-        float *h = row + ((size_t)g * (G + 2) + j) * hd;
+        const size_t h0 = ((size_t)g * (G + 2) + j) * hd;
+        float *h = row + h0;
         const float cs = rope[2 * i], sn = rope[2 * i + 1];
-        const float a = h[i], b = h[i + half];
+        const float a = rowbuf[h0 + 2 * i], b = rowbuf[h0 + 2 * i + 1];
         if (j <= G) {
             const float a2 = a * cs - b * sn, b2 = a * sn + b * cs;
             if (j < G) {
@@ -233,7 +239,7 @@ __global__ void argmax_kernel(const float *v, int n, int *out, int *status) {
 
 bool prefill_supported(const Model &m) {
     return m.weight_bf16 && m.kv_bf16 && m.dim % 64 == 0 && (m.n_heads * m.head_dim) % 64 == 0 &&
-           m.hidden % 8 == 0 && (m.head_dim == 64 || m.head_dim == 128);
+           m.hidden % 8 == 0 && (m.head_dim == 64 || m.head_dim == 128) && (size_t)m.qkv.rows * 4 <= 48 * 1024;
 }
 
 static cudaError_t weight_map(CUtensorMap *map, const Mat &M, int layer) {
@@ -301,7 +307,7 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
             rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(p.x, gn, p.xn, xlo, m.dim, m.norm_eps);
             PF_CK(gemm(p.xn_map, p.xn_lo_map, p.maps[4 * l + 0], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
                        m.qkv.rows, m.status, s));
-            rope_append_kernel<true><<<T, 256, 0, s>>>(m, p.qkv, l, seq, p0);
+            rope_append_kernel<true><<<T, 256, (size_t)m.qkv.rows * 4, s>>>(m, p.qkv, l, seq, p0);
             dim3 ag((T + 63) / 64, m.n_heads);
             if (m.head_dim == 64)
                 attn_prefill_kernel<64, true><<<ag, 256, 0, s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);

@@ -282,7 +282,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     // least 16) takes the rest.  The grid is one CTA per SM.
     c->grid = sms;
     const int grid = c->grid;
-    if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) || !plan_mat(m.qkv, qkv_rows, dim, 1, esz, B, false, grid) ||
+    if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) || !plan_mat(m.qkv, qkv_rows, dim, 2, esz, B, false, grid) ||
         !plan_mat(m.wo, dim, qd, 1, esz, B, true, grid) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, grid) ||
         !plan_mat(m.w2, dim, hid, 1, esz, B, true, grid))
         return fail(c, SLM_EUNSUPPORTED,
@@ -350,15 +350,22 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     for (int l = 0; l < L; l++) {
         const uint8_t *an = take(dim);
         for (int i = 0; i < dim; i++) norms[(size_t)l * 2 * dim + i] = widen(an, esz, i);
-        // QKV rows grouped by kv head: [q heads g*G .. g*G+G-1; k head g; v head g]
+        // QKV rows grouped by kv head: [q heads g*G .. g*G+G-1; k head g; v head g], and
+        // within each head in RoPE pairs: stored rows 2i, 2i + 1 = dims i, i + hd/2
         uint8_t *qkv = h.data() + off_qkv + (size_t)l * m.qkv.layer_stride;
         const uint8_t *wq = take((size_t)qd * dim), *wk = take((size_t)kvd * dim), *wv = take((size_t)kvd * dim);
-        const int G = H / KV;
+        const int G = H / KV, half = hd / 2;
+        auto pack_head = [&](int dst0, const uint8_t *src) {
+            for (int i = 0; i < half; i++) {
+                pack_rows(qkv, m.qkv, dst0 + 2 * i, src + (size_t)i * dim * esz, 1, esz);
+                pack_rows(qkv, m.qkv, dst0 + 2 * i + 1, src + (size_t)(i + half) * dim * esz, 1, esz);
+            }
+        };
         for (int g = 0; g < KV; g++) {
             const int r0 = g * (G + 2) * hd;
-            pack_rows(qkv, m.qkv, r0, wq + (size_t)g * G * hd * dim * esz, G * hd, esz);
-            pack_rows(qkv, m.qkv, r0 + G * hd, wk + (size_t)g * hd * dim * esz, hd, esz);
-            pack_rows(qkv, m.qkv, r0 + (G + 1) * hd, wv + (size_t)g * hd * dim * esz, hd, esz);
+            for (int j = 0; j < G; j++) pack_head(r0 + j * hd, wq + (size_t)(g * G + j) * hd * dim * esz);
+            pack_head(r0 + G * hd, wk + (size_t)g * hd * dim * esz);
+            pack_head(r0 + (G + 1) * hd, wv + (size_t)g * hd * dim * esz);
         }
         pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, take((size_t)dim * qd), dim, esz);
         const uint8_t *fn = take(dim);
