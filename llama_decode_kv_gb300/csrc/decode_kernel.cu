@@ -206,7 +206,7 @@ __device__ __forceinline__ const Mat &phase_mat(const Model &m, int phase) {
 
 __device__ void cursor_enter(const StepParams &P, Cursor &c) {
     const Mat &M = phase_mat(P.m, c.phase);
-    unit_range(M.rows / M.rows_per_unit, P.grid, blockIdx.x, c.u0, c.u1);
+    phase_slice(P, c.phase, M.rows / M.rows_per_unit, blockIdx.x, c.u0, c.u1);
     c.kt = 0;
     c.u = c.u0;
 }
@@ -313,7 +313,7 @@ __device__ __forceinline__ size_t ll_layer(const StepParams &P, int layer, int p
 __device__ __forceinline__ void init_residual(const StepParams &P, Shared &S) {
     const Model &m = P.m;
     int r0, r1;
-    unit_range(m.dim, P.grid, blockIdx.x, r0, r1);
+    phase_slice(P, 1, m.dim, blockIdx.x, r0, r1);
     for (int b = 0; b < P.batch; b++) {
         int tok = token_of(P, b);
         for (int i = threadIdx.x; i < r1 - r0; i += kComputeThreads)
@@ -486,73 +486,98 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[V]) {
 // Independent accumulator chains per (row, batch row): enough to keep the FMA pipe and
 // the shared-memory loads busy with two warps per scheduler.
 template <int NB, int RG> struct Unroll {
-    static constexpr int value = RG * NB >= 8 ? 1 : RG * NB >= 4 ? 2 : 4;
+    static constexpr int value = RG * NB >= 8 ? 1 : RG * NB >= 4 ? 2 : 3;
 };
 
-// Dots of RG weight rows with every staged batch row.  Group row r lives at
-// base + r * rowbytes; rows r >= nr are skipped.  Value index r * NB + b.
+// A lane's first U pieces of each of a group's RG weight rows, held in registers: for
+// the layer phases they are loaded before the input vector is polled.
 template <int NB, int RG, bool WBF16>
-__device__ __forceinline__ void rows_dot(const uint8_t *base, size_t rowbytes, int nr, const float *xs, int KBp,
-                                         int batch, float (&out)[RG * NB]) {
+struct GroupW {
+    static constexpr int U = Unroll<NB, RG>::value;
+    uint4 w[U][RG];
+};
+
+// Row r of the group at base + r * rowbytes; rows >= nr read as zero.
+template <int NB, int RG, bool WBF16>
+__device__ __forceinline__ void load_pieces(uint4 (&w)[Unroll<NB, RG>::value][RG], const uint8_t *base, size_t rowbytes,
+                                            int nr, int p0, int pieces) {
+#pragma unroll
+    for (int u = 0; u < Unroll<NB, RG>::value; u++)
+#pragma unroll
+        for (int r = 0; r < RG; r++) {
+            const int p = p0 + 32 * u;
+            w[u][r] = (p < pieces && r < nr) ? ((const uint4 *)(base + (size_t)r * rowbytes))[p] : make_uint4(0, 0, 0, 0);
+        }
+}
+
+// acc[u][r * NB + b] += piece (p0 + 32 u) of row r . the same piece of staged row b.
+template <int NB, int RG, bool WBF16>
+__device__ __forceinline__ void fma_pieces(const uint4 (&w)[Unroll<NB, RG>::value][RG], int p0, int pieces,
+                                           const float *xs, int KBp, int batch,
+                                           float (&acc)[Unroll<NB, RG>::value][RG * NB]) {
     constexpr int U = Unroll<NB, RG>::value;
     constexpr int EPP = WBF16 ? 8 : 4;
+    (void)EPP;
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+        const int p = p0 + 32 * u;
+        if (p >= pieces) break;
+#pragma unroll
+        for (int b = 0; b < NB; b++) {
+            if (NB > 1 && b >= batch) break;
+            float x[EPP];
+            if constexpr (WBF16) {
+                const float *xr = xs + (size_t)b * KBp + p * 4;  // planes of xpos()
+                const float4 x0 = *(const float4 *)xr, x1 = *(const float4 *)(xr + (KBp >> 1));
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+            } else {
+                const float4 x0 = *(const float4 *)(xs + (size_t)b * KBp + p * 4);
+                x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+            }
+#pragma unroll
+            for (int r = 0; r < RG; r++) {
+                const uint4 q = w[u][r];
+                float &a = acc[u][r * NB + b];
+                if constexpr (WBF16) {
+                    a = fmaf(bf16_lo(q.x), x[0], a);
+                    a = fmaf(bf16_hi(q.x), x[1], a);
+                    a = fmaf(bf16_lo(q.y), x[2], a);
+                    a = fmaf(bf16_hi(q.y), x[3], a);
+                    a = fmaf(bf16_lo(q.z), x[4], a);
+                    a = fmaf(bf16_hi(q.z), x[5], a);
+                    a = fmaf(bf16_lo(q.w), x[6], a);
+                    a = fmaf(bf16_hi(q.w), x[7], a);
+                } else {
+                    a = fmaf(__uint_as_float(q.x), x[0], a);
+                    a = fmaf(__uint_as_float(q.y), x[1], a);
+                    a = fmaf(__uint_as_float(q.z), x[2], a);
+                    a = fmaf(__uint_as_float(q.w), x[3], a);
+                }
+            }
+        }
+    }
+}
+
+// Dots of RG weight rows with every staged batch row: the lane's first U pieces per row
+// come from G, the rest from shared memory.  Value index r * NB + b.
+template <int NB, int RG, bool WBF16>
+__device__ __forceinline__ void rows_dot(const GroupW<NB, RG, WBF16> &G, const uint8_t *base, size_t rowbytes, int nr,
+                                         const float *xs, int KBp, int batch, float (&out)[RG * NB]) {
+    constexpr int U = Unroll<NB, RG>::value;
     const int lane = threadIdx.x & 31;
-    const int pieces = KBp / EPP;
+    const int pieces = KBp / (WBF16 ? 8 : 4);
     float acc[U][RG * NB];
 #pragma unroll
     for (int u = 0; u < U; u++)
 #pragma unroll
         for (int v = 0; v < RG * NB; v++) acc[u][v] = 0.f;
-    const uint4 *rows[RG];
-#pragma unroll
-    for (int r = 0; r < RG; r++) rows[r] = (const uint4 *)(base + (size_t)(r < nr ? r : 0) * rowbytes);
+    fma_pieces<NB, RG, WBF16>(G.w, lane, pieces, xs, KBp, batch, acc);
 #pragma unroll 1
-    for (int p0 = lane; p0 < pieces; p0 += 32 * U) {
+    for (int p0 = lane + 32 * U; p0 < pieces; p0 += 32 * U) {
         uint4 w[U][RG];
-#pragma unroll
-        for (int u = 0; u < U; u++)
-#pragma unroll
-            for (int r = 0; r < RG; r++)
-                w[u][r] = (p0 + 32 * u < pieces && r < nr) ? rows[r][p0 + 32 * u] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int p = p0 + 32 * u;
-            if (p >= pieces) break;
-#pragma unroll
-            for (int b = 0; b < NB; b++) {
-                if (NB > 1 && b >= batch) break;
-                float x[EPP];
-                if constexpr (WBF16) {
-                    const float *xr = xs + (size_t)b * KBp + p * 4;  // planes of xpos()
-                    const float4 x0 = *(const float4 *)xr, x1 = *(const float4 *)(xr + (KBp >> 1));
-                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-                    x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-                } else {
-                    const float4 x0 = *(const float4 *)(xs + (size_t)b * KBp + p * 4);
-                    x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-                }
-#pragma unroll
-                for (int r = 0; r < RG; r++) {
-                    const uint4 q = w[u][r];
-                    float &a = acc[u][r * NB + b];
-                    if constexpr (WBF16) {
-                        a = fmaf(bf16_lo(q.x), x[0], a);
-                        a = fmaf(bf16_hi(q.x), x[1], a);
-                        a = fmaf(bf16_lo(q.y), x[2], a);
-                        a = fmaf(bf16_hi(q.y), x[3], a);
-                        a = fmaf(bf16_lo(q.z), x[4], a);
-                        a = fmaf(bf16_hi(q.z), x[5], a);
-                        a = fmaf(bf16_lo(q.w), x[6], a);
-                        a = fmaf(bf16_hi(q.w), x[7], a);
-                    } else {
-                        a = fmaf(__uint_as_float(q.x), x[0], a);
-                        a = fmaf(__uint_as_float(q.y), x[1], a);
-                        a = fmaf(__uint_as_float(q.z), x[2], a);
-                        a = fmaf(__uint_as_float(q.w), x[3], a);
-                    }
-                }
-            }
-        }
+        load_pieces<NB, RG, WBF16>(w, base, rowbytes, nr, p0, pieces);
+        fma_pieces<NB, RG, WBF16>(w, p0, pieces, xs, KBp, batch, acc);
     }
 #pragma unroll
     for (int v = 0; v < RG * NB; v++) {
@@ -573,47 +598,82 @@ __device__ __forceinline__ float inv_rms(const Model &m, const float *ssp, int b
     return 1.0f / sqrtf(ss / (float)m.dim + m.norm_eps);
 }
 
-// QKV epilogue of one RoPE pair unit: (a, c) = rows (dim i, dim i + d/2) of sub-head s
-// of kv group g (s < G: query head g G + s; s = G: key; s = G + 1: value), already
-// scaled by 1/rms.  q and k are rotated; q is multiplied by log2(e) / sqrt(d) (scores in
-// base-2 units); k and v are rounded to the cache type and appended at the row's
-// position.  Every value is published for the attention items.
-__device__ __forceinline__ void qkv_pair_epilogue(const StepParams &P, int layer, int b, int unit, float a, float c) {
+// What the lane that will hold a group's value does with it; everything that does not
+// depend on the value is worked out before the input arrives.
+enum { EK_Q = 0, EK_K = 1, EK_V = 2, EK_W13 = 3, EK_RES = 4, EK_LOGITS = 5 };
+struct EpiCtx {
+    uint64_t *dst;   // exchange word this lane publishes (RoPE pair: the first; second at + half)
+    uint8_t *cache;  // key / value cache element of a RoPE pair's first dim
+    float cs, sn;    // RoPE of a q / k pair
+    int kind;        // EK_*
+    int half;        // RoPE pair: dims between its two elements
+    int own;         // Wo / W2: owned row within the CTA's slice; logits: vocabulary index
+    int b;           // batch row of the value; -1: this lane publishes nothing
+};
+
+// Group of RG rows (RPU = 1) or one RoPE / SwiGLU pair unit (RG = RPU = 2) starting at
+// unit j0 of a chunk whose first unit is unit0 of the CTA's slice [u0, ...); ng units.
+template <int NB, int RG, int RPU>
+__device__ __forceinline__ EpiCtx prepare_ctx(const StepParams &P, int epi, int layer, int u0, int unit0, int j0, int ng) {
+    constexpr int V = RG * NB;
+    constexpr int SHIFT = 5 - Log2<V>::value;
     const Model &m = P.m;
-    const int hd = m.head_dim, half = hd >> 1, G = m.n_heads / m.n_kv_heads;
-    const int per_group = (G + 2) * half;
-    const int g = unit / per_group, rem = unit - g * per_group;
-    const int s = rem / half, i = rem - s * half;
-    const int pos = P.pos[b];
-    float o0 = a, o1 = c;
-    if (s <= G) {
-        const float cs = m.rope[((size_t)pos * half + i) * 2], sn = m.rope[((size_t)pos * half + i) * 2 + 1];
-        o0 = a * cs - c * sn;
-        o1 = a * sn + c * cs;
-    }
-    if (s < G) {
-        const float qscale = rsqrtf((float)hd) * 1.4426950408889634f;
-        o0 *= qscale;
-        o1 *= qscale;
-    } else {
-        const bool bf = m.kv_bf16;
-        const size_t rowbytes = (size_t)hd * (bf ? 2 : 4);
-        uint8_t *row = (s == G ? m.kc : m.vc) +
-                       ((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + pos) * rowbytes;
-        if (bf) {
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(o0), h1 = __float2bfloat16_rn(o1);
-            ((__nv_bfloat16 *)row)[i] = h0;
-            ((__nv_bfloat16 *)row)[i + half] = h1;
-            o0 = __bfloat162float(h0);
-            o1 = __bfloat162float(h1);
-        } else {
-            ((float *)row)[i] = o0;
-            ((float *)row)[i + half] = o1;
+    const int lane = threadIdx.x & 31;
+    const int idx = lane >> SHIFT;  // value this lane holds after the reduction
+    const bool holder = (lane & ((1 << SHIFT) - 1)) == 0;
+    const int r = idx / NB, b = idx - r * NB;
+    EpiCtx c;
+    c.b = -1;
+    c.dst = nullptr;
+    c.cache = nullptr;
+    c.cs = 1.f;
+    c.sn = 0.f;
+    c.kind = EK_RES;
+    c.half = 0;
+    c.own = 0;
+    if constexpr (RPU == 2) {  // the lane of the pair's first row publishes
+        const int u = r >> 1;
+        if (!holder || (r & 1) || u >= ng || b >= P.batch) return c;
+        const int unit = u0 + unit0 + j0 + u;
+        c.b = b;
+        if (epi == EPI_W13) {
+            c.kind = EK_W13;
+            c.dst = m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit;
+            return c;
         }
+        const int hd = m.head_dim, half = hd >> 1, G = m.n_heads / m.n_kv_heads;
+        const int per_group = (G + 2) * half;
+        const int g = unit / per_group, rem = unit - g * per_group;
+        const int s = rem / half, i = rem - s * half;
+        const int pos = P.pos[b];
+        c.half = half;
+        c.kind = s < G ? EK_Q : s == G ? EK_K : EK_V;
+        if (s <= G) {
+            const float *rp = m.rope + ((size_t)pos * half + i) * 2;
+            c.cs = rp[0];
+            c.sn = rp[1];
+        }
+        if (s >= G) {
+            const int esz = m.kv_bf16 ? 2 : 4;
+            c.cache = (s == G ? m.kc : m.vc) +
+                      (((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + pos) * hd + i) * esz;
+        }
+        c.dst = m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + ((size_t)g * (G + 2) + s) * hd + i;
+        return c;
+    } else {
+        if (!holder || r >= ng || b >= P.batch) return c;
+        const int i = unit0 + j0 + r;  // unit within the CTA's slice
+        c.b = b;
+        c.own = i;
+        if (epi == EPI_LOGITS) {
+            c.kind = EK_LOGITS;
+            c.own = u0 + i;
+            return c;
+        }
+        c.dst = (epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim) : m.ll_x + ll_layer(P, layer + 1, m.dim)) +
+                (size_t)b * m.dim + u0 + i;
+        return c;
     }
-    uint64_t *dst = m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + ((size_t)g * (G + 2) + s) * hd;
-    ll_store(dst + i, o0, P.tag);
-    ll_store(dst + i + half, o1, P.tag);
 }
 
 // A logits candidate this lane holds after a group (v = -inf: none).
@@ -622,69 +682,80 @@ struct Cand {
     int i, b;
 };
 
-// One group of RG rows (RPU = 1) or RG / 2 pair units (RPU = 2) of a warp's chunk: the
-// dots, then the phase's epilogue.  j0 / ng: first unit and unit count of the group
-// within the chunk; c_unit0: the chunk's first unit within the CTA's slice.
+// The dots of a prepared group, the warp reduction and the epilogue.  rs1: 1/rms of the
+// single batch row when NB = 1 (RMSNorm inputs).
 template <int NB, int RG, int RPU, bool WBF16>
-__device__ __forceinline__ Cand gemv_group(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
-                                        const uint8_t *buf, int j0, int ng, int c_unit0, int c_kt, int u0) {
+__device__ __forceinline__ Cand group_compute(const StepParams &P, const Mat &M, Shared &S,
+                                              const GroupW<NB, RG, WBF16> &G, const EpiCtx &c, const uint8_t *base,
+                                              int nr, int kt, float rs1) {
     constexpr int V = RG * NB;
     constexpr int SHIFT = 5 - Log2<V>::value;
     const Model &m = P.m;
     const int lane = threadIdx.x & 31;
-    const int batch = P.batch;
     const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
     Cand cd{-INFINITY, 0, 0};
     float acc[V];
-    rows_dot<NB, RG, WBF16>(buf + (size_t)j0 * RPU * rowbytes, rowbytes, ng * RPU, S.xs, M.KBp, batch, acc);
+    rows_dot<NB, RG, WBF16>(G, base, rowbytes, nr, S.xs, M.KBp, P.batch, acc);
     const float val = reduce_scatter<V>(acc);
-    const int idx = lane >> SHIFT;  // value held by this lane
-    const bool holder = (lane & ((1 << SHIFT) - 1)) == 0;
-    const int r = idx / NB, b = idx - r * NB;  // group row, batch row
+    float second = 0.f;
+    if constexpr (RPU == 2) second = __shfl_sync(0xffffffffu, val, ((((lane >> SHIFT) + NB) << SHIFT) & 31));
+    if (c.b < 0) return cd;
     const uint32_t tag = P.tag;
-    if constexpr (RPU == 2) {  // pair units: (gate, up) of W1/W3; (dim i, dim i + d/2) of QKV
-        const float second = __shfl_sync(0xffffffffu, val, ((idx + NB) << SHIFT) & 31);
-        const int u = r >> 1;
-        if (!holder || (r & 1) || u >= ng || b >= batch) return cd;
-        const int unit = u0 + c_unit0 + j0 + u;
-        const float rs = inv_rms(m, S.ssp, b);
-        const float x1 = val * rs, x2 = second * rs;
-        if (epi == EPI_W13) {
-            const float s = x1 / (1.0f + __expf(-x1));
-            ll_store(m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit, s * x2, tag);
-        } else {
-            qkv_pair_epilogue(P, layer, b, unit, x1, x2);
+    const float rs = c.kind == EK_RES ? 1.f : NB == 1 ? rs1 : inv_rms(m, S.ssp, c.b);
+    const float v = val * rs;
+    if constexpr (RPU == 2) {
+        const float x2 = second * rs;
+        if (c.kind == EK_W13) {
+            const float sg = v / (1.0f + __expf(-v));
+            ll_store(c.dst, sg * x2, tag);
+            return cd;
         }
+        float o0 = v, o1 = x2;
+        if (c.kind != EK_V) {
+            o0 = v * c.cs - x2 * c.sn;
+            o1 = v * c.sn + x2 * c.cs;
+        }
+        if (c.kind == EK_Q) {  // scores in base-2 units: q * log2(e) / sqrt(d)
+            const float qscale = rsqrtf((float)m.head_dim) * 1.4426950408889634f;
+            o0 *= qscale;
+            o1 *= qscale;
+        } else if (m.kv_bf16) {  // k, v: round to the cache type, append
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(o0), h1 = __float2bfloat16_rn(o1);
+            ((__nv_bfloat16 *)c.cache)[0] = h0;
+            ((__nv_bfloat16 *)c.cache)[c.half] = h1;
+            o0 = __bfloat162float(h0);
+            o1 = __bfloat162float(h1);
+        } else {
+            ((float *)c.cache)[0] = o0;
+            ((float *)c.cache)[c.half] = o1;
+        }
+        ll_store(c.dst, o0, tag);
+        ll_store(c.dst + c.half, o1, tag);
         return cd;
     } else {
-        if (!holder || r >= ng || b >= batch) return cd;
-        const int i = c_unit0 + j0 + r;  // unit within the CTA's slice
-        const int unit = u0 + i;
-        float v = val;
-        if (epi == EPI_LOGITS) {
-            v *= inv_rms(m, S.ssp, b);
-            if (P.logits) P.logits[(size_t)b * m.vocab + unit] = v;
+        if (c.kind == EK_LOGITS) {
+            if (P.logits) P.logits[(size_t)c.b * m.vocab + c.own] = v;
             if (v != v) {
                 atomicOr(m.status, kStNanLogits);
             } else {
                 cd.v = v;
-                cd.i = unit;
-                cd.b = b;
+                cd.i = c.own;
+                cd.b = c.b;
             }
             return cd;
         }
+        float t = v;
         if (M.nkt > 1) {  // accumulate this K tile; finish after the last one
-            float *a = S.accs + (size_t)i * kMaxBatch + b;
-            v = (c_kt == 0 ? 0.f : *a) + v;
-            *a = v;
-            if (c_kt != M.nkt - 1) return cd;
+            float *a = S.accs + (size_t)c.own * kMaxBatch + c.b;
+            t = (kt == 0 ? 0.f : *a) + t;
+            *a = t;
+            if (kt != M.nkt - 1) return cd;
         }
         // Wo / W2: residual add on the owned row, publish the new residual
-        float *own = S.xown + b * kMaxOwn + i;
-        const float xn = *own + v;
+        float *own = S.xown + c.b * kMaxOwn + c.own;
+        const float xn = *own + t;
         *own = xn;
-        uint64_t *dst = epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim) : m.ll_x + ll_layer(P, layer + 1, m.dim);
-        ll_store(dst + (size_t)b * m.dim + unit, xn, tag);
+        ll_store(c.dst, xn, tag);
         return cd;
     }
 }
@@ -701,67 +772,73 @@ __device__ __forceinline__ void keep_best(const Cand &cd, float (&best_v)[NB], i
         }
 }
 
-// The chunks of one matrix for this CTA, K tile by K tile: chunk i of the step belongs
-// to warp i % 8; with a multiple of 8 ring slots every use of a slot belongs to the same
-// warp, which takes them in order.  Each warp goes straight to its own chunks, and
-// waits for its first one's weights before the input is polled (the producer is far
-// enough ahead that they are normally resident).  Returns the updated chunk counter.
-// For the logits, each lane keeps the best (value, index) per batch row.
-template <int NB, bool WBF16, bool LOGITS>
-__device__ __forceinline__ uint32_t walk_chunks(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
-                                                uint32_t chunk_i, int tslot, float (&best_v)[NB], int (&best_i)[NB]) {
-    // Row groups: at batch 1 only the logits have chunks of several rows (a CTA's share
-    // of the layer matrices is a few rows, one per chunk), so the layer phases keep a
-    // single group shape there and the code stays small.
-    constexpr int R = (NB == 1 && !LOGITS) ? 1 : GemvShape<NB>::R;
+__device__ __forceinline__ bool is_norm_input(int epi) { return epi == EPI_QKV || epi == EPI_W13 || epi == EPI_LOGITS; }
+
+// The chunks of one of a layer's matrices for this CTA, K tile by K tile: chunk i of
+// the step belongs to warp i % 8; with a multiple of 8 ring slots every use of a slot
+// belongs to the same warp, which takes them in order.  At batch 1 a chunk (at most 8
+// rows) is one row group; at larger batches each unit (a row, or a RoPE / SwiGLU pair)
+// is one.  Each warp goes straight to its own chunks and, before the input is polled,
+// waits for its first chunk's weights, loads its first group's pieces into registers
+// and prepares that group's epilogue; after the poll only the arithmetic and the
+// stores remain.  Returns the updated chunk counter.
+template <int NB, bool WBF16>
+__device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
+                                               uint32_t chunk_i, int tslot) {
+    constexpr int RG = NB == 1 ? 8 : 2;  // rows of a group
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
-    unit_range(M.rows / M.rows_per_unit, P.grid, blockIdx.x, u0, u1);
+    phase_slice(P, epi, M.rows / M.rows_per_unit, blockIdx.x, u0, u1);
     trace_mark(P, tslot, 0);
     if (u0 == u1) return chunk_i;
     const int cu = M.rows_per_chunk / M.rows_per_unit;  // units per chunk
     const int cpk = (u1 - u0 + cu - 1) / cu;            // chunks per K tile
     const int nch = M.nkt * cpk;
     const uint32_t slots = (uint32_t)P.ring_slots;
-    // this warp's chunks of the phase: j, j + 8, ...; j < 8 <= slots, so the first one
-    // never waits for a chunk consumed after the poll
+    const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
+    const int pieces = M.KBp / (WBF16 ? 8 : 4);
+    const bool pairs = M.rows_per_unit == 2;
+    // the warp's chunks of the phase: j, j + 8, ...; the current group: units [g, g + ng)
+    // of chunk j
     int j = (warp - (int)(chunk_i & 7)) & 7;
-    if (j < nch) {
+    int g = 0, ng = 0;
+    GroupW<NB, RG, WBF16> wp;
+    EpiCtx ctx;
+    const uint8_t *buf = nullptr;
+    // Prepare the group at unit g of chunk j: weights of its first pieces into registers,
+    // epilogue.  j < 8 <= slots: the first chunk never waits for a chunk consumed after
+    // the poll.
+    auto prepare = [&]() {
         const uint32_t ci = chunk_i + (uint32_t)j;
-        wait_slot(P, &S.full[ci % slots], (ci / slots) & 1);
-    }
+        const int kt = j / cpk, unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0);
+        ng = NB == 1 ? nunits : 1;
+        if (g == 0) wait_slot(P, &S.full[ci % slots], (ci / slots) & 1);
+        buf = S.ring + (size_t)(ci % slots) * kChunkBytes + (size_t)g * M.rows_per_unit * rowbytes;
+        load_pieces<NB, RG, WBF16>(wp.w, buf, rowbytes, ng * M.rows_per_unit, lane, pieces);
+        ctx = pairs ? prepare_ctx<NB, RG, 2>(P, epi, layer, u0, unit0, g, ng)
+                    : prepare_ctx<NB, RG, 1>(P, epi, layer, u0, unit0, g, ng);
+    };
+    if (j < nch) prepare();
 #pragma unroll 1
     for (int kt = 0; kt < M.nkt; kt++) {
         stage_input(P, epi, layer, M, kt, S);
         if (kt == 0) trace_mark(P, tslot, 1);
+        const float rs1 = (NB == 1 && is_norm_input(epi)) ? inv_rms(P.m, S.ssp, 0) : 1.f;
 #pragma unroll 1
-        for (; j < nch && j < (kt + 1) * cpk; j += kComputeWarps) {
-            const uint32_t ci = chunk_i + (uint32_t)j;
-            const uint32_t slot = ci % slots;
-            wait_slot(P, &S.full[slot], (ci / slots) & 1);
+        while (j < nch && j < (kt + 1) * cpk) {
             const int unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0);
-            const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
-            if (M.rows_per_unit == 2) {
-#pragma unroll 1
-                for (int g = 0; g < nunits; g++)
-                    gemv_group<NB, 2, 2, WBF16>(P, epi, layer, M, S, buf, g, 1, unit0, kt, u0);
-            } else {
-                int g = 0;
-#pragma unroll 1
-                for (; g + R <= nunits; g += R) {
-                    const Cand cd = gemv_group<NB, R, 1, WBF16>(P, epi, layer, M, S, buf, g, R, unit0, kt, u0);
-                    if constexpr (LOGITS) keep_best<NB>(cd, best_v, best_i);
-                }
-                if constexpr (R > 1) {
-#pragma unroll 1
-                    for (; g < nunits; g++) {
-                        const Cand cd = gemv_group<NB, 1, 1, WBF16>(P, epi, layer, M, S, buf, g, 1, unit0, kt, u0);
-                        if constexpr (LOGITS) keep_best<NB>(cd, best_v, best_i);
-                    }
-                }
+            if (pairs)
+                group_compute<NB, RG, 2, WBF16>(P, M, S, wp, ctx, buf, ng * 2, kt, rs1);
+            else
+                group_compute<NB, RG, 1, WBF16>(P, M, S, wp, ctx, buf, ng, kt, rs1);
+            g += ng;
+            if (g >= nunits) {  // chunk done: release its slot, move to the warp's next one
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[(chunk_i + (uint32_t)j) % slots]);
+                g = 0;
+                j += kComputeWarps;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.empty[slot]);
+            if (j < nch) prepare();
         }
     }
     if (P.trace) compute_sync();  // the timeline's "done" covers every warp
@@ -769,12 +846,62 @@ __device__ __forceinline__ uint32_t walk_chunks(const StepParams &P, int epi, in
     return chunk_i + (uint32_t)nch;
 }
 
+// The logits: chunks of up to R rows per group (8 at batch 1), each lane keeping the
+// best (value, index) per batch row.
+template <int NB, bool WBF16>
+__device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &M, Shared &S, uint32_t chunk_i, int tslot,
+                                                float (&best_v)[NB], int (&best_i)[NB]) {
+    constexpr int R = NB == 1 ? 8 : GemvShape<NB>::R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int u0, u1;
+    phase_slice(P, 4, M.rows, blockIdx.x, u0, u1);
+    trace_mark(P, tslot, 0);
+    if (u0 == u1) return chunk_i;
+    const int cu = M.rows_per_chunk;
+    const int nch = (u1 - u0 + cu - 1) / cu;
+    const uint32_t slots = (uint32_t)P.ring_slots;
+    const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
+    const int pieces = M.KBp / (WBF16 ? 8 : 4);
+    int j = (warp - (int)(chunk_i & 7)) & 7;
+    if (j < nch) wait_slot(P, &S.full[(chunk_i + (uint32_t)j) % slots], ((chunk_i + (uint32_t)j) / slots) & 1);
+    stage_input(P, EPI_LOGITS, 0, M, 0, S);
+    trace_mark(P, tslot, 1);
+    const float rs1 = NB == 1 ? inv_rms(P.m, S.ssp, 0) : 1.f;
+#pragma unroll 1
+    for (; j < nch; j += kComputeWarps) {
+        const uint32_t ci = chunk_i + (uint32_t)j, slot = ci % slots;
+        wait_slot(P, &S.full[slot], (ci / slots) & 1);
+        const int unit0 = j * cu, nunits = min(cu, u1 - u0 - unit0);
+        const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
+#pragma unroll 1
+        for (int g = 0; g < nunits; g += R) {
+            const int ng = min(R, nunits - g);
+            if (R > 1 && ng == 1) {
+                GroupW<NB, 1, WBF16> w;
+                load_pieces<NB, 1, WBF16>(w.w, buf + (size_t)g * rowbytes, rowbytes, 1, lane, pieces);
+                const EpiCtx c = prepare_ctx<NB, 1, 1>(P, EPI_LOGITS, 0, u0, unit0, g, 1);
+                keep_best<NB>(group_compute<NB, 1, 1, WBF16>(P, M, S, w, c, buf + (size_t)g * rowbytes, 1, 0, rs1),
+                              best_v, best_i);
+            } else {
+                GroupW<NB, R, WBF16> w;
+                load_pieces<NB, R, WBF16>(w.w, buf + (size_t)g * rowbytes, rowbytes, ng, lane, pieces);
+                const EpiCtx c = prepare_ctx<NB, R, 1>(P, EPI_LOGITS, 0, u0, unit0, g, ng);
+                keep_best<NB>(group_compute<NB, R, 1, WBF16>(P, M, S, w, c, buf + (size_t)g * rowbytes, ng, 0, rs1),
+                              best_v, best_i);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+    }
+    if (P.trace) compute_sync();
+    trace_mark(P, tslot, 2);
+    return chunk_i + (uint32_t)nch;
+}
+
 template <int NB, bool WBF16>
 __device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                             uint32_t chunk_i, int tslot) {
-    float bv[NB];
-    int bi[NB];
-    return walk_chunks<NB, WBF16, false>(P, epi, layer, M, S, chunk_i, tslot, bv, bi);
+    return layer_walk<NB, WBF16>(P, epi, layer, M, S, chunk_i, tslot);
 }
 
 // The logits and the greedy argmax: per lane, per warp, per CTA best candidates (lowest
@@ -791,7 +918,7 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
         best_v[b] = -INFINITY;
         best_i[b] = 0x7fffffff;
     }
-    walk_chunks<NB, WBF16, true>(P, EPI_LOGITS, 0, m.emb, S, chunk_i, tslot, best_v, best_i);
+    logits_walk<NB, WBF16>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
     trace_mark(P, tslot + 1, 0);
     compute_sync();  // the logits phase is done with S.xs
 #pragma unroll
@@ -933,12 +1060,45 @@ __device__ __forceinline__ void attn_item(const StepParams &P, int layer, int b,
     attn_core(T, S.xs, &S.flags[0]);
 }
 
+// The cached keys and values an attention item of layer `layer` will read do not
+// depend on this step: the CTAs that run items ask L2 for them when the layer starts,
+// so that the item's copy into shared memory does not wait for HBM.
+__device__ __forceinline__ void prefetch_attention_kv(const StepParams &P, int layer) {
+    const Model &m = P.m;
+    const int total = P.item_start[P.batch];
+    int a0, an;
+    attention_ctas(P, a0, an);
+    const int me = (int)blockIdx.x - a0;
+    if (me < 0 || me >= an || me >= total || threadIdx.x >= 2) return;
+    const size_t rowbytes = (size_t)m.head_dim * (m.kv_bf16 ? 2 : 4);
+    for (int item = me; item < total; item += an) {
+        int b = 0;
+        while (item >= P.item_start[b + 1]) b++;
+        const int local = item - P.item_start[b], nc = P.nchunk[b];
+        const int g = local / nc, c = local - g * nc;
+        const int t0 = c * P.attn_chunk, tc = min(P.pos[b], t0 + P.attn_chunk);  // cached rows
+        if (g >= m.n_kv_heads || tc <= t0) continue;
+        const size_t off = ((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + t0) * rowbytes;
+        size_t bytes = (size_t)(tc - t0) * rowbytes;
+        const uint8_t *src = (threadIdx.x == 0 ? m.kc : m.vc) + off;
+        while (bytes) {  // one bulk prefetch moves less than 4 GB; stay well below
+            const uint32_t n = (uint32_t)min(bytes, (size_t)(1u << 20));
+            bulk_prefetch_l2(src, n);
+            src += n;
+            bytes -= n;
+        }
+    }
+}
+
 __device__ __forceinline__ void attention_phase(const StepParams &P, int layer, Shared &S) {
     const int tslot = layer * kTracePerLayer + 1;
     trace_mark(P, tslot, 0);
     const int total = P.item_start[P.batch];
     const int KV = P.m.n_kv_heads;
-    for (int item = blockIdx.x; item < total; item += P.grid) {
+    int a0, an;
+    attention_ctas(P, a0, an);
+    const int me = (int)blockIdx.x - a0;
+    for (int item = me; me >= 0 && me < an && item < total; item += an) {
         int b = 0;
         while (item >= P.item_start[b + 1]) b++;
         const int local = item - P.item_start[b];
@@ -978,6 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 #pragma unroll 1
         for (int ph = 0; ph < kTracePerLayer; ph++) {
             const int t = l * kTracePerLayer + ph;
+            if (ph == 0) prefetch_attention_kv(P, l);
             if (ph == 1) {
                 attention_phase(P, l, S);
                 continue;

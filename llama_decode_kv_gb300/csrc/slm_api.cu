@@ -40,6 +40,8 @@ struct slm_ctx {
     uint32_t launch_seq = 0;     // exchange tag of the last launch
     unsigned long long *d_trace = nullptr;  // phase timeline, when tracing is on
     bool prefill_tc = false;     // long prompts go through the tensor-core prefill
+    bool roles = false;          // CTA roles for steps of at most kRolesMaxBatch rows
+    int role0[5] = {0, 0, 0, 0, 0};
     PrefillPlan plan;
     bool trace_on = false;
     int *d_tokens = nullptr;     // staging for host-provided tokens [max(max_seq, max_batch)]
@@ -109,9 +111,10 @@ static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // every batch row fits in shared memory and a unit of rows fits in one ring slot;
 // otherwise split K (only for residual-add epilogues, where the tiles' partial sums are
 // accumulated).  A chunk (one warp's piece of work) holds whole units: enough that a
-// CTA's share splits into about one chunk per warp or more, at most one slot.
+// CTA's share (of `ctas` CTAs) splits into about one chunk per warp or more, at most one
+// slot and at most 8 rows (one row group of the batch-1 kernel).
 static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int max_batch,
-                     bool allow_split, int grid) {
+                     bool allow_split, int ctas) {
     for (int nkt = 1; nkt <= 64; nkt++) {
         int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), kPadElems);
         int real_nkt = (K + KB - 1) / KB;
@@ -127,8 +130,8 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
             M.rows_per_unit = rows_per_unit;
             M.units = real_nkt * (rows / rows_per_unit);
             const int units = rows / rows_per_unit;
-            const int per_cta = (units + grid - 1) / grid;
-            const int fit = (int)(kChunkBytes / unit_bytes);
+            const int per_cta = (units + ctas - 1) / ctas;
+            const int fit = std::min((int)(kChunkBytes / unit_bytes), 8 / rows_per_unit);
             const int upc = std::max(1, std::min(fit, (per_cta + kComputeWarps - 1) / kComputeWarps));
             M.rows_per_chunk = upc * rows_per_unit;
             M.layer_stride = (long long)real_nkt * rows * KB * esz;
@@ -282,9 +285,35 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     // least 16) takes the rest.  The grid is one CTA per SM.
     c->grid = sms;
     const int grid = c->grid;
-    if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) || !plan_mat(m.qkv, qkv_rows, dim, 2, esz, B, false, grid) ||
-        !plan_mat(m.wo, dim, qd, 1, esz, B, true, grid) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, grid) ||
-        !plan_mat(m.w2, dim, hid, 1, esz, B, true, grid))
+    // Roles (see StepParams): engines of small models at small batches.  CTAs
+    // [role0[r], role0[r + 1]) take role r; the sizes follow each role's weight bytes.
+    {
+        bool ok = true;
+        if (const char *e = getenv("SLM_NO_ROLES")) ok = atoi(e) == 0;
+        const double b_qkv = (double)qkv_rows * dim, b_w13 = 2.0 * hid * dim, b_res = (double)dim * qd + (double)dim * hid;
+        const double total = b_qkv + b_w13 + b_res;
+        const int R = grid - kRoleAttnCtas;
+        ok = ok && B <= kRolesMaxBatch && total * esz <= kRolesMaxLayerBytes && R >= 3;
+        if (ok) {
+            const int n_qkv = std::max(1, (int)std::lround(R * b_qkv / total));
+            const int n_w13 = std::max(1, (int)std::lround(R * b_w13 / total));
+            const int n_res = R - n_qkv - n_w13;
+            ok = n_res >= 1 && (dim + n_res - 1) / n_res <= kMaxOwn;
+            c->role0[0] = 0;
+            c->role0[1] = n_qkv;
+            c->role0[2] = n_qkv + kRoleAttnCtas;
+            c->role0[3] = n_qkv + kRoleAttnCtas + n_res;
+            c->role0[4] = grid;
+        }
+        c->roles = ok;
+    }
+    const int ctas_qkv = c->roles ? c->role0[1] - c->role0[0] : grid;
+    const int ctas_res = c->roles ? c->role0[3] - c->role0[2] : grid;
+    const int ctas_w13 = c->roles ? c->role0[4] - c->role0[3] : grid;
+    if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) ||
+        !plan_mat(m.qkv, qkv_rows, dim, 2, esz, B, false, ctas_qkv) ||
+        !plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, ctas_w13) ||
+        !plan_mat(m.w2, dim, hid, 1, esz, B, true, ctas_res))
         return fail(c, SLM_EUNSUPPORTED,
                     "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
     m.emb.layer_stride = 0;
@@ -478,11 +507,20 @@ extern "C" int slm_create(const slm_config *config, const void *weights, size_t 
     return SLM_OK;
 }
 
-// Split-K geometry of the attention phase for this step: about two items per CTA, at
-// least kMinAttnChunk positions per chunk, at most kMaxChunksPerSeq chunks per row.
-// When every row's chunk states fit the Wo consumers' shared-memory tile (and at most
-// kMaxChunksA chunks per row), the consumers merge them; otherwise the last CTA to
-// finish a (row, kv head) merges and publishes the output.
+// Work split of this step: the engine's roles when it has them and the batch is small
+// (the step is then bound by the hand-offs between phases, and a CTA that loops over
+// one small piece of code keeps it in the SM's instruction cache).
+static void plan_roles(const slm_ctx *c, StepParams &P) {
+    P.roles = c->roles && P.batch <= kRolesMaxBatch;
+    for (int r = 0; r < 5; r++) P.role0[r] = c->role0[r];
+}
+
+// Split-K geometry of the attention phase for this step: about two items per CTA (at
+// most kRoleAttnCtas items when the CTAs have roles), at least kMinAttnChunk positions
+// per chunk, at most kMaxChunksPerSeq chunks per row.  When every row's chunk states
+// fit the Wo consumers' shared-memory tile (and at most kMaxChunksA chunks per row),
+// the consumers merge them; otherwise the last CTA to finish a (row, kv head) merges
+// and publishes the output.
 static void plan_attention(const slm_ctx *c, StepParams &P) {
     const Model &m = c->m;
     const int KV = m.n_kv_heads, H = m.n_heads, hd = m.head_dim;
@@ -492,7 +530,14 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
         work += (long long)(P.pos[b] + 1) * KV;
         max_ctx = std::max(max_ctx, P.pos[b] + 1);
     }
-    long long ch = (work + 2LL * c->grid - 1) / (2LL * c->grid);
+    plan_roles(c, P);
+    long long ch;
+    if (P.roles) {  // chunks so that the items fit kRoleAttnCtas CTAs
+        const long long per_row = std::max(1, kRoleAttnCtas / (P.batch * KV));
+        ch = (max_ctx + per_row - 1) / per_row;
+    } else {
+        ch = (work + 2LL * c->grid - 1) / (2LL * c->grid);
+    }
     ch = std::max<long long>(ch, kMinAttnChunk);
     ch = std::max<long long>(ch, (max_ctx + kMaxChunksPerSeq - 1) / kMaxChunksPerSeq);
     ch = (ch + 31) / 32 * 32;
@@ -517,6 +562,14 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
     for (int b = 0; b < P.batch; b++) {
         P.nchunk[b] = (int)((P.pos[b] + 1 + ch - 1) / ch);
         P.item_start[b + 1] = P.item_start[b] + KV * P.nchunk[b];
+    }
+    const int items = P.item_start[P.batch];
+    if (!P.roles) {
+        // The CTAs that run attention items (CTA i takes item i) finish that phase last;
+        // when they are few, the Wo / W2 rows go to the others so that nobody waits for
+        // them twice.
+        const int rest = c->grid - items;
+        P.res_cta0 = (items <= c->grid / 4 && rest > 0 && (m.dim + rest - 1) / rest <= kMaxOwn) ? items : 0;
     }
 }
 

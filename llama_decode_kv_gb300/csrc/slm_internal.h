@@ -21,6 +21,9 @@ constexpr int kMaxGroupPass = 4;                      // query heads per attenti
 constexpr int kMaxChunksPerSeq = 64;                  // split-K chunks per (row, kv head)
 constexpr int kMaxChunksA = 16;                       // chunks when consumers merge them
 constexpr int kMinAttnChunk = 32;                     // positions
+constexpr int kRoleAttnCtas = 16;                     // attention CTAs when CTAs have roles
+constexpr int kRolesMaxBatch = 4;                     // roles only up to this batch ...
+constexpr double kRolesMaxLayerBytes = 16e6;          //   ... and these weight bytes per layer
 constexpr int kTensorPrefillMin = 16;                 // prompts this long use the GEMM prefill
 constexpr size_t kXsBudget = 88 * 1024;               // activation tile, at most (16-slot ring)
 constexpr size_t kSmemLimit = 227 * 1024;             // dynamic shared memory per CTA
@@ -89,6 +92,15 @@ struct StepParams {
     int nchunk[kMaxBatch];
     int attn_chunk;                 // positions per split-K chunk
     int attn_consumer_merge;        // 1: Wo consumers merge chunk states; 0: last CTA merges
+    // How the CTAs share the work.  roles = 0: every CTA takes a slice of every matrix,
+    // attention item i runs on CTA i, and Wo / W2 rows (the residual) go to CTAs
+    // [res_cta0, grid) (the attention CTAs finish that phase last).  roles = 1: each CTA
+    // keeps one role for the whole step, so that it loops over one small piece of code:
+    // CTAs [role0[r], role0[r + 1]) take role r = 0 QKV rows, 1 attention items, 2 the
+    // residual rows (Wo and W2), 3 W1/W3 pairs; all CTAs share the logits.
+    int res_cta0;
+    int roles;
+    int role0[5];
     const int *tokens;              // device [batch]
     float *logits;                  // device [batch][vocab] or null
     int *next_ids;                  // device [batch] or null
@@ -115,6 +127,34 @@ __host__ __device__ inline void unit_range(int units_total, int grid, int cta, i
     long long t = units_total;
     u0 = (int)(t * cta / grid);
     u1 = (int)(t * (cta + 1) / grid);
+}
+
+// The slice of phase `phase` (0 QKV, 1 Wo, 2 W1/W3, 3 W2, 4 logits) for CTA cta.
+__host__ __device__ inline void phase_slice(const StepParams &P, int phase, int units_total, int cta, int &u0,
+                                            int &u1) {
+    if (phase == 4) {
+        unit_range(units_total, P.grid, cta, u0, u1);
+        return;
+    }
+    int lo = 0, hi = P.grid;
+    if (P.roles) {
+        const int r = phase == 0 ? 0 : (phase == 1 || phase == 3) ? 2 : 3;
+        lo = P.role0[r];
+        hi = P.role0[r + 1];
+    } else if (phase == 1 || phase == 3) {
+        lo = P.res_cta0;
+    }
+    if (cta < lo || cta >= hi) {
+        u0 = u1 = 0;
+        return;
+    }
+    unit_range(units_total, hi - lo, cta - lo, u0, u1);
+}
+
+// The CTAs that run attention items: item i on CTA first + i (mod count).
+__host__ __device__ inline void attention_ctas(const StepParams &P, int &first, int &count) {
+    first = P.roles ? P.role0[1] : 0;
+    count = P.roles ? P.role0[2] - P.role0[1] : P.grid;
 }
 
 }  // namespace slm
