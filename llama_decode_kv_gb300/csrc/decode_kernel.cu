@@ -958,20 +958,31 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
     if (blockIdx.x == 0) {
         // CTA 0: poll [batch][grid][2] words into shared memory, reduce per row
         poll_words(P, m.ll_amax, P.grid * 2, batch, P.grid * 2, S.xs, P.grid * 2, 0, nullptr, nullptr);
-        if (tid < batch) {
+        for (int b = warp; b < batch; b += kComputeWarps) {  // a warp per batch row
             float bv = -INFINITY;
             int bi = 0x7fffffff;
-            const float *r = S.xs + (size_t)tid * P.grid * 2;
-            for (int c = 0; c < P.grid; c++) {
-                float v = r[2 * c];
-                int i = __float_as_int(r[2 * c + 1]);
+            const float *r = S.xs + (size_t)b * P.grid * 2;
+            for (int c = lane; c < P.grid; c += 32) {
+                const float v = r[2 * c];
+                const int i = __float_as_int(r[2 * c + 1]);
                 if (v > bv || (v == bv && i < bi)) {
                     bv = v;
                     bi = i;
                 }
             }
-            if (bi == 0x7fffffff) bi = 0;  // all NaN: the status word already records it
-            if (P.next_ids) P.next_ids[tid] = bi;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (v2 > bv || (v2 == bv && i2 < bi)) {
+                    bv = v2;
+                    bi = i2;
+                }
+            }
+            if (lane == 0) {
+                if (bi == 0x7fffffff) bi = 0;  // all NaN: the status word already records it
+                if (P.next_ids) P.next_ids[b] = bi;
+            }
         }
     }
     trace_mark(P, tslot + 1, 2);
