@@ -126,44 +126,101 @@ constexpr int kPollBatch = 8;  // loads each thread keeps in flight
 // With `gain` (a single row): element j is stored as x_j * gain_j and each warp stores
 // its sum of x_j^2 in ssp[warp * kMaxBatch].  All compute threads call it; it ends with
 // their barrier.
+template <int WIDE = 1>
 __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *src, int src_ld, int rows, int len,
                                         float *dst, int dst_ld, int perm_ld, const float *gain, float *ssp) {
     const int tid = threadIdx.x;
-    const int n = rows * len;
     const uint32_t tag = P.tag;
+    // WIDE = 2 (long vectors of batched rows): words are fetched two at a time (one
+    // 16-byte load; each 8-byte word is still single-copy atomic and carries its own
+    // tag) when rows and the source are aligned, which halves the load rounds.
+    const int wpl = (((uintptr_t)src & 15) == 0 && (src_ld & 1) == 0 && (len & 1) == 0) ? 2 : 1;
     float ss = 0.f;
+    if constexpr (WIDE == 1) {
+        const int n = rows * len;
+        for (int base = 0; base < n; base += kComputeThreads * kPollBatch) {
+            int so[kPollBatch], dof[kPollBatch];
+            float g[kPollBatch];
+            bool need[kPollBatch];
+#pragma unroll
+            for (int k = 0; k < kPollBatch; k++) {
+                const int i = base + k * kComputeThreads + tid;
+                need[k] = i < n;
+                const int r = need[k] ? i / len : 0, j = need[k] ? i - r * len : 0;
+                so[k] = r * src_ld + j;
+                dof[k] = r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j);
+                g[k] = (gain && need[k]) ? __ldg(gain + j) : 1.f;
+            }
+            unsigned long long t0 = 0;
+            for (int it = 0;; it++) {
+                uint64_t w[kPollBatch];
+#pragma unroll
+                for (int k = 0; k < kPollBatch; k++) w[k] = need[k] ? ll_load(src + so[k]) : 0;
+                bool pending = false;
+#pragma unroll
+                for (int k = 0; k < kPollBatch; k++) {
+                    if (!need[k]) continue;
+                    if ((uint32_t)(w[k] >> 32) == tag) {
+                        const float x = __uint_as_float((uint32_t)w[k]);
+                        ss = fmaf(x, x, ss);
+                        dst[dof[k]] = x * g[k];
+                        need[k] = false;
+                    } else {
+                        pending = true;
+                    }
+                }
+                if (!pending) break;
+                if (it == 0) t0 = global_ns();
+                if ((it & 15) == 15) {  // the abort flag and the clock, every 16 rounds
+                    if (ld_volatile_int(P.m.abort_flag)) break;
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(P.m.status, kStExchangeTimeout);
+                        atomicExch(P.m.abort_flag, 1);
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+    const int n = rows * len / wpl;  // loads
     for (int base = 0; base < n; base += kComputeThreads * kPollBatch) {
-        int so[kPollBatch], dof[kPollBatch];
-        float g[kPollBatch];
-        bool need[kPollBatch];
+        int so[kPollBatch];
+        uint32_t pend = 0;  // bit 2k + h: word h of load k still missing
 #pragma unroll
         for (int k = 0; k < kPollBatch; k++) {
-            const int i = base + k * kComputeThreads + tid;
-            need[k] = i < n;
-            const int r = need[k] ? i / len : 0, j = need[k] ? i - r * len : 0;
-            so[k] = r * src_ld + j;
-            dof[k] = r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j);
-            g[k] = (gain && need[k]) ? __ldg(gain + j) : 1.f;
+            const int l = base + k * kComputeThreads + tid;
+            const int i = l < n ? l * wpl : 0;  // first word of the load
+            const int r = i / len;
+            so[k] = r * src_ld + (i - r * len);
+            if (l < n) pend |= (wpl == 2 ? 3u : 1u) << (2 * k);
         }
         unsigned long long t0 = 0;
         for (int it = 0;; it++) {
-            uint64_t w[kPollBatch];
-#pragma unroll
-            for (int k = 0; k < kPollBatch; k++) w[k] = need[k] ? ll_load(src + so[k]) : 0;
-            bool pending = false;
+            uint64_t w[kPollBatch][2];
 #pragma unroll
             for (int k = 0; k < kPollBatch; k++) {
-                if (!need[k]) continue;
-                if ((uint32_t)(w[k] >> 32) == tag) {
-                    const float x = __uint_as_float((uint32_t)w[k]);
-                    ss = fmaf(x, x, ss);
-                    dst[dof[k]] = x * g[k];
-                    need[k] = false;
-                } else {
-                    pending = true;
+                w[k][0] = w[k][1] = 0;
+                if (pend & (3u << (2 * k))) {
+                    if (wpl == 2)
+                        ll_load2(src + so[k], w[k][0], w[k][1]);
+                    else
+                        w[k][0] = ll_load(src + so[k]);
                 }
             }
-            if (!pending) break;
+#pragma unroll
+            for (int k = 0; k < kPollBatch; k++)
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const uint32_t bit = 1u << (2 * k + h);
+                    if (!(pend & bit) || (uint32_t)(w[k][h] >> 32) != tag) continue;
+                    pend &= ~bit;
+                    const int i = (base + k * kComputeThreads + tid) * wpl + h;  // word index
+                    const int r = i / len, j = i - r * len;
+                    const float x = __uint_as_float((uint32_t)w[k][h]);
+                    ss = fmaf(x, x, ss);
+                    dst[r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j)] = gain ? x * __ldg(gain + j) : x;
+                }
+            if (!pend) break;
             if (it == 0) t0 = global_ns();
             if ((it & 15) == 15) {  // the abort flag and the clock, every 16 rounds
                 if (ld_volatile_int(P.m.abort_flag)) break;
@@ -174,6 +231,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                 }
             }
         }
+    }
     }
     if (ssp) {
         ss = warp_sum(ss);
@@ -401,6 +459,7 @@ __device__ __forceinline__ void merge_chunk_states(const StepParams &P, int laye
 // Stage the input of phase `epi` (K tile kt) into S.xs as fp32 [batch][KBp] (element
 // order given by xpos).  An RMSNorm input is left as x * gain, with the per-warp sums
 // of x^2 in S.ssp.
+template <int NB>
 __device__ __forceinline__ void stage_input(const StepParams &P, int epi, int layer, const Mat &M, int kt, Shared &S) {
     const Model &m = P.m;
     const int tid = threadIdx.x;
@@ -428,9 +487,9 @@ __device__ __forceinline__ void stage_input(const StepParams &P, int epi, int la
             const uint64_t *src = epi == EPI_W13 ? m.ll_xa + ll_layer(P, layer, m.dim)
                                                  : m.ll_x + ll_layer(P, epi == EPI_QKV ? layer : m.n_layers, m.dim);
             if (P.batch == 1) {
-                poll_words(P, src, m.dim, 1, m.dim, S.xs, M.KBp, pl, g, S.ssp);
+                poll_words<(NB > 1 ? 2 : 1)>(P, src, m.dim, 1, m.dim, S.xs, M.KBp, pl, g, S.ssp);
             } else {
-                poll_words(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, pl, nullptr, nullptr);
+                poll_words<(NB > 1 ? 2 : 1)>(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, pl, nullptr, nullptr);
                 norm_pass(P, S.xs, M.KBp, perm, g, S.ssp);
             }
         }
@@ -440,12 +499,12 @@ __device__ __forceinline__ void stage_input(const StepParams &P, int epi, int la
         } else {
             const int qd = m.n_heads * m.head_dim;
             zero_pad(P, S.xs, M.KBp, qd, perm);
-            poll_words(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, pl, nullptr, nullptr);
+            poll_words<(NB > 1 ? 2 : 1)>(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, pl, nullptr, nullptr);
         }
     } else {  // W2: tile kt of the SwiGLU output
         const int k0 = kt * M.KB, kn = min(M.K - k0, M.KB);
         zero_pad(P, S.xs, M.KBp, kn, perm);
-        poll_words(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, pl, nullptr,
+        poll_words<(NB > 1 ? 2 : 1)>(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, pl, nullptr,
                    nullptr);
     }
 }
@@ -777,8 +836,8 @@ __device__ __forceinline__ bool is_norm_input(int epi) { return epi == EPI_QKV |
 // The chunks of one of a layer's matrices for this CTA, K tile by K tile: chunk i of
 // the step belongs to warp i % 8; with a multiple of 8 ring slots every use of a slot
 // belongs to the same warp, which takes them in order.  At batch 1 a chunk (at most 8
-// rows) is one row group; at larger batches each unit (a row, or a RoPE / SwiGLU pair)
-// is one.  Each warp goes straight to its own chunks and, before the input is polled,
+// rows) is one row group; at larger batches a group is a RoPE / SwiGLU pair or two rows
+// (each activation load then serves two rows).  Each warp goes straight to its own chunks and, before the input is polled,
 // waits for its first chunk's weights, loads its first group's pieces into registers
 // and prepares that group's epilogue; after the poll only the arithmetic and the
 // stores remain.  Returns the updated chunk counter.
@@ -811,7 +870,7 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
     auto prepare = [&]() {
         const uint32_t ci = chunk_i + (uint32_t)j;
         const int kt = j / cpk, unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0);
-        ng = NB == 1 ? nunits : 1;
+        ng = NB == 1 ? nunits : pairs ? 1 : min(2, nunits - g);  // batches: 2 rows share each activation load
         if (g == 0) wait_slot(P, &S.full[ci % slots], (ci / slots) & 1);
         buf = S.ring + (size_t)(ci % slots) * kChunkBytes + (size_t)g * M.rows_per_unit * rowbytes;
         load_pieces<NB, RG, WBF16>(wp.w, buf, rowbytes, ng * M.rows_per_unit, lane, pieces);
@@ -821,7 +880,7 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
     if (j < nch) prepare();
 #pragma unroll 1
     for (int kt = 0; kt < M.nkt; kt++) {
-        stage_input(P, epi, layer, M, kt, S);
+        stage_input<NB>(P, epi, layer, M, kt, S);
         if (kt == 0) trace_mark(P, tslot, 1);
         const float rs1 = (NB == 1 && is_norm_input(epi)) ? inv_rms(P.m, S.ssp, 0) : 1.f;
 #pragma unroll 1
@@ -864,7 +923,7 @@ __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &
     const int pieces = M.KBp / (WBF16 ? 8 : 4);
     int j = (warp - (int)(chunk_i & 7)) & 7;
     if (j < nch) wait_slot(P, &S.full[(chunk_i + (uint32_t)j) % slots], ((chunk_i + (uint32_t)j) / slots) & 1);
-    stage_input(P, EPI_LOGITS, 0, M, 0, S);
+    stage_input<NB>(P, EPI_LOGITS, 0, M, 0, S);
     trace_mark(P, tslot, 1);
     const float rs1 = NB == 1 ? inv_rms(P.m, S.ssp, 0) : 1.f;
 #pragma unroll 1

@@ -115,4 +115,10 @@ __device__ __forceinline__ uint64_t ll_load(const uint64_t *p) {
     return w;
 }
 
+// Two consecutive tagged words with one 16-byte load (p 16-byte aligned); each word is
+// single-copy atomic on its own.
+__device__ __forceinline__ void ll_load2(const uint64_t *p, uint64_t &a, uint64_t &b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
 }  // namespace slm

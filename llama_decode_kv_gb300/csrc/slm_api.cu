@@ -132,7 +132,10 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
             const int units = rows / rows_per_unit;
             const int per_cta = (units + ctas - 1) / ctas;
             const int fit = std::min((int)(kChunkBytes / unit_bytes), 8 / rows_per_unit);
-            const int upc = std::max(1, std::min(fit, (per_cta + kComputeWarps - 1) / kComputeWarps));
+            // batches: at least two single rows per chunk, so that a row group reuses
+            // each activation load for two rows
+            const int want = (per_cta + kComputeWarps - 1) / kComputeWarps;
+            const int upc = std::max(1, std::min(fit, max_batch > 1 && rows_per_unit == 1 ? std::max(2, want) : want));
             M.rows_per_chunk = upc * rows_per_unit;
             M.layer_stride = (long long)real_nkt * rows * KB * esz;
             return true;
