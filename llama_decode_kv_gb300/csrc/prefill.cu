@@ -126,73 +126,190 @@ __global__ void rope_append_kernel(const Model m, float *qkv, int layer, int seq
     }
 }
 
-// Causal attention of query rows p0 .. p0 + T - 1 (one CTA: 64 rows of one query head).
-// Four threads per row each hold HD/4 dimensions of q and of the output; keys and values
-// are staged 64 positions at a time in shared memory; online softmax in the log2 domain.
-template <int HD, bool KVBF16>
-__global__ void __launch_bounds__(256) attn_prefill_kernel(const Model m, const float *qkv, uint16_t *out, size_t lo_off,
-                                                           int layer, int seq, int p0, int T) {
-    constexpr int DPT = HD / 4, QB = 64, KB = 4096 / HD;  // query rows per CTA, keys per stage
-    __shared__ float ks[KB][HD + 1];
-    __shared__ float vs[KB][HD];
+// ---- tensor-core causal attention (flash-attention style, mma.sync bf16 -> fp32)
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half)
+    return *(const uint32_t *)&v;
+}
+
+// Causal attention of query rows p0 .. p0 + T - 1 of one query head on the tensor cores:
+// a CTA takes 64 rows (4 warps x 16), walks the cached keys / values 64 positions at a
+// time (bf16, copied to padded shared memory with cp.async), S = Q K^T and O += P V by
+// mma.sync m16n8k16 with fp32 accumulation, online softmax in the log2 domain (q is
+// pre-multiplied by log2(e) / sqrt(HD)), causal mask on the blocks that reach the rows'
+// own positions.  Q and P enter the MMAs as bf16.
+template <int HD>
+__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, const float *qkv, uint16_t *out,
+                                                              size_t lo_off, int layer, int seq, int p0, int T) {
+    constexpr int QB = 64, KB = 64, LD = HD + 8;  // rows per CTA, keys per block, padded row (elements)
+    extern __shared__ __align__(16) uint16_t sm[];
+    uint16_t *qs = sm;                  // [QB][LD]
+    uint16_t *ks = qs + QB * LD;        // [KB][LD]
+    uint16_t *vs = ks + KB * LD;        // [KB][LD]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;
     const int h = blockIdx.y, KV = m.n_kv_heads, G = m.n_heads / KV, g = h / G;
-    const int r = threadIdx.x >> 2, sub = threadIdx.x & 3;
-    const int t = blockIdx.x * QB + r;           // row within the block
-    const int pos = p0 + t;                      // this row's position
-    const bool live = t < T;
-    const int last = p0 + min(T, (int)(blockIdx.x + 1) * QB) - 1;  // last position of the CTA
+    const int q0 = blockIdx.x * QB;                       // first row of the CTA
+    const int last = p0 + min(T, q0 + QB) - 1;            // last position any row reads
     const float qscale = rsqrtf((float)HD) * 1.4426950408889634f;
-    float q[DPT], o[DPT];
-    const float *qr = qkv + (size_t)(live ? t : 0) * m.qkv.rows + ((size_t)g * (G + 2) + (h - g * G)) * HD + sub * DPT;
-#pragma unroll
-    for (int d = 0; d < DPT; d++) {
-        q[d] = live ? qr[d] * qscale : 0.f;
-        o[d] = 0.f;
+    // Q tile: fp32 -> scaled bf16
+    for (int e = tid; e < QB * HD; e += blockDim.x) {
+        const int r = e / HD, d = e - r * HD, t = q0 + r;
+        float v = 0.f;
+        if (t < T) v = qkv[(size_t)t * m.qkv.rows + ((size_t)g * (G + 2) + (h - g * G)) * HD + d] * qscale;
+        qs[r * LD + d] = f32_to_bf16_bits(v);
     }
-    float mx = -INFINITY, l = 0.f;
-    const size_t rowbytes = (size_t)HD * (KVBF16 ? 2 : 4);
+    __syncthreads();
+    uint32_t qa[HD / 16][4];  // A fragments of this warp's 16 rows
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; kk++) {
+        const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c = kk * 16 + (lane >> 4) * 8;
+        ldsm_x4(qa[kk], qs + r * LD + c);
+    }
+    float o[HD / 8][4];
+#pragma unroll
+    for (int n = 0; n < HD / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};  // rows g4, g4 + 8
+    const int pos0 = p0 + q0 + warp * 16 + g4, pos1 = pos0 + 8;    // this lane's two rows
+    const size_t rowbytes = (size_t)HD * 2;
     const uint8_t *kbase = m.kc + ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq) * rowbytes;
     const uint8_t *vbase = m.vc + ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq) * rowbytes;
     for (int k0 = 0; k0 <= last; k0 += KB) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < KB * HD; e += blockDim.x) {
-            const int j = e / HD, d = e - j * HD, kp = k0 + j;
-            float kv = 0.f, vv = 0.f;
+        __syncthreads();  // previous block's readers are done
+        for (int e = tid; e < KB * (HD / 8); e += blockDim.x) {  // 16-byte pieces
+            const int j = e / (HD / 8), c = (e - j * (HD / 8)) * 8, kp = k0 + j;
+            uint16_t *kd = ks + j * LD + c, *vd = vs + j * LD + c;
             if (kp <= last) {
-                if (KVBF16) {
-                    kv = bf16_bits_to_f32(((const uint16_t *)(kbase + (size_t)kp * rowbytes))[d]);
-                    vv = bf16_bits_to_f32(((const uint16_t *)(vbase + (size_t)kp * rowbytes))[d]);
-                } else {
-                    kv = ((const float *)(kbase + (size_t)kp * rowbytes))[d];
-                    vv = ((const float *)(vbase + (size_t)kp * rowbytes))[d];
-                }
+                cp_async16(kd, kbase + (size_t)kp * rowbytes + c * 2);
+                cp_async16(vd, vbase + (size_t)kp * rowbytes + c * 2);
+            } else {
+                *(uint4 *)kd = make_uint4(0, 0, 0, 0);
+                *(uint4 *)vd = make_uint4(0, 0, 0, 0);
             }
-            ks[j][d] = kv;
-            vs[j][d] = vv;
         }
+        cp_async_wait_all();
         __syncthreads();
-        const int jmax = min(KB, last - k0 + 1);
-        for (int j = 0; j < jmax; j++) {
-            float s = 0.f;
+        // S = Q K^T for 64 keys: 8 tiles of 8 keys
+        float sc[KB / 8][4];
 #pragma unroll
-            for (int d = 0; d < DPT; d++) s = fmaf(q[d], ks[j][sub * DPT + d], s);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (k0 + j > pos) continue;  // causal mask (uniform within a row's 4 threads)
-            const float mn = fmaxf(mx, s);
-            const float corr = exp2f(mx - mn), p = exp2f(s - mn);
-            l = l * corr + p;
+        for (int n = 0; n < KB / 8; n++) {
+            sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-            for (int d = 0; d < DPT; d++) o[d] = fmaf(p, vs[j][sub * DPT + d], o[d] * corr);
-            mx = mn;
+            for (int kk = 0; kk < HD / 16; kk += 2) {  // two k-steps per x4 load
+                uint32_t b[4];
+                const int r = n * 8 + (lane & 7), c = kk * 16 + (lane >> 3) * 8;
+                ldsm_x4(b, ks + r * LD + c);
+                mma_bf16_16816(sc[n], qa[kk], b[0], b[1]);
+                mma_bf16_16816(sc[n], qa[kk + 1], b[2], b[3]);
+            }
+        }
+        // causal mask, row maxima
+        const bool diag = k0 + KB - 1 > pos0;
+        float mx0 = mrow[0], mx1 = mrow[1];
+#pragma unroll
+        for (int n = 0; n < KB / 8; n++) {
+            const int kp = k0 + n * 8 + 2 * t4;
+            if (diag) {
+                if (kp > pos0) sc[n][0] = -INFINITY;
+                if (kp + 1 > pos0) sc[n][1] = -INFINITY;
+                if (kp > pos1) sc[n][2] = -INFINITY;
+                if (kp + 1 > pos1) sc[n][3] = -INFINITY;
+            }
+            mx0 = fmaxf(mx0, fmaxf(sc[n][0], sc[n][1]));
+            mx1 = fmaxf(mx1, fmaxf(sc[n][2], sc[n][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float c0 = exp2f(mrow[0] - mx0), c1 = exp2f(mrow[1] - mx1);  // exp2(-inf) = 0
+        mrow[0] = mx0;
+        mrow[1] = mx1;
+        lrow[0] *= c0;
+        lrow[1] *= c1;
+#pragma unroll
+        for (int n = 0; n < HD / 8; n++) {
+            o[n][0] *= c0;
+            o[n][1] *= c0;
+            o[n][2] *= c1;
+            o[n][3] *= c1;
+        }
+        // P = 2^(S - m) as bf16 A fragments; O += P V
+#pragma unroll
+        for (int kk = 0; kk < KB / 16; kk++) {
+            float p[8];
+            p[0] = exp2f(sc[2 * kk][0] - mx0);
+            p[1] = exp2f(sc[2 * kk][1] - mx0);
+            p[2] = exp2f(sc[2 * kk][2] - mx1);
+            p[3] = exp2f(sc[2 * kk][3] - mx1);
+            p[4] = exp2f(sc[2 * kk + 1][0] - mx0);
+            p[5] = exp2f(sc[2 * kk + 1][1] - mx0);
+            p[6] = exp2f(sc[2 * kk + 1][2] - mx1);
+            p[7] = exp2f(sc[2 * kk + 1][3] - mx1);
+            lrow[0] += p[0] + p[1] + p[4] + p[5];
+            lrow[1] += p[2] + p[3] + p[6] + p[7];
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(p[0], p[1]);
+            pa[1] = pack_bf16x2(p[2], p[3]);
+            pa[2] = pack_bf16x2(p[4], p[5]);
+            pa[3] = pack_bf16x2(p[6], p[7]);
+#pragma unroll
+            for (int n = 0; n < HD / 8; n += 2) {  // two dim tiles per x4 load
+                uint32_t b[4];
+                const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c = n * 8 + (lane >> 4) * 8;
+                ldsm_x4_t(b, vs + r * LD + c);
+                mma_bf16_16816(o[n], pa, b[0], b[1]);
+                mma_bf16_16816(o[n + 1], pa, b[2], b[3]);
+            }
         }
     }
-    if (!live) return;
-    const size_t orow = (size_t)t * m.n_heads * HD + (size_t)h * HD + sub * DPT;
-    const float inv = 1.0f / l;
+    // row sums over the quad, normalise, store (bf16 hi + lo planes)
+    float l0 = lrow[0], l1 = lrow[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int t0 = q0 + warp * 16 + g4, t1 = t0 + 8;
+    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
 #pragma unroll
-    for (int d = 0; d < DPT; d++) split_store(out, out + lo_off, orow + d, o[d] * inv);
+    for (int n = 0; n < HD / 8; n++) {
+        const int d = n * 8 + 2 * t4;
+        if (t0 < T) {
+            const size_t row = (size_t)t0 * m.n_heads * HD + (size_t)h * HD + d;
+            split_store(out, out + lo_off, row, o[n][0] * i0);
+            split_store(out, out + lo_off, row + 1, o[n][1] * i0);
+        }
+        if (t1 < T) {
+            const size_t row = (size_t)t1 * m.n_heads * HD + (size_t)h * HD + d;
+            split_store(out, out + lo_off, row, o[n][2] * i1);
+            split_store(out, out + lo_off, row + 1, o[n][3] * i1);
+        }
+    }
 }
+
+template <int HD>
+static size_t attn_tc_smem() { return (size_t)3 * 64 * (HD + 8) * 2; }
 
 // argmax of one row (lowest index on ties); a NaN sets the status word.
 __global__ void argmax_kernel(const float *v, int n, int *out, int *status) {
@@ -248,6 +365,14 @@ static cudaError_t weight_map(CUtensorMap *map, const Mat &M, int layer) {
 
 cudaError_t prefill_prepare(const Model &m, PrefillPlan &p, int rows) {
     p.rows = rows;
+    {
+        cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)attn_tc_smem<64>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)attn_tc_smem<128>());
+        if (e != cudaSuccess) return e;
+    }
     p.maps.resize((size_t)4 * m.n_layers + 1);
     for (int l = 0; l < m.n_layers; l++) {
         cudaError_t e;
@@ -310,9 +435,9 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
             rope_append_kernel<true><<<T, 256, (size_t)m.qkv.rows * 4, s>>>(m, p.qkv, l, seq, p0);
             dim3 ag((T + 63) / 64, m.n_heads);
             if (m.head_dim == 64)
-                attn_prefill_kernel<64, true><<<ag, 256, 0, s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
+                attn_prefill_tc_kernel<64><<<ag, 128, attn_tc_smem<64>(), s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
             else
-                attn_prefill_kernel<128, true><<<ag, 256, 0, s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
+                attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
             PF_CK(cudaGetLastError());
             PF_CK(gemm(p.o_map, p.o_lo_map, p.maps[4 * l + 1], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
