@@ -835,16 +835,16 @@ __device__ __forceinline__ bool is_norm_input(int epi) { return epi == EPI_QKV |
 
 // The chunks of one of a layer's matrices for this CTA, K tile by K tile: chunk i of
 // the step belongs to warp i % 8; with a multiple of 8 ring slots every use of a slot
-// belongs to the same warp, which takes them in order.  At batch 1 a chunk (at most 8
-// rows) is one row group; at larger batches a group is a RoPE / SwiGLU pair or two rows
-// (each activation load then serves two rows).  Each warp goes straight to its own chunks and, before the input is polled,
+// belongs to the same warp, which takes them in order.  At batch 1 a chunk of 4-8 rows
+// is one row group; otherwise a group is a RoPE / SwiGLU pair or two rows (each
+// activation load then serves two rows).  Each warp goes straight to its own chunks and, before the input is polled,
 // waits for its first chunk's weights, loads its first group's pieces into registers
 // and prepares that group's epilogue; after the poll only the arithmetic and the
 // stores remain.  Returns the updated chunk counter.
-template <int NB, bool WBF16>
+template <int NB, bool WBF16, int RG>
 __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                                uint32_t chunk_i, int tslot) {
-    constexpr int RG = NB == 1 ? 8 : 2;  // rows of a group
+    // RG: rows of a group (8 at batch 1 when chunks hold at least 4 rows, else 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
     phase_slice(P, epi, M.rows / M.rows_per_unit, blockIdx.x, u0, u1);
@@ -870,7 +870,7 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
     auto prepare = [&]() {
         const uint32_t ci = chunk_i + (uint32_t)j;
         const int kt = j / cpk, unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0);
-        ng = NB == 1 ? nunits : pairs ? 1 : min(2, nunits - g);  // batches: 2 rows share each activation load
+        ng = min(nunits - g, RG / M.rows_per_unit);  // batches: 2 rows share each activation load
         if (g == 0) wait_slot(P, &S.full[ci % slots], (ci / slots) & 1);
         buf = S.ring + (size_t)(ci % slots) * kChunkBytes + (size_t)g * M.rows_per_unit * rowbytes;
         load_pieces<NB, RG, WBF16>(wp.w, buf, rowbytes, ng * M.rows_per_unit, lane, pieces);
@@ -957,10 +957,10 @@ __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &
     return chunk_i + (uint32_t)nch;
 }
 
-template <int NB, bool WBF16>
+template <int NB, bool WBF16, bool G8>
 __device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                             uint32_t chunk_i, int tslot) {
-    return layer_walk<NB, WBF16>(P, epi, layer, M, S, chunk_i, tslot);
+    return layer_walk<NB, WBF16, (NB == 1 && G8) ? 8 : 2>(P, epi, layer, M, S, chunk_i, tslot);
 }
 
 // The logits and the greedy argmax: per lane, per warp, per CTA best candidates (lowest
@@ -1182,7 +1182,9 @@ __device__ __forceinline__ void attention_phase(const StepParams &P, int layer, 
 
 // ------------------------------------------------------------------ the kernel
 
-template <int NB, bool WBF16>
+// G8: batch-1 row groups of up to 8 rows (models whose chunks hold several rows);
+// otherwise groups of 2 rows or one pair.
+template <int NB, bool WBF16, bool G8>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Shared S = carve(smem_raw, P);
@@ -1215,7 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             }
             const int epi = ph == 0 ? EPI_QKV : ph == 2 ? EPI_WO : ph == 3 ? EPI_W13 : EPI_W2;
             const Mat M = ph == 0 ? m.qkv : ph == 2 ? m.wo : ph == 3 ? m.w13 : m.w2;
-            chunk_i = gemv_phase<NB, WBF16>(P, epi, l, M, S, chunk_i, t);
+            chunk_i = gemv_phase<NB, WBF16, G8>(P, epi, l, M, S, chunk_i, t);
         }
     }
     if (P.do_logits) logits_phase<NB, WBF16>(P, S, chunk_i, m.n_layers * kTracePerLayer);
@@ -1227,9 +1229,9 @@ size_t decode_smem_bytes(int xs_bytes, int ring_slots) {
     return ring_offset(xs_bytes) + (size_t)ring_slots * kChunkBytes;
 }
 
-template <int NB, bool WBF16>
+template <int NB, bool WBF16, bool G8>
 static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
-    auto fn = decode_step_kernel<NB, WBF16>;
+    auto fn = decode_step_kernel<NB, WBF16, G8>;
     const size_t smem = decode_smem_bytes(P.xs_bytes, P.ring_slots);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1239,10 +1241,10 @@ static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
 
 template <bool WBF16>
 static cudaError_t launch_w(const StepParams &P, cudaStream_t stream) {
-    if (P.batch <= 1) return launch_nb<1, WBF16>(P, stream);
-    if (P.batch <= 4) return launch_nb<4, WBF16>(P, stream);
-    if (P.batch <= 8) return launch_nb<8, WBF16>(P, stream);
-    return launch_nb<16, WBF16>(P, stream);
+    if (P.batch <= 1) return P.wide_groups ? launch_nb<1, WBF16, true>(P, stream) : launch_nb<1, WBF16, false>(P, stream);
+    if (P.batch <= 4) return launch_nb<4, WBF16, false>(P, stream);
+    if (P.batch <= 8) return launch_nb<8, WBF16, false>(P, stream);
+    return launch_nb<16, WBF16, false>(P, stream);
 }
 
 cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream) {
@@ -1250,7 +1252,7 @@ cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream) {
 }
 
 cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm) {
-    auto fn = weight_bf16 ? decode_step_kernel<1, true> : decode_step_kernel<1, false>;
+    auto fn = weight_bf16 ? decode_step_kernel<1, true, true> : decode_step_kernel<1, false, true>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kThreads, smem);

@@ -579,6 +579,7 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
 static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
     P.m = c->m;
     P.grid = c->grid;
+    P.wide_groups = c->m.w13.rows_per_chunk >= 4;  // the largest layer matrix sets the group width
     if (++c->launch_seq == 0) c->launch_seq = 1;  // tag 0 marks never-written words
     P.tag = c->launch_seq;
     P.trace = c->trace_on ? c->d_trace : nullptr;

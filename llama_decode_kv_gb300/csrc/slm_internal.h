@@ -101,6 +101,7 @@ struct StepParams {
     int res_cta0;
     int roles;
     int role0[5];
+    int wide_groups;                // batch 1: row groups of up to 8 rows (else 2)
     const int *tokens;              // device [batch]
     float *logits;                  // device [batch][vocab] or null
     int *next_ids;                  // device [batch] or null
