@@ -907,10 +907,10 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
 
 // The logits: chunks of up to R rows per group (8 at batch 1), each lane keeping the
 // best (value, index) per batch row.
-template <int NB, bool WBF16>
+template <int NB, bool WBF16, bool G8>
 __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &M, Shared &S, uint32_t chunk_i, int tslot,
                                                 float (&best_v)[NB], int (&best_i)[NB]) {
-    constexpr int R = NB == 1 ? 8 : GemvShape<NB>::R;
+    constexpr int R = NB == 1 ? (G8 ? 8 : 2) : GemvShape<NB>::R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
     phase_slice(P, 4, M.rows, blockIdx.x, u0, u1);
@@ -965,7 +965,7 @@ __device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int
 
 // The logits and the greedy argmax: per lane, per warp, per CTA best candidates (lowest
 // index on ties); CTA 0 collects every CTA's candidate.
-template <int NB, bool WBF16>
+template <int NB, bool WBF16, bool G8>
 __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uint32_t chunk_i, int tslot) {
     const Model &m = P.m;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -977,7 +977,7 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
         best_v[b] = -INFINITY;
         best_i[b] = 0x7fffffff;
     }
-    logits_walk<NB, WBF16>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
+    logits_walk<NB, WBF16, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
     trace_mark(P, tslot + 1, 0);
     compute_sync();  // the logits phase is done with S.xs
 #pragma unroll
@@ -1220,7 +1220,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             chunk_i = gemv_phase<NB, WBF16, G8>(P, epi, l, M, S, chunk_i, t);
         }
     }
-    if (P.do_logits) logits_phase<NB, WBF16>(P, S, chunk_i, m.n_layers * kTracePerLayer);
+    if (P.do_logits) logits_phase<NB, WBF16, G8>(P, S, chunk_i, m.n_layers * kTracePerLayer);
 }
 
 // ------------------------------------------------------------------ host-side launch
