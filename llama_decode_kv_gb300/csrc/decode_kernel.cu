@@ -1233,8 +1233,12 @@ template <int NB, bool WBF16, bool G8>
 static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
     auto fn = decode_step_kernel<NB, WBF16, G8>;
     const size_t smem = decode_smem_bytes(P.xs_bytes, P.ring_slots);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    static size_t smem_set = 0;  // the attribute only grows; set it once per size (host latency per step)
+    if (smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
     void *args[] = {(void *)&P};
     return cudaLaunchCooperativeKernel((const void *)fn, dim3(P.grid), dim3(kThreads), args, smem, stream);
 }

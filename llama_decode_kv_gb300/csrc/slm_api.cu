@@ -48,6 +48,8 @@ struct slm_ctx {
     float *d_logits = nullptr;   // staging for host-requested logits [max_batch][vocab]
     int *d_ids = nullptr;        // staging for host-requested ids [max_batch]
     int *h_ids = nullptr;        // pinned
+    int *h_step = nullptr;       // mapped pinned [2][kMaxBatch]: host tokens, then ids, of a step
+    int *d_step = nullptr;       //   its device address (the kernel reads / writes it directly)
     std::string err;
 };
 
@@ -248,6 +250,7 @@ extern "C" void slm_destroy(slm_ctx *ctx) {
     cudaDeviceSynchronize();
     for (void *p : ctx->allocs) cudaFree(p);
     if (ctx->h_ids) cudaFreeHost(ctx->h_ids);
+    if (ctx->h_step) cudaFreeHost(ctx->h_step);
     delete ctx;
 }
 
@@ -470,6 +473,8 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         CK(c, cudaMemset(*b.dst, 0, b.bytes));
     }
     CK(c, cudaMallocHost((void **)&c->h_ids, (size_t)B * 4));
+    CK(c, cudaHostAlloc((void **)&c->h_step, (size_t)2 * kMaxBatch * 4, cudaHostAllocMapped));
+    CK(c, cudaHostGetDevicePointer((void **)&c->d_step, c->h_step, 0));
     // tensor-core prefill buffers (blocks of up to 2048 prompt positions)
     if (prefill_supported(m)) {
         PrefillPlan &pp = c->plan;
@@ -626,22 +631,24 @@ extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids
         for (int i = 0; i < batch; i++)
             if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab)
                 return fail(c, SLM_EINVAL, "token %d out of range at row %d", tokens[i], i);
-        CK(c, cudaMemcpyAsync(c->d_tokens, tokens, (size_t)batch * 4, cudaMemcpyHostToDevice, s));
-        P.tokens = c->d_tokens;
+        // host tokens: the kernel reads them from mapped pinned memory (no copy launch);
+        // every call with host buffers ends with a synchronisation, so no earlier step
+        // still reads this buffer
+        memcpy(c->h_step, tokens, (size_t)batch * 4);
+        P.tokens = c->d_step;
     } else {
         P.tokens = tokens;
     }
     P.logits = logits ? (log_dev ? logits : c->d_logits) : nullptr;
-    P.next_ids = ids_dev ? next_ids : c->d_ids;
+    P.next_ids = ids_dev ? next_ids : c->d_step + kMaxBatch;  // host ids: written straight to mapped memory
     P.do_logits = 1;
     int rc = launch(c, P, s);
     if (rc) return rc;
     for (int i = 0; i < batch; i++) c->len[P.seq[i]] = P.pos[i] + 1;
     if (!log_dev) CK(c, cudaMemcpyAsync(logits, c->d_logits, (size_t)batch * c->cfg.vocab * 4, cudaMemcpyDeviceToHost, s));
-    if (!ids_dev) CK(c, cudaMemcpyAsync(c->h_ids, c->d_ids, (size_t)batch * 4, cudaMemcpyDeviceToHost, s));
     if (!tok_dev || !log_dev || !ids_dev) {
         CK(c, cudaStreamSynchronize(s));
-        if (!ids_dev) memcpy(next_ids, c->h_ids, (size_t)batch * 4);
+        if (!ids_dev) memcpy(next_ids, c->h_step + kMaxBatch, (size_t)batch * 4);
     }
     return SLM_OK;
 }
