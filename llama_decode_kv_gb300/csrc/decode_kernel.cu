@@ -111,6 +111,29 @@ __device__ __forceinline__ int xpos(int k, int KBp, bool perm) {
     return perm ? ((k & 4) ? (KBp >> 1) : 0) + ((k >> 3) << 2) + (k & 3) : k;
 }
 
+// Batch-16 tensor-core phases keep their activations as two bf16 planes, hi and lo
+// (x = hi + lo to about 16 mantissa bits), rows of `pld` elements, lo plane 16 rows
+// after hi; element (r, j) of both at r * pld + j.
+__device__ __forceinline__ void plane_store(uint16_t *hi, int pld, int r, int j, float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+    hi[r * pld + j] = *(const uint16_t *)&h;
+    hi[kMaxBatch * pld + r * pld + j] = *(const uint16_t *)&l;
+}
+
+// Elements (r, j) and (r, j + 1), j even.
+__device__ __forceinline__ void plane_store2(uint16_t *hi, int pld, int r, int j, float x0, float x1) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    *(__nv_bfloat162 *)(hi + r * pld + j) = h;
+    *(__nv_bfloat162 *)(hi + kMaxBatch * pld + r * pld + j) = l;
+}
+
+__device__ __forceinline__ float plane_load(const uint16_t *hi, int pld, int r, int j) {
+    return __uint_as_float((uint32_t)hi[r * pld + j] << 16) + __uint_as_float((uint32_t)hi[kMaxBatch * pld + r * pld + j] << 16);
+}
+
 // Timeline hook: thread 0 of each CTA stamps (phase, point) when tracing is on.
 __device__ __forceinline__ void trace_mark(const StepParams &P, int slot, int point) {
     if (P.trace && threadIdx.x == 0)
@@ -119,16 +142,18 @@ __device__ __forceinline__ void trace_mark(const StepParams &P, int slot, int po
 
 // ------------------------------------------------------------------ polling
 
-constexpr int kPollBatch = 8;  // loads each thread keeps in flight
+constexpr int kPollBatch = 8;   // loads each thread keeps in flight
+constexpr int kPollBatchW = 8;   //   (rows of a batch)
 
 // Poll rows x len tagged words src[r * src_ld + j] into shared memory dst[r * dst_ld +
 // xpos(j)] (natural order when perm_ld is 0) until every tag equals the launch's tag.
-// With `gain` (a single row): element j is stored as x_j * gain_j and each warp stores
-// its sum of x_j^2 in ssp[warp * kMaxBatch].  All compute threads call it; it ends with
-// their barrier.
+// With `gain`: element j is stored as x_j * gain_j and each warp stores its part of row
+// r's sum of x_j^2 in ssp[warp * kMaxBatch + r] (every r < rows; one row for WIDE = 1).
+// All compute threads call it; it ends with their barrier.
 template <int WIDE = 1>
 __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *src, int src_ld, int rows, int len,
-                                        float *dst, int dst_ld, int perm_ld, const float *gain, float *ssp) {
+                                        float *dst, int dst_ld, int perm_ld, const float *gain, float *ssp,
+                                        bool planes = false) {
     const int tid = threadIdx.x;
     const uint32_t tag = P.tag;
     // WIDE = 2 (long vectors of batched rows): words are fetched two at a time (one
@@ -181,61 +206,100 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                 }
             }
         }
+        if (ssp) {
+            ss = warp_sum(ss);
+            if ((tid & 31) == 0) ssp[(tid >> 5) * kMaxBatch] = ss;
+        }
     } else {
-    const int n = rows * len / wpl;  // loads
-    for (int base = 0; base < n; base += kComputeThreads * kPollBatch) {
-        int so[kPollBatch];
-        uint32_t pend = 0;  // bit 2k + h: word h of load k still missing
+    // Row b is polled by threads [b * tpr, (b + 1) * tpr): a thread's words all belong to
+    // one row, so its sum of squares is that row's.
+    int rp = 1;
+    while (rp < rows) rp <<= 1;
+    const int tpr = kComputeThreads / rp;  // >= 16
+    const int b = tid / tpr, t = tid - b * tpr;
+    const int nl = len / wpl;  // loads per row
+    // Every CTA reads the same block: each starts at its own column.
+    const int rot = (int)(((long long)blockIdx.x * nl) / gridDim.x);
+    if (b < rows) {
+        const uint64_t *srow = src + (size_t)b * src_ld;
+        for (int base = 0; base < nl; base += tpr * kPollBatchW) {
+            int wj[kPollBatchW];  // first word (column) of load k
+            float g0[kPollBatchW], g1[kPollBatchW];
+            uint32_t pend = 0;   // bit 2k + h: word h of load k still missing
 #pragma unroll
-        for (int k = 0; k < kPollBatch; k++) {
-            const int l = base + k * kComputeThreads + tid;
-            const int i = l < n ? l * wpl : 0;  // first word of the load
-            const int r = i / len;
-            so[k] = r * src_ld + (i - r * len);
-            if (l < n) pend |= (wpl == 2 ? 3u : 1u) << (2 * k);
-        }
-        unsigned long long t0 = 0;
-        for (int it = 0;; it++) {
-            uint64_t w[kPollBatch][2];
-#pragma unroll
-            for (int k = 0; k < kPollBatch; k++) {
-                w[k][0] = w[k][1] = 0;
-                if (pend & (3u << (2 * k))) {
-                    if (wpl == 2)
-                        ll_load2(src + so[k], w[k][0], w[k][1]);
-                    else
-                        w[k][0] = ll_load(src + so[k]);
-                }
+            for (int k = 0; k < kPollBatchW; k++) {
+                const int l = base + k * tpr + t;
+                int e = l + rot;
+                if (e >= nl) e -= nl;
+                wj[k] = l < nl ? e * wpl : 0;
+                g0[k] = (gain && l < nl) ? __ldg(gain + wj[k]) : 1.f;
+                g1[k] = (gain && l < nl && wpl == 2) ? __ldg(gain + wj[k] + 1) : 1.f;
+                if (l < nl) pend |= (wpl == 2 ? 3u : 1u) << (2 * k);
             }
+            unsigned long long t0 = 0;
+            for (int it = 0;; it++) {
+                uint64_t w[kPollBatchW][2];
 #pragma unroll
-            for (int k = 0; k < kPollBatch; k++)
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const uint32_t bit = 1u << (2 * k + h);
-                    if (!(pend & bit) || (uint32_t)(w[k][h] >> 32) != tag) continue;
-                    pend &= ~bit;
-                    const int i = (base + k * kComputeThreads + tid) * wpl + h;  // word index
-                    const int r = i / len, j = i - r * len;
-                    const float x = __uint_as_float((uint32_t)w[k][h]);
-                    ss = fmaf(x, x, ss);
-                    dst[r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j)] = gain ? x * __ldg(gain + j) : x;
+                for (int k = 0; k < kPollBatchW; k++) {
+                    w[k][0] = w[k][1] = 0;
+                    if (pend & (3u << (2 * k))) {
+                        if (wpl == 2)
+                            ll_load2(srow + wj[k], w[k][0], w[k][1]);
+                        else
+                            w[k][0] = ll_load(srow + wj[k]);
+                    }
                 }
-            if (!pend) break;
-            if (it == 0) t0 = global_ns();
-            if ((it & 15) == 15) {  // the abort flag and the clock, every 16 rounds
-                if (ld_volatile_int(P.m.abort_flag)) break;
-                if (global_ns() - t0 > kWaitLimitNs) {
-                    atomicOr(P.m.status, kStExchangeTimeout);
-                    atomicExch(P.m.abort_flag, 1);
-                    break;
+#pragma unroll
+                for (int k = 0; k < kPollBatchW; k++) {
+                    if (planes && wpl == 2 && ((pend >> (2 * k)) & 3u) == 3u && (uint32_t)(w[k][0] >> 32) == tag &&
+                        (uint32_t)(w[k][1] >> 32) == tag) {  // both words: one 32-bit store per plane
+                        pend &= ~(3u << (2 * k));
+                        const float x0 = __uint_as_float((uint32_t)w[k][0]), x1 = __uint_as_float((uint32_t)w[k][1]);
+                        ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+                        plane_store2((uint16_t *)dst, dst_ld, b, wj[k], x0 * g0[k], x1 * g1[k]);
+                        continue;
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const uint32_t bit = 1u << (2 * k + h);
+                        if (!(pend & bit) || (uint32_t)(w[k][h] >> 32) != tag) continue;
+                        pend &= ~bit;
+                        const int j = wj[k] + h;
+                        const float x = __uint_as_float((uint32_t)w[k][h]);
+                        ss = fmaf(x, x, ss);
+                        const float y = x * (h ? g1[k] : g0[k]);
+                        if (planes)  // dst_ld is the plane row length
+                            plane_store((uint16_t *)dst, dst_ld, b, j, y);
+                        else
+                            dst[b * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j)] = y;
+                    }
+                }
+                if (!pend) break;
+                if (it == 0) t0 = global_ns();
+                if ((it & 15) == 15) {  // the abort flag and the clock, every 16 rounds
+                    if (ld_volatile_int(P.m.abort_flag)) break;
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(P.m.status, kStExchangeTimeout);
+                        atomicExch(P.m.abort_flag, 1);
+                        break;
+                    }
                 }
             }
         }
     }
+    if (ssp) {  // per warp and row: lanes of one row are min(tpr, 32) consecutive lanes
+        const int wl = tpr < 32 ? tpr : 32;
+        for (int off = wl >> 1; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const int warp = tid >> 5, lane = tid & 31;
+        const float s0 = __shfl_sync(0xffffffffu, ss, 0), s16 = __shfl_sync(0xffffffffu, ss, 16);
+        const int row_a = (warp * 32) / tpr, row_b = (warp * 32 + 16) / tpr;  // rows of lanes 0 and 16
+        if (lane < rows) {
+            float v = 0.f;
+            if (lane == row_a) v += s0;
+            if (row_b != row_a && lane == row_b) v += s16;
+            ssp[warp * kMaxBatch + lane] = v;
+        }
     }
-    if (ssp) {
-        ss = warp_sum(ss);
-        if ((tid & 31) == 0) ssp[(tid >> 5) * kMaxBatch] = ss;
     }
     compute_sync();
 }
@@ -383,7 +447,8 @@ __device__ __forceinline__ void init_residual(const StepParams &P, Shared &S) {
 // row b in ssp[warp * kMaxBatch + b] (0 for rows it does not hold) and every element is
 // multiplied by its gain.  Rows are spread over power-of-two groups of threads.  Ends
 // with a barrier.
-__device__ __forceinline__ void norm_pass(const StepParams &P, float *xs, int ld, bool perm, const float *gain, float *ssp) {
+__device__ __forceinline__ void norm_pass(const StepParams &P, float *xs, int ld, bool perm, const float *gain, float *ssp,
+                                          int pld = 0) {
     const int batch = P.batch, dim = P.m.dim;
     int rp = 1;
     while (rp < batch) rp <<= 1;
@@ -392,11 +457,26 @@ __device__ __forceinline__ void norm_pass(const StepParams &P, float *xs, int ld
     float ss = 0.f;
     if (b < batch) {
         float *r = xs + (size_t)b * ld;
-        for (int j = t; j < dim; j += tpr) {
-            const int q = xpos(j, ld, perm);
-            const float x = r[q];
-            ss = fmaf(x, x, ss);
-            r[q] = x * __ldg(gain + j);
+        constexpr int U = 4;  // gains fetched U at a time: no chain of dependent loads
+        for (int j0 = t; j0 < dim; j0 += U * tpr) {
+            float gv[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) gv[u] = j0 + u * tpr < dim ? __ldg(gain + j0 + u * tpr) : 0.f;
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int j = j0 + u * tpr;
+                if (j >= dim) break;
+                if (pld) {  // activation planes
+                    const float x = plane_load((const uint16_t *)xs, pld, b, j);
+                    ss = fmaf(x, x, ss);
+                    plane_store((uint16_t *)xs, pld, b, j, x * gv[u]);
+                    continue;
+                }
+                const int q = xpos(j, ld, perm);
+                const float x = r[q];
+                ss = fmaf(x, x, ss);
+                r[q] = x * gv[u];
+            }
         }
     }
     const int w = tpr < 32 ? tpr : 32;  // lanes of one row within a warp
@@ -413,22 +493,35 @@ __device__ __forceinline__ void norm_pass(const StepParams &P, float *xs, int ld
     compute_sync();
 }
 
-__device__ void zero_pad(const StepParams &P, float *xs, int ld, int from, bool perm) {
+__device__ void zero_pad(const StepParams &P, float *xs, int ld, int from, bool perm, int pld = 0) {
+    if (pld) {  // activation planes: columns [from, ld) of the live rows of both planes.
+        // Rows past the batch may hold anything: an MMA output row depends only on its
+        // own activation row, and those outputs are dropped.
+        const int n = ld - from;
+        if (n <= 0) return;
+        uint16_t *h = (uint16_t *)xs;
+        for (int e = threadIdx.x; e < 2 * P.batch * n; e += kComputeThreads) {
+            const int q = e / n, k = from + (e - q * n);  // q: plane-row (plane q / batch)
+            const int plane = q >= P.batch, r = q - plane * P.batch;
+            h[(plane * kMaxBatch + r) * pld + k] = 0;
+        }
+        return;
+    }
     for (int b = 0; b < P.batch; b++)
         for (int k = from + (int)threadIdx.x; k < ld; k += kComputeThreads) xs[(size_t)b * ld + xpos(k, ld, perm)] = 0.f;
 }
 
 // Merge the chunk states of every (row, head) published by the attention items into
 // the Wo input tile: o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
-__device__ __forceinline__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M, Shared &S) {
+__device__ __forceinline__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M, Shared &S, int pld) {
     const Model &m = P.m;
     const bool perm = m.weight_bf16;
     const int H = m.n_heads, hd = m.head_dim, st = hd + 2;
     int ncmax = 1;
     for (int b = 0; b < P.batch; b++) ncmax = max(ncmax, P.nchunk[b]);
-    float *stage = S.xs + (size_t)P.batch * M.KBp;  // [batch][H][ncmax][hd + 2]
+    float *stage = S.xs + (pld ? (size_t)kMaxBatch * pld : (size_t)P.batch * M.KBp);  // [batch][H][ncmax][hd + 2]
     const uint64_t *src = m.ll_part + ll_layer(P, layer, H * kMaxChunksA * st);
-    zero_pad(P, S.xs, M.KBp, H * hd, perm);
+    zero_pad(P, S.xs, M.KBp, H * hd, perm, pld);
     for (int b = 0; b < P.batch; b++) {
         const int nc = P.nchunk[b];
         // rows (b, h) x (nc * st) words, source row stride kMaxChunksA * st
@@ -450,7 +543,10 @@ __device__ __forceinline__ void merge_chunk_states(const StepParams &P, int laye
                 L = fmaf(sp[(size_t)c * st + 1], sc, L);
                 O = fmaf(sp[(size_t)c * st + 2 + d], sc, O);
             }
-            S.xs[(size_t)b * M.KBp + xpos(e, M.KBp, perm)] = O / L;
+            if (pld)
+                plane_store((uint16_t *)S.xs, pld, b, e, O / L);
+            else
+                S.xs[(size_t)b * M.KBp + xpos(e, M.KBp, perm)] = O / L;
         }
     }
     compute_sync();
@@ -465,12 +561,15 @@ __device__ __forceinline__ void stage_input(const StepParams &P, int epi, int la
     const int tid = threadIdx.x;
     const bool perm = m.weight_bf16;
     const int pl = perm ? M.KBp : 0;
+    const int pld = (NB == kMaxBatch && perm) ? M.KBp + 8 : 0;  // activation planes (tensor-core phases)
+    float *dst = S.xs;
+    const int dld = pld ? pld : M.KBp;
     compute_sync();  // everyone is done with the previous tile
     if (epi == EPI_QKV || epi == EPI_W13 || epi == EPI_LOGITS) {
         const float *g = epi == EPI_QKV   ? m.norms + (size_t)layer * 2 * m.dim
                          : epi == EPI_W13 ? m.norms + (size_t)layer * 2 * m.dim + m.dim
                                           : m.norms + (size_t)m.n_layers * 2 * m.dim;
-        zero_pad(P, S.xs, M.KBp, m.dim, perm);
+        zero_pad(P, S.xs, M.KBp, m.dim, perm, pld);
         if (epi == EPI_QKV && tid < P.batch) {  // the QKV epilogue's RoPE rows, into L1 meanwhile
             const float *rr = m.rope + (size_t)P.pos[tid] * m.head_dim;
             for (int k = 0; k < m.head_dim; k += 32) prefetch_l1(rr + k);
@@ -478,34 +577,34 @@ __device__ __forceinline__ void stage_input(const StepParams &P, int epi, int la
         if (epi == EPI_QKV && layer == 0) {
             for (int b = 0; b < P.batch; b++) {
                 const int tok = token_of(P, b);
-                for (int k = tid; k < m.dim; k += kComputeThreads)
-                    S.xs[(size_t)b * M.KBp + xpos(k, M.KBp, perm)] = emb_elem(m, tok, k);
+                for (int k = tid; k < m.dim; k += kComputeThreads) {
+                    if (pld)
+                        plane_store((uint16_t *)S.xs, pld, b, k, emb_elem(m, tok, k));
+                    else
+                        S.xs[(size_t)b * M.KBp + xpos(k, M.KBp, perm)] = emb_elem(m, tok, k);
+                }
             }
             compute_sync();
-            norm_pass(P, S.xs, M.KBp, perm, g, S.ssp);
+            norm_pass(P, S.xs, M.KBp, perm, g, S.ssp, pld);
         } else {
             const uint64_t *src = epi == EPI_W13 ? m.ll_xa + ll_layer(P, layer, m.dim)
                                                  : m.ll_x + ll_layer(P, epi == EPI_QKV ? layer : m.n_layers, m.dim);
-            if (P.batch == 1) {
-                poll_words<(NB > 1 ? 2 : 1)>(P, src, m.dim, 1, m.dim, S.xs, M.KBp, pl, g, S.ssp);
-            } else {
-                poll_words<(NB > 1 ? 2 : 1)>(P, src, m.dim, P.batch, m.dim, S.xs, M.KBp, pl, nullptr, nullptr);
-                norm_pass(P, S.xs, M.KBp, perm, g, S.ssp);
-            }
+            poll_words<(NB > 1 ? 2 : 1)>(P, src, m.dim, P.batch, m.dim, dst, dld, pl, g, S.ssp, pld > 0);
         }
     } else if (epi == EPI_WO) {
         if (P.attn_consumer_merge) {
-            merge_chunk_states(P, layer, M, S);
+            merge_chunk_states(P, layer, M, S, pld);
         } else {
             const int qd = m.n_heads * m.head_dim;
-            zero_pad(P, S.xs, M.KBp, qd, perm);
-            poll_words<(NB > 1 ? 2 : 1)>(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, S.xs, M.KBp, pl, nullptr, nullptr);
+            zero_pad(P, S.xs, M.KBp, qd, perm, pld);
+            poll_words<(NB > 1 ? 2 : 1)>(P, m.ll_o + ll_layer(P, layer, qd), qd, P.batch, qd, dst, dld, pl, nullptr, nullptr,
+                                         pld > 0);
         }
     } else {  // W2: tile kt of the SwiGLU output
         const int k0 = kt * M.KB, kn = min(M.K - k0, M.KB);
-        zero_pad(P, S.xs, M.KBp, kn, perm);
-        poll_words<(NB > 1 ? 2 : 1)>(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, S.xs, M.KBp, pl, nullptr,
-                   nullptr);
+        zero_pad(P, S.xs, M.KBp, kn, perm, pld);
+        poll_words<(NB > 1 ? 2 : 1)>(P, m.ll_h + ll_layer(P, layer, m.hidden) + k0, m.hidden, P.batch, kn, dst, dld, pl,
+                                     nullptr, nullptr, pld > 0);
     }
 }
 
@@ -957,10 +1056,202 @@ __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &
     return chunk_i + (uint32_t)nch;
 }
 
+// ------------------------------------------------------------------ batch 16: tensor cores
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+
+__device__ __forceinline__ void ldsm2(uint32_t &r0, uint32_t &r1, const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(smem_addr(p)));
+}
+
+// One value of a batch-16 tensor-core tile: row `unit` (pairs: its first row) of the
+// CTA's slice for batch row b.  Same epilogues as the CUDA-core groups.
+__device__ __forceinline__ Cand mma_epilogue(const StepParams &P, int epi, int layer, const Mat &M, Shared &S, int u0,
+                                             int i, int b, float v, float v2, int kt) {
+    const Model &m = P.m;
+    Cand cd{-INFINITY, 0, 0};
+    const uint32_t tag = P.tag;
+    const int unit = u0 + i;
+    if (epi == EPI_W13 || epi == EPI_QKV) {  // pair unit: v = first row, v2 = second
+        const float rs = inv_rms(m, S.ssp, b);
+        const float x1 = v * rs, x2 = v2 * rs;
+        if (epi == EPI_W13) {
+            const float sg = x1 / (1.0f + __expf(-x1));
+            ll_store(m.ll_h + ll_layer(P, layer, m.hidden) + (size_t)b * m.hidden + unit, sg * x2, tag);
+            return cd;
+        }
+        const int hd = m.head_dim, half = hd >> 1, G = m.n_heads / m.n_kv_heads;
+        const int per_group = (G + 2) * half;
+        const int g = unit / per_group, rem = unit - g * per_group;
+        const int sub = rem / half, d = rem - sub * half;
+        const int pos = P.pos[b];
+        float o0 = x1, o1 = x2;
+        if (sub <= G) {
+            const float *rp = m.rope + ((size_t)pos * half + d) * 2;
+            o0 = x1 * rp[0] - x2 * rp[1];
+            o1 = x1 * rp[1] + x2 * rp[0];
+        }
+        if (sub < G) {
+            const float qscale = rsqrtf((float)hd) * 1.4426950408889634f;
+            o0 *= qscale;
+            o1 *= qscale;
+        } else {
+            const bool bf = m.kv_bf16;
+            uint8_t *row = (sub == G ? m.kc : m.vc) +
+                           ((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + pos) * hd * (bf ? 2 : 4);
+            if (bf) {
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(o0), h1 = __float2bfloat16_rn(o1);
+                ((__nv_bfloat16 *)row)[d] = h0;
+                ((__nv_bfloat16 *)row)[d + half] = h1;
+                o0 = __bfloat162float(h0);
+                o1 = __bfloat162float(h1);
+            } else {
+                ((float *)row)[d] = o0;
+                ((float *)row)[d + half] = o1;
+            }
+        }
+        uint64_t *dst = m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + ((size_t)g * (G + 2) + sub) * hd + d;
+        ll_store(dst, o0, tag);
+        ll_store(dst + half, o1, tag);
+        return cd;
+    }
+    if (epi == EPI_LOGITS) {
+        v *= inv_rms(m, S.ssp, b);
+        if (P.logits) P.logits[(size_t)b * m.vocab + unit] = v;
+        if (v != v) {
+            atomicOr(m.status, kStNanLogits);
+        } else {
+            cd.v = v;
+            cd.i = unit;
+            cd.b = b;
+        }
+        return cd;
+    }
+    float t = v;  // Wo / W2: K tiles accumulate, then the residual add
+    if (M.nkt > 1) {
+        float *a = S.accs + (size_t)i * kMaxBatch + b;
+        t = (kt == 0 ? 0.f : *a) + t;
+        *a = t;
+        if (kt != M.nkt - 1) return cd;
+    }
+    float *own = S.xown + b * kMaxOwn + i;
+    const float xn = *own + t;
+    *own = xn;
+    uint64_t *dstw = epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim) : m.ll_x + ll_layer(P, layer + 1, m.dim);
+    ll_store(dstw + (size_t)b * m.dim + unit, xn, tag);
+    return cd;
+}
+
+// A matrix's chunks for this CTA at batch 16, on the tensor cores: each chunk (at most 8
+// rows) is one n8 tile of mma.sync m16n8k16 -- A = the 16 batch rows of activations
+// (bf16 hi and lo planes: two MMAs per K step, fp32 accumulation), B = the chunk's
+// weight rows read with ldmatrix straight from the ring slot.  Chunk ownership and
+// ring protocol as in layer_walk.  For the logits, lanes keep their best candidates.
+template <bool LOGITS>
+__device__ __forceinline__ uint32_t mma_walk(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
+                                             uint32_t chunk_i, int tslot, float (&best_v)[kMaxBatch],
+                                             int (&best_i)[kMaxBatch]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;
+    int u0, u1;
+    phase_slice(P, epi, M.rows / M.rows_per_unit, blockIdx.x, u0, u1);
+    trace_mark(P, tslot, 0);
+    if (u0 == u1) return chunk_i;
+    const int rpu = M.rows_per_unit;
+    const int cu = M.rows_per_chunk / rpu;
+    const int cpk = (u1 - u0 + cu - 1) / cu;
+    const int nch = M.nkt * cpk;
+    const uint32_t slots = (uint32_t)P.ring_slots;
+    const size_t rowbytes = (size_t)M.KBp * 2;
+    const int pld = M.KBp + 8;
+    const uint16_t *hi = (const uint16_t *)S.xs, *lo = hi + kMaxBatch * pld;
+    int j = (warp - (int)(chunk_i & 7)) & 7;
+    if (j < nch) wait_slot(P, &S.full[(chunk_i + (uint32_t)j) % slots], ((chunk_i + (uint32_t)j) / slots) & 1);
+#pragma unroll 1
+    for (int kt = 0; kt < M.nkt; kt++) {
+        stage_input<kMaxBatch>(P, epi, layer, M, kt, S);
+        if (kt == 0) trace_mark(P, tslot, 1);
+#pragma unroll 1
+        for (; j < nch && j < (kt + 1) * cpk; j += kComputeWarps) {
+            const uint32_t ci = chunk_i + (uint32_t)j, slot = ci % slots;
+            wait_slot(P, &S.full[slot], (ci / slots) & 1);
+            const int unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0), nr = nunits * rpu;
+            const uint8_t *buf = S.ring + (size_t)slot * kChunkBytes;
+            // B rows: lanes 0-7 give the rows of k 0..7, lanes 8-15 of k 8..15 (rows past the
+            // chunk read its last row; their outputs are dropped)
+            const uint8_t *bp = buf + (size_t)min(lane & 7, nr - 1) * rowbytes + ((lane >> 3) & 1) * 16;
+            const uint16_t *ah = hi + (lane & 15) * pld + (lane >> 4) * 8, *al = lo + (lane & 15) * pld + (lane >> 4) * 8;
+            // four independent accumulators (hi / lo plane x even / odd K step) keep four
+            // MMA chains in flight instead of one
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+            float f[4] = {0.f, 0.f, 0.f, 0.f}, g[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+            for (int k = 0; k < M.KBp; k += 32) {  // KBp is a multiple of 64
+                uint32_t a[4], c[4], a2[4], c2[4], b0, b1, b2, b3;
+                ldsm4(a, ah + k);
+                ldsm4(c, al + k);
+                ldsm2(b0, b1, bp + k * 2);
+                ldsm4(a2, ah + k + 16);
+                ldsm4(c2, al + k + 16);
+                ldsm2(b2, b3, bp + (k + 16) * 2);
+                mma16816(d, a, b0, b1);
+                mma16816(e, c, b0, b1);
+                mma16816(f, a2, b2, b3);
+                mma16816(g, c2, b2, b3);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; q++) d[q] = (d[q] + f[q]) + (e[q] + g[q]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[slot]);
+            // d0 = (batch g4, row 2 t4), d1 = (g4, 2 t4 + 1), d2 / d3 the same for batch g4 + 8
+            const int n0 = 2 * t4;
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int b = g4 + 8 * h;
+                if (b >= P.batch) continue;
+                const float v0 = d[2 * h], v1 = d[2 * h + 1];
+                if (rpu == 2) {
+                    if (t4 < nunits) mma_epilogue(P, epi, layer, M, S, u0, unit0 + t4, b, v0, v1, kt);
+                } else {
+                    if (n0 < nr) {
+                        const Cand cd = mma_epilogue(P, epi, layer, M, S, u0, unit0 + n0, b, v0, 0.f, kt);
+                        if constexpr (LOGITS) keep_best<kMaxBatch>(cd, best_v, best_i);
+                    }
+                    if (n0 + 1 < nr) {
+                        const Cand cd = mma_epilogue(P, epi, layer, M, S, u0, unit0 + n0 + 1, b, v1, 0.f, kt);
+                        if constexpr (LOGITS) keep_best<kMaxBatch>(cd, best_v, best_i);
+                    }
+                }
+            }
+        }
+    }
+    if (P.trace) compute_sync();
+    trace_mark(P, tslot, 2);
+    return chunk_i + (uint32_t)nch;
+}
+
 template <int NB, bool WBF16, bool G8>
 __device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                             uint32_t chunk_i, int tslot) {
-    return layer_walk<NB, WBF16, (NB == 1 && G8) ? 8 : 2>(P, epi, layer, M, S, chunk_i, tslot);
+    if constexpr (NB == kMaxBatch && WBF16) {  // batch 16: tensor cores
+        float bv[kMaxBatch];
+        int bi[kMaxBatch];
+        return mma_walk<false>(P, epi, layer, M, S, chunk_i, tslot, bv, bi);
+    } else {
+        return layer_walk<NB, WBF16, (NB == 1 && G8) ? 8 : 2>(P, epi, layer, M, S, chunk_i, tslot);
+    }
 }
 
 // The logits and the greedy argmax: per lane, per warp, per CTA best candidates (lowest
@@ -977,7 +1268,10 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
         best_v[b] = -INFINITY;
         best_i[b] = 0x7fffffff;
     }
-    logits_walk<NB, WBF16, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
+    if constexpr (NB == kMaxBatch && WBF16)
+        mma_walk<true>(P, EPI_LOGITS, 0, m.emb, S, chunk_i, tslot, best_v, best_i);
+    else
+        logits_walk<NB, WBF16, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
     trace_mark(P, tslot + 1, 0);
     compute_sync();  // the logits phase is done with S.xs
 #pragma unroll

@@ -120,7 +120,9 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
     for (int nkt = 1; nkt <= 64; nkt++) {
         int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), kPadElems);
         int real_nkt = (K + KB - 1) / KB;
-        size_t xs = (size_t)max_batch * KB * 4;
+        // batches of more than 8 rows run the tensor-core kernel: 16 rows of bf16 hi + lo
+        // planes, padded by 8 elements
+        size_t xs = max_batch > 8 ? (size_t)kMaxBatch * (KB + 8) * 4 : (size_t)max_batch * KB * 4;
         size_t unit_bytes = (size_t)KB * esz * rows_per_unit;
         if (xs <= kXsBudget && unit_bytes <= (size_t)kChunkBytes) {
             if (real_nkt > 1 && !allow_split) return false;
@@ -327,8 +329,10 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     {
         const int G = H / KV;
         size_t need = 0;
-        for (const Mat *M : {&m.emb, &m.qkv, &m.w13}) need = std::max(need, ((size_t)B * M->KBp + dim) * 4);
-        for (const Mat *M : {&m.wo, &m.w2}) need = std::max(need, (size_t)B * M->KBp * 4);
+        // activation tile (the tensor-core kernel of batches > 8 keeps 16 padded rows)
+        auto tile = [&](const Mat *M) { return B > 8 ? (size_t)kMaxBatch * (M->KBp + 8) * 4 : (size_t)B * M->KBp * 4; };
+        for (const Mat *M : {&m.emb, &m.qkv, &m.w13}) need = std::max(need, tile(M) + (size_t)dim * 4);
+        for (const Mat *M : {&m.wo, &m.w2}) need = std::max(need, tile(M));
         c->attn_stage = B <= 2 ? 16 * 1024 : 32 * 1024;
         need = std::max(need, (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) + (G + 2) * hd) * 4 +
                                   c->attn_stage);
@@ -557,7 +561,7 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
     // cost more than letting the last CTA of each (row, kv head) merge
     nc_fit = std::min<long long>(nc_fit, 8192 / ((long long)P.batch * H * (hd + 2)));
     P.attn_consumer_merge = 0;
-    if (nc_fit >= 1) {
+    if (nc_fit >= 1 && P.batch <= 8) {  // larger batches: producer merge (the Wo tile is planes there)
         long long ch_a = std::max<long long>(ch, (max_ctx + nc_fit - 1) / nc_fit);
         ch_a = (ch_a + 31) / 32 * 32;
         if (ch_a <= 4 * std::max<long long>(ch, 128)) {

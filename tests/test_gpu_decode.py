@@ -177,3 +177,21 @@ def test_smol_b1_workload_full(slm):
     eng = _engine(slm, s, W)
     g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, wl.decode_steps, 1, [0])
     compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, [0], "smol_b1")
+
+
+@pytest.mark.parametrize("name,batch", [("bf16_tc_b13", 13), ("bf16_tc_b16_bf16kv", 16)])
+def test_batch16_tensor_core_path(slm, name, batch):
+    # batches of 9..16 rows with bf16 weights run the GEMV phases and the logits on the
+    # tensor cores (activations as bf16 hi + lo planes); ragged contexts
+    kv = synth.DTYPE_BF16 if "bf16kv" in name else synth.DTYPE_F32
+    s = synth.TINY.replace(max_batch=16, max_seq=96, weight_dtype=synth.DTYPE_BF16, kv_dtype=kv,
+                           dim=128, n_heads=4, n_kv_heads=2, head_dim=32, hidden=200, vocab=300)
+    W = synth.make_weights(s, seed=13)
+    lens = [3 + (7 * r) % 40 for r in range(batch)]
+    prompts = [synth.make_prompt(s, r, lens[r]) for r in range(batch)]
+    steps = 4
+    rows = list(range(batch))
+    ref_ids, ref_logits = oracle_reference(s, prompts, steps, rows, seed=13)
+    eng = _engine(slm, s, W)
+    g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, steps, batch, rows)
+    compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, rows, name)
