@@ -1,5 +1,6 @@
 #!/usr/bin/env python
-"""Decode benchmark: greedy KV-cached decode on the SmolLM2-135M shape at batch 1.
+"""Decode benchmark: greedy KV-cached decode on the SmolLM2-135M shape at batch 1 (headline)
+and batch 16 (the `batch16` object of the same line).
 
 ``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``
 
@@ -199,6 +200,58 @@ def prefill_measure(slm, torch, W, local: int, reps: int = 3):
     return t, flops
 
 
+def batch16_measure(slm, torch, W, local: int, warmup: int = 3):
+    """The SmolLM2 batch-16 workload: 16 independent rows with a bf16 KV cache, each
+    prefilled with a seeded 512-token prompt (tensor-core prefill, untimed), then batched
+    greedy decode steps up to context 1024, timed with CUDA events on the launching
+    stream.  HBM bytes per step = the weights once + every row's K and V reads."""
+    wl = synth.WORKLOADS["smol_b16"]
+    s, B = wl.shape, wl.batch
+    eng = slm.Engine(s, W)  # the weights do not depend on the batch or the cache type
+    dev = torch.device("cuda", local)
+    nid = torch.empty(1, dtype=torch.int32, device=dev)
+    toks = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
+    for r in range(B):
+        rc = eng.prefill(r, torch.as_tensor(synth.make_prompt(s, r, wl.prompt_len)).to(dev), None, nid)
+        if rc != 0:
+            raise RuntimeError(f"slm_prefill: {eng.last_error()}")
+        toks[0][r] = nid[0]
+    rows = list(range(B))
+    state = {"pos": wl.prompt_len, "cur": 0, "ctx": []}
+
+    def step():
+        c = state["cur"]
+        rc = eng.decode_step(rows, toks[c], [state["pos"]] * B, None, toks[1 - c])
+        if rc != 0:
+            raise RuntimeError(f"slm_decode_step: {eng.last_error()}")
+        state["ctx"].append(state["pos"] + 1)
+        state["pos"] += 1
+        state["cur"] = 1 - c
+
+    for _ in range(warmup):
+        step()
+    state["ctx"].clear()
+    n = s.max_seq - state["pos"]
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if eng.sync() != 0:
+        raise RuntimeError(f"device status after the batch-16 run: {eng.last_error()}")
+    eng.close()
+    bytes_step = sum(synth.weight_bytes(s) + B * kv_bytes_read(s, c) for c in state["ctx"]) / n
+    return {"workload": "smol_b16: SmolLM2-135M shape, bf16 KV cache, 16 rows x 512-token prompt, greedy decode "
+                        f"to context {s.max_seq}",
+            "tokens_per_s": B * n / (ms / 1e3), "ms_per_step": ms / n, "steps": n, "warmup": warmup,
+            "contexts": [min(state["ctx"]), max(state["ctx"])], "bytes_per_step": bytes_step,
+            "hbm_gbs": bytes_step / (ms / 1e3 / n) / 1e9}
+
+
 def cpu_baseline(shape, W, prompt, budget_s: float):
     """The oracle, as it stands, on the host: greedy decode steps after the prompt."""
     import oracle
@@ -339,6 +392,9 @@ def run_ours(args, world, rank, local):
 
     pf_t, pf_flops = prefill_measure(slm, torch, W, local)
     tflops_peak = peaks_tensor()
+    b16 = batch16_measure(slm, torch, W, local)
+    b16["roofline_frac"] = b16["hbm_gbs"] / peak
+    b16["peak_gbs"] = peak
 
     if rank != 0:
         return
@@ -372,6 +428,7 @@ def run_ours(args, world, rank, local):
                     "tflops": pf_flops / pf_t / 1e12, "peak_tflops": tflops_peak,
                     "frac": pf_flops / pf_t / 1e12 / tflops_peak, "bound": "tensor",
                     "note": "activation operands split into bf16 hi + lo: the tensor cores execute 2x these FLOPs"},
+        "batch16": b16,
         "clocks": clk,
     }
     if world == 1:
