@@ -50,20 +50,11 @@ struct Shared {
     float *wbest_v;     // [kComputeWarps][kMaxBatch]
     int *wbest_i;       // [kComputeWarps][kMaxBatch]
     int *flags;         // [4]: 0 = last-arriver flag
-    float *xown;        // [kMaxBatch][kMaxOwn] residual rows this CTA owns
-    float *accs;        // [kMaxOwn][kMaxBatch] accumulators across K tiles
+    float *xown;        // [max_batch][own_ld] residual rows this CTA owns
+    float *accs;        // [own_ld][kMaxBatch] accumulators across K tiles (if any)
     float *xs;          // activation tile / attention scratch, P.xs_bytes
     uint8_t *ring;      // [P.ring_slots][kChunkBytes]
 };
-
-// Layout: barriers and small arrays, owned residual rows, K-tile accumulators, the
-// activation tile, then the weight ring (sized at create time from what is left).
-constexpr int kMiscBytes = 2 * kMaxRingSlots * 8 + 3 * kComputeWarps * kMaxBatch * 4 + 16;
-constexpr int kOwnOffset = ((kMiscBytes + 127) / 128) * 128;
-constexpr int kAccOffset = kOwnOffset + kMaxBatch * kMaxOwn * 4;
-constexpr int kXsOffset = kAccOffset + kMaxOwn * kMaxBatch * 4;
-
-__host__ __device__ inline size_t ring_offset(int xs_bytes) { return ((size_t)kXsOffset + xs_bytes + 1023) / 1024 * 1024; }
 
 __device__ __forceinline__ Shared carve(uint8_t *base, const StepParams &P) {
     Shared s;
@@ -79,10 +70,10 @@ __device__ __forceinline__ Shared carve(uint8_t *base, const StepParams &P) {
     s.wbest_i = (int *)p;
     p += kComputeWarps * kMaxBatch * 4;
     s.flags = (int *)p;
-    s.xown = (float *)(base + kOwnOffset);
-    s.accs = (float *)(base + kAccOffset);
-    s.xs = (float *)(base + kXsOffset);
-    s.ring = base + ring_offset(P.xs_bytes);
+    s.xown = (float *)(base + kSmallBytes);
+    s.accs = (float *)(base + kSmallBytes + own_bytes(P.m.max_batch, P.own_ld));
+    s.xs = (float *)(base + xs_offset(P.m.max_batch, P.own_ld, P.acc_bytes));
+    s.ring = base + ring_offset(P.m.max_batch, P.own_ld, P.acc_bytes, P.xs_bytes);
     return s;
 }
 
@@ -311,6 +302,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
 struct Chunk {
     const uint8_t *src;
     uint32_t bytes;
+    uint32_t rowbytes;
 };
 
 // ------------------------------------------------------------------ streaming warp
@@ -346,6 +338,7 @@ __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
             out.src = M.base + (long long)(c.phase == 4 ? 0 : c.layer) * M.layer_stride +
                       ((long long)c.kt * M.rows + (long long)c.u * M.rows_per_unit) * rowbytes;
             out.bytes = (uint32_t)((long long)nunits * M.rows_per_unit * rowbytes);
+            out.rowbytes = (uint32_t)rowbytes;
             c.u += nunits;
             return true;
         }
@@ -369,7 +362,9 @@ __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
     return false;
 }
 
-// Copies this CTA's chunks into the ring, in the order the compute warps use them.
+// Copies this CTA's chunks into the ring, in the order the compute warps use them; with
+// PAD, row by row at a stride of rowbytes + kRowPad.
+template <bool PAD>
 __device__ __forceinline__ void producer(const StepParams &P, Shared &S) {
     const uint32_t slots = (uint32_t)P.ring_slots;
     Cursor ic;
@@ -386,7 +381,13 @@ __device__ __forceinline__ void producer(const StepParams &P, Shared &S) {
             if (!wait_slot(P, &S.empty[slot], parity)) break;
         }
         mbar_expect_tx(&S.full[slot], c.bytes);
-        bulk_g2s(S.ring + (size_t)slot * kChunkBytes, c.src, c.bytes, &S.full[slot]);
+        if (PAD) {
+            for (uint32_t r = 0, n = c.bytes / c.rowbytes; r < n; r++)
+                bulk_g2s(S.ring + (size_t)slot * kChunkBytes + r * (c.rowbytes + kRowPad), c.src + (size_t)r * c.rowbytes,
+                         c.rowbytes, &S.full[slot]);
+        } else {
+            bulk_g2s(S.ring + (size_t)slot * kChunkBytes, c.src, c.bytes, &S.full[slot]);
+        }
         issued++;
     }
     // Never leave with a copy in flight: wait (bounded, ignoring the abort flag) for the
@@ -439,7 +440,7 @@ __device__ __forceinline__ void init_residual(const StepParams &P, Shared &S) {
     for (int b = 0; b < P.batch; b++) {
         int tok = token_of(P, b);
         for (int i = threadIdx.x; i < r1 - r0; i += kComputeThreads)
-            S.xown[b * kMaxOwn + i] = emb_elem(m, tok, r0 + i);
+            S.xown[b * P.own_ld + i] = emb_elem(m, tok, r0 + i);
     }
 }
 
@@ -910,7 +911,7 @@ __device__ __forceinline__ Cand group_compute(const StepParams &P, const Mat &M,
             if (kt != M.nkt - 1) return cd;
         }
         // Wo / W2: residual add on the owned row, publish the new residual
-        float *own = S.xown + c.b * kMaxOwn + c.own;
+        float *own = S.xown + c.b * P.own_ld + c.own;
         const float xn = *own + t;
         *own = xn;
         ll_store(c.dst, xn, tag);
@@ -1146,7 +1147,7 @@ __device__ __forceinline__ Cand mma_epilogue(const StepParams &P, int epi, int l
         *a = t;
         if (kt != M.nkt - 1) return cd;
     }
-    float *own = S.xown + b * kMaxOwn + i;
+    float *own = S.xown + b * P.own_ld + i;
     const float xn = *own + t;
     *own = xn;
     uint64_t *dstw = epi == EPI_WO ? m.ll_xa + ll_layer(P, layer, m.dim) : m.ll_x + ll_layer(P, layer + 1, m.dim);
@@ -1161,8 +1162,7 @@ __device__ __forceinline__ Cand mma_epilogue(const StepParams &P, int epi, int l
 // ring protocol as in layer_walk.  For the logits, lanes keep their best candidates.
 template <bool LOGITS>
 __device__ __forceinline__ uint32_t mma_walk(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
-                                             uint32_t chunk_i, int tslot, float (&best_v)[kMaxBatch],
-                                             int (&best_i)[kMaxBatch]) {
+                                             uint32_t chunk_i, int tslot, float (&best_v)[2], int (&best_i)[2]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g4 = lane >> 2, t4 = lane & 3;
     int u0, u1;
@@ -1174,7 +1174,7 @@ __device__ __forceinline__ uint32_t mma_walk(const StepParams &P, int epi, int l
     const int cpk = (u1 - u0 + cu - 1) / cu;
     const int nch = M.nkt * cpk;
     const uint32_t slots = (uint32_t)P.ring_slots;
-    const size_t rowbytes = (size_t)M.KBp * 2;
+    const size_t rowbytes = (size_t)M.KBp * 2 + kRowPad;  // ring row stride (padded)
     const int pld = M.KBp + 8;
     const uint16_t *hi = (const uint16_t *)S.xs, *lo = hi + kMaxBatch * pld;
     int j = (warp - (int)(chunk_i & 7)) & 7;
@@ -1225,13 +1225,23 @@ __device__ __forceinline__ uint32_t mma_walk(const StepParams &P, int epi, int l
                 if (rpu == 2) {
                     if (t4 < nunits) mma_epilogue(P, epi, layer, M, S, u0, unit0 + t4, b, v0, v1, kt);
                 } else {
+                    // a lane only ever holds batch rows g4 (h = 0) and g4 + 8 (h = 1): it keeps
+                    // one candidate for each
                     if (n0 < nr) {
                         const Cand cd = mma_epilogue(P, epi, layer, M, S, u0, unit0 + n0, b, v0, 0.f, kt);
-                        if constexpr (LOGITS) keep_best<kMaxBatch>(cd, best_v, best_i);
+                        if constexpr (LOGITS)
+                            if (cd.v > best_v[h] || (cd.v == best_v[h] && cd.i < best_i[h])) {
+                                best_v[h] = cd.v;
+                                best_i[h] = cd.i;
+                            }
                     }
                     if (n0 + 1 < nr) {
                         const Cand cd = mma_epilogue(P, epi, layer, M, S, u0, unit0 + n0 + 1, b, v1, 0.f, kt);
-                        if constexpr (LOGITS) keep_best<kMaxBatch>(cd, best_v, best_i);
+                        if constexpr (LOGITS)
+                            if (cd.v > best_v[h] || (cd.v == best_v[h] && cd.i < best_i[h])) {
+                                best_v[h] = cd.v;
+                                best_i[h] = cd.i;
+                            }
                     }
                 }
             }
@@ -1246,8 +1256,8 @@ template <int NB, bool WBF16, bool G8>
 __device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                             uint32_t chunk_i, int tslot) {
     if constexpr (NB == kMaxBatch && WBF16) {  // batch 16: tensor cores
-        float bv[kMaxBatch];
-        int bi[kMaxBatch];
+        float bv[2];
+        int bi[2];
         return mma_walk<false>(P, epi, layer, M, S, chunk_i, tslot, bv, bi);
     } else {
         return layer_walk<NB, WBF16, (NB == 1 && G8) ? 8 : 2>(P, epi, layer, M, S, chunk_i, tslot);
@@ -1261,6 +1271,33 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
     const Model &m = P.m;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int batch = P.batch;
+    if constexpr (NB == kMaxBatch && WBF16) {
+        // lane (g4, t4) holds candidates of batch rows g4 and g4 + 8: reduce over t4
+        float bv[2] = {-INFINITY, -INFINITY};
+        int bi[2] = {0x7fffffff, 0x7fffffff};
+        mma_walk<true>(P, EPI_LOGITS, 0, m.emb, S, chunk_i, tslot, bv, bi);
+        trace_mark(P, tslot + 1, 0);
+        compute_sync();  // the logits phase is done with S.xs
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float v = bv[h];
+            int i = bi[h];
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+                const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
+                if (v2 > v || (v2 == v && i2 < i)) {
+                    v = v2;
+                    i = i2;
+                }
+            }
+            const int b = (lane >> 2) + 8 * h;
+            if ((lane & 3) == 0 && b < batch) {
+                S.wbest_v[warp * kMaxBatch + b] = v;
+                S.wbest_i[warp * kMaxBatch + b] = i;
+            }
+        }
+    } else {
     float best_v[NB];
     int best_i[NB];
 #pragma unroll
@@ -1268,10 +1305,7 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
         best_v[b] = -INFINITY;
         best_i[b] = 0x7fffffff;
     }
-    if constexpr (NB == kMaxBatch && WBF16)
-        mma_walk<true>(P, EPI_LOGITS, 0, m.emb, S, chunk_i, tslot, best_v, best_i);
-    else
-        logits_walk<NB, WBF16, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
+    logits_walk<NB, WBF16, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
     trace_mark(P, tslot + 1, 0);
     compute_sync();  // the logits phase is done with S.xs
 #pragma unroll
@@ -1291,6 +1325,7 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
             S.wbest_v[warp * kMaxBatch + b] = v;
             S.wbest_i[warp * kMaxBatch + b] = i;
         }
+    }
     }
     compute_sync();
     if (tid < batch) {
@@ -1492,7 +1527,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
     __syncthreads();
     if (tid >= kComputeThreads) {
-        if (tid == kComputeThreads) producer(P, S);
+        if (tid == kComputeThreads) producer<NB == kMaxBatch && WBF16>(P, S);
         return;
     }
     const Model &m = P.m;
@@ -1519,14 +1554,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
 // ------------------------------------------------------------------ host-side launch
 
-size_t decode_smem_bytes(int xs_bytes, int ring_slots) {
-    return ring_offset(xs_bytes) + (size_t)ring_slots * kChunkBytes;
+size_t decode_smem_bytes(int max_batch, int own_ld, int acc_bytes, int xs_bytes, int ring_slots) {
+    return ring_offset(max_batch, own_ld, acc_bytes, xs_bytes) + (size_t)ring_slots * kChunkBytes;
 }
 
 template <int NB, bool WBF16, bool G8>
 static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
     auto fn = decode_step_kernel<NB, WBF16, G8>;
-    const size_t smem = decode_smem_bytes(P.xs_bytes, P.ring_slots);
+    const size_t smem = decode_smem_bytes(P.m.max_batch, P.own_ld, P.acc_bytes, P.xs_bytes, P.ring_slots);
     static size_t smem_set = 0;  // the attribute only grows; set it once per size (host latency per step)
     if (smem > smem_set) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -23,7 +23,7 @@
 namespace slm {
 cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream);
 cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm);
-size_t decode_smem_bytes(int xs_bytes, int ring_slots);
+size_t decode_smem_bytes(int max_batch, int own_ld, int acc_bytes, int xs_bytes, int ring_slots);
 }  // namespace slm
 
 using namespace slm;
@@ -34,6 +34,7 @@ struct slm_ctx {
     int grid = 0;
     size_t smem = 0;
     int ring_slots = 0, xs_bytes = 0, attn_stage = 0;
+    int own_ld = 0, acc_bytes = 0;  // decode kernel shared-memory layout (see ring_offset)
     Model m{};
     std::vector<void *> allocs;
     std::vector<int> len;
@@ -116,7 +117,7 @@ static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // CTA's share (of `ctas` CTAs) splits into about one chunk per warp or more, at most one
 // slot and at most 8 rows (one row group of the batch-1 kernel).
 static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int max_batch,
-                     bool allow_split, int ctas) {
+                     bool allow_split, int ctas, size_t budget) {
     for (int nkt = 1; nkt <= 64; nkt++) {
         int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), kPadElems);
         int real_nkt = (K + KB - 1) / KB;
@@ -124,7 +125,9 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
         // planes, padded by 8 elements
         size_t xs = max_batch > 8 ? (size_t)kMaxBatch * (KB + 8) * 4 : (size_t)max_batch * KB * 4;
         size_t unit_bytes = (size_t)KB * esz * rows_per_unit;
-        if (xs <= kXsBudget && unit_bytes <= (size_t)kChunkBytes) {
+        // (the batch-16 tensor-core kernel pads every bf16 row in the ring by kRowPad)
+        const size_t slot_unit = unit_bytes + (max_batch > 8 && esz == 2 ? (size_t)kRowPad * rows_per_unit : 0);
+        if (xs <= budget && slot_unit <= (size_t)kChunkBytes) {
             if (real_nkt > 1 && !allow_split) return false;
             M.rows = rows;
             M.K = K;
@@ -135,7 +138,7 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
             M.units = real_nkt * (rows / rows_per_unit);
             const int units = rows / rows_per_unit;
             const int per_cta = (units + ctas - 1) / ctas;
-            const int fit = std::min((int)(kChunkBytes / unit_bytes), 8 / rows_per_unit);
+            const int fit = std::min((int)(kChunkBytes / slot_unit), 8 / rows_per_unit);
             // batches: at least two single rows per chunk, so that a row group reuses
             // each activation load for two rows
             const int want = (per_cta + kComputeWarps - 1) / kComputeWarps;
@@ -318,14 +321,32 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     const int ctas_qkv = c->roles ? c->role0[1] - c->role0[0] : grid;
     const int ctas_res = c->roles ? c->role0[3] - c->role0[2] : grid;
     const int ctas_w13 = c->roles ? c->role0[4] - c->role0[3] : grid;
-    if (!plan_mat(m.emb, V, dim, 1, esz, B, false, grid) ||
-        !plan_mat(m.qkv, qkv_rows, dim, 2, esz, B, false, ctas_qkv) ||
-        !plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res) || !plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, ctas_w13) ||
-        !plan_mat(m.w2, dim, hid, 1, esz, B, true, ctas_res))
+    // Residual rows a CTA may own: with roles the residual CTAs' share; otherwise the
+    // share when up to a quarter of the CTAs are left to attention (res_cta0).
+    c->own_ld = c->roles ? (dim + ctas_res - 1) / ctas_res : (dim + (grid - grid / 4) - 1) / (grid - grid / 4);
+    if (c->own_ld > kMaxOwn) return fail(c, SLM_EUNSUPPORTED, "dim %d too large for %d CTAs", dim, grid);
+    // The activation tile takes what a 16-slot ring leaves; the norm inputs also keep a
+    // dim-long row beside it.  The residual matrices are planned first without K-tile
+    // accumulators, and again with them if either has to be split.
+    auto budget = [&](size_t acc) {
+        return kSmemLimit - (size_t)kMinRingSlots * kChunkBytes - xs_offset(B, c->own_ld, (int)acc);
+    };
+    c->acc_bytes = 0;
+    bool planned = plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res, budget(0)) &&
+                   plan_mat(m.w2, dim, hid, 1, esz, B, true, ctas_res, budget(0));
+    if (planned && (m.wo.nkt > 1 || m.w2.nkt > 1)) {
+        c->acc_bytes = (int)acc_bytes_for(c->own_ld);
+        planned = plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res, budget(c->acc_bytes)) &&
+                  plan_mat(m.w2, dim, hid, 1, esz, B, true, ctas_res, budget(c->acc_bytes));
+    }
+    const size_t bn = budget(c->acc_bytes) - (size_t)dim * 4;
+    planned = planned && plan_mat(m.emb, V, dim, 1, esz, B, false, grid, bn) &&
+              plan_mat(m.qkv, qkv_rows, dim, 2, esz, B, false, ctas_qkv, bn) &&
+              plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, ctas_w13, bn);
+    if (!planned)
         return fail(c, SLM_EUNSUPPORTED,
                     "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
     m.emb.layer_stride = 0;
-    if ((dim + grid - 1) / grid > kMaxOwn) return fail(c, SLM_EUNSUPPORTED, "dim %d too large for %d CTAs", dim, grid);
     {
         const int G = H / KV;
         size_t need = 0;
@@ -337,14 +358,14 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         need = std::max(need, (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) + (G + 2) * hd) * 4 +
                                   c->attn_stage);
         need = std::max(need, (size_t)B * grid * 2 * 4);  // argmax candidates
-        c->xs_bytes = (int)round_up(need, 1024);
-        const size_t base = decode_smem_bytes(c->xs_bytes, 0);
+        c->xs_bytes = (int)round_up(need, 128);
+        const size_t base = decode_smem_bytes(B, c->own_ld, c->acc_bytes, c->xs_bytes, 0);
         int slots = base < kSmemLimit ? (int)((kSmemLimit - base) / kChunkBytes) : 0;
         slots = std::min(kMaxRingSlots, slots / 8 * 8);
         if (slots < kMinRingSlots)
             return fail(c, SLM_EUNSUPPORTED, "shared memory too small: %zu B of scratch leaves %d ring slots", need, slots);
         c->ring_slots = slots;
-        c->smem = decode_smem_bytes(c->xs_bytes, slots);
+        c->smem = decode_smem_bytes(B, c->own_ld, c->acc_bytes, c->xs_bytes, slots);
     }
     int per_sm = 0;
     CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
@@ -581,7 +602,7 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
         // when they are few, the Wo / W2 rows go to the others so that nobody waits for
         // them twice.
         const int rest = c->grid - items;
-        P.res_cta0 = (items <= c->grid / 4 && rest > 0 && (m.dim + rest - 1) / rest <= kMaxOwn) ? items : 0;
+        P.res_cta0 = (items <= c->grid / 4 && rest > 0 && (m.dim + rest - 1) / rest <= c->own_ld) ? items : 0;
     }
 }
 
@@ -593,6 +614,8 @@ static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
     P.tag = c->launch_seq;
     P.trace = c->trace_on ? c->d_trace : nullptr;
     P.ring_slots = c->ring_slots;
+    P.own_ld = c->own_ld;
+    P.acc_bytes = c->acc_bytes;
     P.xs_bytes = c->xs_bytes;
     P.attn_stage_bytes = c->attn_stage;
     plan_attention(c, P);

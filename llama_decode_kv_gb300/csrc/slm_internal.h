@@ -25,11 +25,14 @@ constexpr int kRoleAttnCtas = 16;                     // attention CTAs when CTA
 constexpr int kRolesMaxBatch = 4;                     // roles only up to this batch ...
 constexpr double kRolesMaxLayerBytes = 16e6;          //   ... and these weight bytes per layer
 constexpr int kTensorPrefillMin = 16;                 // prompts this long use the GEMM prefill
-constexpr size_t kXsBudget = 88 * 1024;               // activation tile, at most (16-slot ring)
 constexpr size_t kSmemLimit = 227 * 1024;             // dynamic shared memory per CTA
 constexpr int kMaxOwn = 32;                           // residual rows one CTA may own
 constexpr int kPadElems = 64;                         // K tiles are padded to 64 elements
                                                       //   (one tensor-core K block)
+// The batch-16 tensor-core kernel reads a chunk's rows with ldmatrix, eight rows at one
+// K offset: its ring keeps rows kRowPad bytes further apart than memory does, so that
+// those eight 16-byte reads fall in different bank groups (row bytes are multiples of 128).
+constexpr int kRowPad = 16;
 
 // status word bits (device side)
 constexpr int kStExchangeTimeout = 1;
@@ -109,6 +112,8 @@ struct StepParams {
     uint32_t tag;                   // this launch's exchange tag (never 0)
     int grid;
     int ring_slots;                 // weight ring depth (multiple of 8)
+    int own_ld;                     // residual rows a CTA may own (xown row length)
+    int acc_bytes;                  // K-tile accumulators (0: no residual matrix is K-split)
     int xs_bytes;                   // activation tile / scratch region
     int attn_stage_bytes;           // K + V chunk copy budget within it
     unsigned long long *trace;      // null, or [grid][trace_slots][3] phase timestamps
@@ -119,6 +124,21 @@ struct StepParams {
 // attention, Wo, W1/W3, W2), then logits and argmax.
 constexpr int kTracePerLayer = 5;
 __host__ __device__ inline int trace_slots(int n_layers) { return kTracePerLayer * n_layers + 2; }
+
+// Dynamic shared memory of the decode kernel, in order: barriers and small arrays
+// (kSmallBytes), the residual rows the CTA owns ([max_batch][own_ld] floats), the K-tile
+// accumulators (acc_bytes), the activation tile / scratch (xs_bytes), the weight ring.
+constexpr int kSmallBytes = ((2 * kMaxRingSlots * 8 + 3 * kComputeWarps * kMaxBatch * 4 + 16 + 127) / 128) * 128;
+__host__ __device__ inline size_t own_bytes(int max_batch, int own_ld) {
+    return ((size_t)max_batch * own_ld * 4 + 127) / 128 * 128;
+}
+__host__ __device__ inline size_t acc_bytes_for(int own_ld) { return ((size_t)own_ld * kMaxBatch * 4 + 127) / 128 * 128; }
+__host__ __device__ inline size_t xs_offset(int max_batch, int own_ld, int acc_bytes) {
+    return kSmallBytes + own_bytes(max_batch, own_ld) + (size_t)acc_bytes;
+}
+__host__ __device__ inline size_t ring_offset(int max_batch, int own_ld, int acc_bytes, int xs_bytes) {
+    return (xs_offset(max_batch, own_ld, acc_bytes) + (size_t)xs_bytes + 1023) / 1024 * 1024;
+}
 
 // Record the error text of a failed call that has no context (slm_last_error(NULL)).
 void set_detached_error(const char *msg);
