@@ -170,36 +170,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
         }
         umma_commit(done);
     } else if (warp < 4) {
-        // epilogue: wait for the accumulator, then 16 columns at a time
+        // epilogue: wait for the accumulator, then 32 columns at a time.  The stage
+        // buffers are free once every MMA has completed: fp32 results go through a
+        // per-warp [32][33] shared tile so that each row leaves as one 128-byte run.
         gemm_wait(done, 0, g.status);
         __syncwarp();  // tcgen05.ld is warp-collective
         tc_fence_after();
-        const int row = m0 + warp * 32 + lane;
-        for (int c = 0; c < kBN; c += 16) {
-            uint32_t r[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
-            if (row >= g.M) continue;
+        const int row0 = m0 + warp * 32;
+        float *T = (float *)sa + warp * 32 * 33;
+        const bool vec = (g.ldo & 7) == 0;
+        for (int c = 0; c < kBN; c += 32) {
+            uint32_t r[32];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, *(uint32_t(*)[16])r);
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c + 16), *(uint32_t(*)[16])(r + 16));
             if (g.epi == GEMM_SWIGLU) {
+                // this lane's row: 16 outputs (gate / up pairs), bf16 hi and lo parts
+                const int row = row0 + lane;
+                if (row >= g.M) continue;
+                uint32_t hw[8], lw[8];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const int n = n0 + c + j;
-                    if (n + 1 >= g.N) continue;
-                    const float gt = __uint_as_float(r[j]), up = __uint_as_float(r[j + 1]);
+                for (int j = 0; j < 16; j++) {
+                    const float gt = __uint_as_float(r[2 * j]), up = __uint_as_float(r[2 * j + 1]);
                     const float h = gt / (1.0f + __expf(-gt)) * up;
                     const __nv_bfloat16 hb = __float2bfloat16_rn(h);
                     const __nv_bfloat16 lb = __float2bfloat16_rn(h - __bfloat162float(hb));
-                    g.out_bf16[(size_t)row * g.ldo + (n >> 1)] = *(const uint16_t *)&hb;
-                    if (g.out_bf16_lo) g.out_bf16_lo[(size_t)row * g.ldo + (n >> 1)] = *(const uint16_t *)&lb;
+                    const uint32_t hu = *(const uint16_t *)&hb, lu = *(const uint16_t *)&lb;
+                    hw[j >> 1] = (j & 1) ? (hw[j >> 1] | (hu << 16)) : hu;
+                    lw[j >> 1] = (j & 1) ? (lw[j >> 1] | (lu << 16)) : lu;
+                }
+                const int o0 = (n0 + c) >> 1;  // first output column
+                uint16_t *dh = g.out_bf16 + (size_t)row * g.ldo + o0;
+                uint16_t *dl = g.out_bf16_lo ? g.out_bf16_lo + (size_t)row * g.ldo + o0 : nullptr;
+                if (vec && n0 + c + 32 <= g.N) {
+                    ((uint4 *)dh)[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    ((uint4 *)dh)[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                    if (dl) {
+                        ((uint4 *)dl)[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        ((uint4 *)dl)[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+                    }
+                } else {
+                    for (int j = 0; j < 16 && n0 + c + 2 * j + 1 < g.N; j++) {
+                        dh[j] = (uint16_t)(hw[j >> 1] >> (16 * (j & 1)));
+                        if (dl) dl[j] = (uint16_t)(lw[j >> 1] >> (16 * (j & 1)));
+                    }
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const int n = n0 + c + j;
-                    if (n >= g.N) continue;
-                    float *o = g.out_f32 + (size_t)row * g.ldo + n;
-                    const float v = __uint_as_float(r[j]);
-                    *o = g.epi == GEMM_ADD_F32 ? *o + v : v;
+                for (int j = 0; j < 32; j++) T[lane * 33 + j] = __uint_as_float(r[j]);
+                __syncwarp();
+                const int n = n0 + c + lane;
+                for (int rr = 0; rr < 32; rr++) {
+                    const int row = row0 + rr;
+                    if (row >= g.M) break;
+                    if (n < g.N) {
+                        float *o = g.out_f32 + (size_t)row * g.ldo + n;
+                        const float v = T[rr * 33 + lane];
+                        *o = g.epi == GEMM_ADD_F32 ? *o + v : v;
+                    }
                 }
+                __syncwarp();
             }
         }
     }
