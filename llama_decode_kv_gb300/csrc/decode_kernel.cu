@@ -70,9 +70,9 @@ __device__ __forceinline__ Shared carve(uint8_t *base, const StepParams &P) {
     s.wbest_i = (int *)p;
     p += kComputeWarps * kMaxBatch * 4;
     s.flags = (int *)p;
-    s.xown = (float *)(base + kSmallBytes);
-    s.accs = (float *)(base + kSmallBytes + own_bytes(P.m.max_batch, P.own_ld));
-    s.xs = (float *)(base + xs_offset(P.m.max_batch, P.own_ld, P.acc_bytes));
+    s.xs = (float *)(base + kSmallBytes);
+    s.xown = (float *)(base + own_offset(P.xs_bytes));
+    s.accs = (float *)(base + own_offset(P.xs_bytes) + own_bytes(P.m.max_batch, P.own_ld));
     s.ring = base + ring_offset(P.m.max_batch, P.own_ld, P.acc_bytes, P.xs_bytes);
     return s;
 }

@@ -329,7 +329,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     // dim-long row beside it.  The residual matrices are planned first without K-tile
     // accumulators, and again with them if either has to be split.
     auto budget = [&](size_t acc) {
-        return kSmemLimit - (size_t)kMinRingSlots * kChunkBytes - xs_offset(B, c->own_ld, (int)acc);
+        return kSmemLimit - (size_t)kMinRingSlots * kChunkBytes - layout_overhead(B, c->own_ld, (int)acc);
     };
     c->acc_bytes = 0;
     bool planned = plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res, budget(0)) &&

@@ -126,18 +126,21 @@ constexpr int kTracePerLayer = 5;
 __host__ __device__ inline int trace_slots(int n_layers) { return kTracePerLayer * n_layers + 2; }
 
 // Dynamic shared memory of the decode kernel, in order: barriers and small arrays
-// (kSmallBytes), the residual rows the CTA owns ([max_batch][own_ld] floats), the K-tile
-// accumulators (acc_bytes), the activation tile / scratch (xs_bytes), the weight ring.
+// (kSmallBytes), the activation tile / scratch (xs_bytes; at a constant offset, so that
+// its addresses need no register), the residual rows the CTA owns ([max_batch][own_ld]
+// floats), the K-tile accumulators (acc_bytes), the weight ring.
 constexpr int kSmallBytes = ((2 * kMaxRingSlots * 8 + 3 * kComputeWarps * kMaxBatch * 4 + 16 + 127) / 128) * 128;
 __host__ __device__ inline size_t own_bytes(int max_batch, int own_ld) {
     return ((size_t)max_batch * own_ld * 4 + 127) / 128 * 128;
 }
 __host__ __device__ inline size_t acc_bytes_for(int own_ld) { return ((size_t)own_ld * kMaxBatch * 4 + 127) / 128 * 128; }
-__host__ __device__ inline size_t xs_offset(int max_batch, int own_ld, int acc_bytes) {
+__host__ __device__ inline size_t own_offset(int xs_bytes) { return kSmallBytes + ((size_t)xs_bytes + 127) / 128 * 128; }
+// Bytes before the activation tile plus what follows it up to the ring.
+__host__ __device__ inline size_t layout_overhead(int max_batch, int own_ld, int acc_bytes) {
     return kSmallBytes + own_bytes(max_batch, own_ld) + (size_t)acc_bytes;
 }
 __host__ __device__ inline size_t ring_offset(int max_batch, int own_ld, int acc_bytes, int xs_bytes) {
-    return (xs_offset(max_batch, own_ld, acc_bytes) + (size_t)xs_bytes + 1023) / 1024 * 1024;
+    return (own_offset(xs_bytes) + own_bytes(max_batch, own_ld) + (size_t)acc_bytes + 1023) / 1024 * 1024;
 }
 
 // Record the error text of a failed call that has no context (slm_last_error(NULL)).
