@@ -137,6 +137,22 @@ int slm_decode_step(slm_ctx *ctx, int32_t batch, const int32_t *seq_ids, const i
  */
 int slm_reset(slm_ctx *ctx, int32_t seq);
 
+/*
+ * slm_fork -- clone a sequence's cache ("Inside nanochat Part 4: Understanding
+ * Inference", Batch Prefilling via Cache Replication: a prompt is prefilled once at
+ * batch 1 and its cache copied to N rows, which then generate independently).
+ *   src: sequence slot in [0, max_batch) holding at least one position (else
+ *     SLM_ESTATE).
+ *   dst_seqs: host int32[n_dst], n_dst in [1, max_batch - 1]; distinct slots, none
+ *     equal to src (else SLM_EINVAL), each empty (else SLM_ESTATE, as the pages'
+ *     cache refuses to be filled when it is not empty).
+ *   Every layer's cached keys and values of positions [0, length of src) are copied
+ *   byte for byte into each destination, whose length becomes src's.  Nothing else
+ *   changes.  Asynchronous on `stream` (one kernel launch): later calls on the same
+ *   stream see the copies.  Errors: SLM_EINVAL, SLM_ESTATE, SLM_ECUDA.
+ */
+int slm_fork(slm_ctx *ctx, int32_t src, int32_t n_dst, const int32_t *dst_seqs, void *stream);
+
 /* slm_seq_len -- current length of a sequence (>= 0), or a negative SLM_E* code. */
 int32_t slm_seq_len(const slm_ctx *ctx, int32_t seq);
 

@@ -49,6 +49,7 @@ _SIGS = {
     "slm_decode_step": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P]),
     "slm_reset": (ctypes.c_int, [_P, _I32]),
     "slm_seq_len": (_I32, [_P, _I32]),
+    "slm_fork": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "slm_sync": (ctypes.c_int, [_P, _P]),
     "slm_destroy": (None, [_P]),
     "slm_last_error": (ctypes.c_char_p, [_P]),
@@ -174,6 +175,11 @@ class Engine:
 
     def reset(self, seq: int = -1):
         self._check(slm_reset(self.ctx, seq), "slm_reset")
+
+    def fork(self, src: int, dst_seqs: Sequence[int], stream=None) -> int:
+        """Clone sequence src's cache into the empty sequences dst_seqs (status code)."""
+        d = (ctypes.c_int32 * len(dst_seqs))(*dst_seqs)
+        return slm_fork(self.ctx, src, len(dst_seqs), d, _stream_ptr(stream))
 
     def seq_len(self, seq: int) -> int:
         return int(slm_seq_len(self.ctx, seq))

@@ -754,6 +754,32 @@ extern "C" int slm_reset(slm_ctx *c, int32_t seq) {
     return SLM_OK;
 }
 
+extern "C" int slm_fork(slm_ctx *c, int32_t src, int32_t n_dst, const int32_t *dst_seqs, void *stream) {
+    if (!c) return SLM_EINVAL;
+    if (!dst_seqs) return fail(c, SLM_EINVAL, "dst_seqs is NULL");
+    const int B = c->cfg.max_batch;
+    if (src < 0 || src >= B) return fail(c, SLM_EINVAL, "source sequence %d out of range", src);
+    if (n_dst < 1 || n_dst > B - 1 || n_dst > kMaxBatch)
+        return fail(c, SLM_EINVAL, "n_dst %d out of range [1, %d]", n_dst, B - 1);
+    if (c->len[src] < 1) return fail(c, SLM_ESTATE, "source sequence %d is empty", src);
+    ForkArgs a{};
+    a.src = src;
+    a.len = c->len[src];
+    for (int i = 0; i < n_dst; i++) {
+        const int d = dst_seqs[i];
+        if (d < 0 || d >= B) return fail(c, SLM_EINVAL, "destination sequence %d out of range", d);
+        if (d == src) return fail(c, SLM_EINVAL, "destination %d is the source", d);
+        for (int j = 0; j < i; j++)
+            if (dst_seqs[j] == d) return fail(c, SLM_EINVAL, "destination %d repeated", d);
+        if (c->len[d] != 0)
+            return fail(c, SLM_ESTATE, "destination sequence %d is not empty (%d positions)", d, c->len[d]);
+        a.dst[i] = d;
+    }
+    CK(c, fork_kv(c->m, a, n_dst, (cudaStream_t)stream));
+    for (int i = 0; i < n_dst; i++) c->len[a.dst[i]] = a.len;
+    return SLM_OK;
+}
+
 extern "C" int32_t slm_seq_len(const slm_ctx *c, int32_t seq) {
     if (!c || seq < 0 || seq >= c->cfg.max_batch) return SLM_EINVAL;
     return c->len[seq];

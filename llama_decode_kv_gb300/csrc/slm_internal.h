@@ -143,6 +143,14 @@ __host__ __device__ inline size_t ring_offset(int max_batch, int own_ld, int acc
     return (own_offset(xs_bytes) + own_bytes(max_batch, own_ld) + (size_t)acc_bytes + 1023) / 1024 * 1024;
 }
 
+// Cache replication (cache_ops.cu): positions [0, len) of sequence src into dst[0..n).
+struct ForkArgs {
+    int dst[kMaxBatch];
+    int src;
+    int len;
+};
+cudaError_t fork_kv(const Model &m, const ForkArgs &a, int n_dst, cudaStream_t stream);
+
 // Record the error text of a failed call that has no context (slm_last_error(NULL)).
 void set_detached_error(const char *msg);
 

@@ -195,3 +195,20 @@ def test_batch16_tensor_core_path(slm, name, batch):
     eng = _engine(slm, s, W)
     g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, steps, batch, rows)
     compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, rows, name)
+
+
+def test_batch16_tensor_core_k_split(slm):
+    # hidden 2048: at 16 padded rows W2's input does not fit the activation tile in one
+    # piece, so the tensor-core residual epilogue accumulates over K tiles
+    s = synth.TINY.replace(max_batch=16, max_seq=64, weight_dtype=synth.DTYPE_BF16, kv_dtype=synth.DTYPE_F32,
+                           dim=128, n_heads=4, n_kv_heads=2, head_dim=32, hidden=2048, vocab=300)
+    W = synth.make_weights(s, seed=17)
+    batch = 12
+    lens = [2 + (5 * r) % 23 for r in range(batch)]
+    prompts = [synth.make_prompt(s, r, lens[r]) for r in range(batch)]
+    steps = 3
+    rows = list(range(batch))
+    ref_ids, ref_logits = oracle_reference(s, prompts, steps, rows, seed=17)
+    eng = _engine(slm, s, W)
+    g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, steps, batch, rows)
+    compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, rows, "bf16_tc_ksplit")
