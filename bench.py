@@ -245,11 +245,31 @@ def batch16_measure(slm, torch, W, local: int, warmup: int = 3):
         raise RuntimeError(f"device status after the batch-16 run: {eng.last_error()}")
     eng.close()
     bytes_step = sum(synth.weight_bytes(s) + B * kv_bytes_read(s, c) for c in state["ctx"]) / n
+    # on-device sampling of the same batch: temperature 0.8, top-k 40, top-p 0.95 over
+    # seeded logits of the vocabulary's size, one uniform per row
+    g = torch.Generator(device=dev).manual_seed(1234)
+    lg = torch.randn((B, s.vocab), generator=g, device=dev) * 2.0
+    us = torch.rand((B,), generator=g, device=dev)
+    ids = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        slm.sample(lg, 0.8, 40, 0.95, us, ids)
+    reps = 50
+    a.record(stream)
+    for _ in range(reps):
+        rc = slm.sample(lg, 0.8, 40, 0.95, us, ids)
+    b.record(stream)
+    torch.cuda.synchronize()
+    if rc != 0:
+        raise RuntimeError("slm_sample failed")
+    samp_us = a.elapsed_time(b) / reps * 1e3
     return {"workload": "smol_b16: SmolLM2-135M shape, bf16 KV cache, 16 rows x 512-token prompt, greedy decode "
                         f"to context {s.max_seq}",
             "tokens_per_s": B * n / (ms / 1e3), "ms_per_step": ms / n, "steps": n, "warmup": warmup,
             "contexts": [min(state["ctx"]), max(state["ctx"])], "bytes_per_step": bytes_step,
-            "hbm_gbs": bytes_step / (ms / 1e3 / n) / 1e9}
+            "hbm_gbs": bytes_step / (ms / 1e3 / n) / 1e9,
+            "sampling": {"call": "slm_sample, 16 rows x 49152 logits, temperature 0.8, top-k 40, top-p 0.95",
+                         "us_per_call": samp_us,
+                         "logit_gbs": B * s.vocab * 4 / (samp_us / 1e6) / 1e9}}
 
 
 def cpu_baseline(shape, W, prompt, budget_s: float):

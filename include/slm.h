@@ -153,6 +153,27 @@ int slm_reset(slm_ctx *ctx, int32_t seq);
  */
 int slm_fork(slm_ctx *ctx, int32_t src, int32_t n_dst, const int32_t *dst_seqs, void *stream);
 
+/*
+ * slm_sample -- draw the next token of each row from its logits ("Inside nanochat
+ * Part 4: Understanding Inference", The Sampling Function; top-p as in kasahare's
+ * --top-p flag, applied after top-k).  Needs no context.
+ *   logits: device float[batch][ld], ld >= vocab (e.g. slm_decode_step's logits).
+ *   temperature: 0 = greedy (argmax, lowest index on ties); otherwise > 0 and finite.
+ *   top_k: 0 = the whole vocabulary, or 1..1024: the k largest logits (ties by lower
+ *     index), sorted largest first.
+ *   top_p: in (0, 1]; below 1 keeps the shortest prefix of the sorted top-k candidates
+ *     whose probability reaches top_p (then top_k must be >= 1).
+ *   uniforms: device float[batch] in [0, 1), the variate of each row's draw (the caller
+ *     owns the random stream): the token is the first candidate, in the order above
+ *     (index order without top-k), whose running sum of softmax(logit / temperature)
+ *     weights exceeds uniforms[row] times their total.
+ *   next_ids: device int32[batch].
+ *   Asynchronous on `stream` (one kernel launch).  Errors (text in slm_last_error(NULL)):
+ *   SLM_EINVAL (NULL or host pointers, sizes, parameters), SLM_ECUDA.
+ */
+int slm_sample(int32_t batch, int32_t vocab, const float *logits, int32_t ld, float temperature, int32_t top_k,
+               float top_p, const float *uniforms, int32_t *next_ids, void *stream);
+
 /* slm_seq_len -- current length of a sequence (>= 0), or a negative SLM_E* code. */
 int32_t slm_seq_len(const slm_ctx *ctx, int32_t seq);
 

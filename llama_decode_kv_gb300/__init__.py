@@ -50,6 +50,7 @@ _SIGS = {
     "slm_reset": (ctypes.c_int, [_P, _I32]),
     "slm_seq_len": (_I32, [_P, _I32]),
     "slm_fork": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
+    "slm_sample": (ctypes.c_int, [_I32, _I32, _P, _I32, ctypes.c_float, _I32, ctypes.c_float, _P, _P, _P]),
     "slm_sync": (ctypes.c_int, [_P, _P]),
     "slm_destroy": (None, [_P]),
     "slm_last_error": (ctypes.c_char_p, [_P]),
@@ -125,6 +126,14 @@ def attention_decode_noalloc(q, k_cache, v_cache, ctx_len, out, kv_dtype: int, s
     lens = (ctypes.c_int32 * B)(*[int(x) for x in ctx_len])
     return slm_attention_decode_noalloc(B, H, KV, hd, cap, kv_dtype, _ptr(q), _ptr(k_cache),
                                         _ptr(v_cache), lens, _ptr(out), _stream_ptr(stream))
+
+
+def sample(logits, temperature: float, top_k: int, top_p: float, uniforms, next_ids, stream=None) -> int:
+    """slm_sample on device tensors: logits [batch][ld] float32, uniforms [batch] float32,
+    next_ids [batch] int32.  Returns the status code."""
+    batch, ld = int(logits.shape[0]), int(logits.shape[1])
+    return slm_sample(batch, ld, _ptr(logits), ld, float(temperature), int(top_k), float(top_p), _ptr(uniforms),
+                      _ptr(next_ids), _stream_ptr(stream))
 
 
 class Engine:

@@ -754,6 +754,37 @@ extern "C" int slm_reset(slm_ctx *c, int32_t seq) {
     return SLM_OK;
 }
 
+static int sample_fail(int code, const char *msg) {
+    set_detached_error(msg);
+    return code;
+}
+
+extern "C" int slm_sample(int32_t batch, int32_t vocab, const float *logits, int32_t ld, float temperature,
+                          int32_t top_k, float top_p, const float *uniforms, int32_t *next_ids, void *stream) {
+    if (batch < 1 || vocab < 1 || ld < vocab) return sample_fail(SLM_EINVAL, "slm_sample: bad batch, vocab or ld");
+    if (!logits || !uniforms || !next_ids) return sample_fail(SLM_EINVAL, "slm_sample: NULL pointer");
+    if (!is_device_ptr(logits) || !is_device_ptr(uniforms) || !is_device_ptr(next_ids))
+        return sample_fail(SLM_EINVAL, "slm_sample: logits, uniforms and next_ids must be device memory");
+    if (!(temperature >= 0.0f) || !std::isfinite(temperature))
+        return sample_fail(SLM_EINVAL, "slm_sample: temperature must be finite and >= 0");
+    if (top_k < 0 || top_k > kMaxTopK) return sample_fail(SLM_EINVAL, "slm_sample: top_k must be in [0, 1024]");
+    if (!(top_p > 0.0f && top_p <= 1.0f)) return sample_fail(SLM_EINVAL, "slm_sample: top_p must be in (0, 1]");
+    if (top_p < 1.0f && top_k < 1 && temperature > 0.0f)
+        return sample_fail(SLM_EINVAL, "slm_sample: top_p < 1 needs top_k >= 1");
+    SampleArgs a;
+    a.logits = logits;
+    a.uniforms = uniforms;
+    a.next_ids = next_ids;
+    a.ld = ld;
+    a.vocab = vocab;
+    a.top_k = top_k;
+    a.temperature = temperature;
+    a.top_p = top_p;
+    cudaError_t e = sample_launch(a, batch, (cudaStream_t)stream);
+    if (e != cudaSuccess) return sample_fail(SLM_ECUDA, cudaGetErrorString(e));
+    return SLM_OK;
+}
+
 extern "C" int slm_fork(slm_ctx *c, int32_t src, int32_t n_dst, const int32_t *dst_seqs, void *stream) {
     if (!c) return SLM_EINVAL;
     if (!dst_seqs) return fail(c, SLM_EINVAL, "dst_seqs is NULL");

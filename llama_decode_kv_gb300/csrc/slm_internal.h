@@ -151,6 +151,17 @@ struct ForkArgs {
 };
 cudaError_t fork_kv(const Model &m, const ForkArgs &a, int n_dst, cudaStream_t stream);
 
+// Next-token sampling (sampling.cu), one CTA per row.
+constexpr int kMaxTopK = 1024;
+struct SampleArgs {
+    const float *logits;  // [batch][ld]
+    const float *uniforms;  // [batch], in [0, 1)
+    int *next_ids;        // [batch]
+    int ld, vocab, top_k;
+    float temperature, top_p;
+};
+cudaError_t sample_launch(const SampleArgs &a, int batch, cudaStream_t stream);
+
 // Record the error text of a failed call that has no context (slm_last_error(NULL)).
 void set_detached_error(const char *msg);
 
