@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         for (int i = tid; i < V; i += kSampleThreads) {
-            const float v = x[i];
+            const float v = __ldg(x + i);
             if (v > bv || (v == bv && i < bi)) {
                 bv = v;
                 bi = i;
@@ -115,8 +115,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         for (int d = 3; d >= 0; d--) {
             if (tid < 256) hist[tid] = 0;
             __syncthreads();
+#pragma unroll 4
             for (int i = tid; i < V; i += kSampleThreads) {
-                const uint32_t key = order_key(x[i]);
+                const uint32_t key = order_key(__ldg(x + i));
                 if ((key & mask) == prefix) atomicAdd(&hist[(key >> (8 * d)) & 255u], 1);
             }
             __syncthreads();
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         // gather: keys above T, then the `remaining` lowest indices whose key is T
         int ngt = 0, neq = 0;
         for (int i = lo; i < hi; i++) {
-            const uint32_t key = order_key(x[i]);
+            const uint32_t key = order_key(__ldg(x + i));
             ngt += key > T;
             neq += key == T;
         }
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         for (int i = tid; i < kMaxTopK; i += kSampleThreads) cand[i] = 0ull;  // below every real entry
         __syncthreads();
         for (int i = lo; i < hi; i++) {
-            const uint32_t key = order_key(x[i]);
+            const uint32_t key = order_key(__ldg(x + i));
             const unsigned long long c = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)i);
             if (key > T) {
                 cand[gt_off++] = c;
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
 
     // the whole vocabulary in index order
     float mx = -INFINITY;
-    for (int i = tid; i < V; i += kSampleThreads) mx = fmaxf(mx, x[i]);
+    for (int i = tid; i < V; i += kSampleThreads) mx = fmaxf(mx, __ldg(x + i));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (lane == 0) bestv[warp] = mx;
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
     for (int w = 1; w < 32; w++) mx = fmaxf(mx, bestv[w]);
     const float vmax = mx / a.temperature;
     float s = 0.0f;
-    for (int i = lo; i < hi; i++) s += expf(x[i] / a.temperature - vmax);
+    for (int i = lo; i < hi; i++) s += expf(__ldg(x + i) / a.temperature - vmax);
     const float incl = block_scan<float>(s, wsum_f);
     cum[tid] = incl;  // range t covers [cum[t - 1], cum[t]): the ranges partition [0, Z)
     if (tid == 0) sel[0] = V - 1;
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleArgs
         float run = pre;
         int pick = hi - 1;
         for (int i = lo; i < hi; i++) {
-            run += expf(x[i] / a.temperature - vmax);
+            run += expf(__ldg(x + i) / a.temperature - vmax);
             if (run > target) {
                 pick = i;
                 break;
