@@ -1,15 +1,16 @@
 // gemm_tc.cu -- bf16 x bf16 -> fp32 GEMM tile on the 5th-generation tensor cores.
 //
-// One CTA computes a 128 x 128 output tile.  The activation operand may come as two bf16
-// parts (hi + lo, ~16 mantissa bits together): each K step then issues two MMAs into the
-// same accumulator against the one weight tile.
-//   warp 4 (one lane)  : TMA producer, cp.async.bulk.tensor.2d of the A and B K-blocks
-//                        (128 rows x 64 bf16 = one 128-byte swizzle atom wide) into a
+// One CTA computes a 128 x BN output tile (BN = 128, or 64 when 128-wide tiles would not
+// fill the GPU once).  The activation operand may come as two bf16 parts (hi + lo, ~16
+// mantissa bits together): each K step then issues two MMAs into the same accumulator
+// against the one weight tile.
+//   warp 4 (one lane)  : TMA producer, cp.async.bulk.tensor of the A and B K-blocks
+//                        (rows x 64 bf16 = one 128-byte swizzle atom wide) into a
 //                        4-stage ring, completion on mbarriers;
-//   warp 5 (one lane)  : tcgen05.mma.cta_group::1.kind::f16 (M 128, N 128, K 16) issuer,
+//   warp 5 (one lane)  : tcgen05.mma.cta_group::1.kind::f16 (M 128, N BN, K 16) issuer,
 //                        accumulating in tensor memory; tcgen05.commit frees each stage
 //                        and finally signals the epilogue;
-//   warps 0-3          : allocate the 128 TMEM columns, then read the accumulator back
+//   warps 0-3          : allocate BN TMEM columns, then read the accumulator back
 //                        with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = tile rows)
 //                        and apply the fused epilogue.
 // Every wait is bounded; TMEM is always freed.
@@ -24,7 +25,8 @@
 
 namespace slm {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4;
+constexpr int kBM = 128, kBK = 64, kStages = 4;
+constexpr int kBRows = 64;  // rows of the narrow weight (B) box, for 64-column tiles
 constexpr int kTileBytes = kBM * kBK * 2;            // 16 KB per operand per stage
 constexpr int kGemmThreads = 192;
 constexpr int kGemmSmem = 1024 + kStages * 3 * kTileBytes + 256;
@@ -104,6 +106,7 @@ __device__ bool gemm_wait(uint64_t *bar, uint32_t parity, int *status) {
 
 // ------------------------------------------------------------------ the kernel
 
+template <int BN>  // output columns per CTA: 128, or 64 when 128-wide tiles would not fill the GPU
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);  // 1024-B aligned stages
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
     uint64_t *done = empty + kStages;
     uint32_t *tmem_slot = (uint32_t *)(done + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
     const int nk = g.K / kBK;
 
     if (threadIdx.x == 0) {
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
     }
     if (warp == 0) {  // 128 fp32 accumulator columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(kBN)
+                     "r"(BN)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -142,19 +145,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
         for (int kb = 0; kb < nk; kb++) {
             const int s = kb % kStages, u = kb / kStages;
             if (kb >= kStages && !gemm_wait(&empty[s], (u - 1) & 1, g.status)) break;
-            mbar_expect_tx(&full[s], (g.a_split ? 3 : 2) * kTileBytes);
+            mbar_expect_tx(&full[s], (g.a_split ? 2 : 1) * kTileBytes + BN * kBK * 2);
             tma_load_2d(sa + s * kTileBytes, &g.a_map, kb * kBK, m0, &full[s]);
             if (g.a_split) tma_load_2d(sl + s * kTileBytes, &g.a_lo_map, kb * kBK, m0, &full[s]);
+            // B: one box of BN rows (the wide map for 128-column tiles)
+            const CUtensorMap *bm = BN == 128 ? &g.b_map_wide : &g.b_map;
             if (g.b_tile_k > 0) {
                 const int k = kb * kBK, z = k / g.b_tile_k;
-                tma_load_3d(sb + s * kTileBytes, &g.b_map, k - z * g.b_tile_k, n0, z, &full[s]);
+                tma_load_3d(sb + s * kTileBytes, bm, k - z * g.b_tile_k, n0, z, &full[s]);
             } else {
-                tma_load_2d(sb + s * kTileBytes, &g.b_map, kb * kBK, n0, &full[s]);
+                tma_load_2d(sb + s * kTileBytes, bm, kb * kBK, n0, &full[s]);
             }
         }
     } else if (warp == 5 && lane == 0) {
         // MMA issuer: 4 K-steps of 16 per stage; the descriptor advances 32 bytes per step
-        const uint32_t idesc = idesc_bf16(kBM, kBN);
+        const uint32_t idesc = idesc_bf16(kBM, BN);
         for (int kb = 0; kb < nk; kb++) {
             const int s = kb % kStages, u = kb / kStages;
             if (!gemm_wait(&full[s], u & 1, g.status)) break;
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
         const int row0 = m0 + warp * 32;
         float *T = (float *)sa + warp * 32 * 33;
         const bool vec = (g.ldo & 7) == 0;
-        for (int c = 0; c < kBN; c += 32) {
+        for (int c = 0; c < BN; c += 32) {
             uint32_t r[32];
             tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, *(uint32_t(*)[16])r);
             tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c + 16), *(uint32_t(*)[16])(r + 16));
@@ -219,15 +224,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
                 for (int j = 0; j < 32; j++) T[lane * 33 + j] = __uint_as_float(r[j]);
                 __syncwarp();
                 const int n = n0 + c + lane;
-                for (int rr = 0; rr < 32; rr++) {
-                    const int row = row0 + rr;
-                    if (row >= g.M) break;
-                    if (n < g.N) {
-                        float *o = g.out_f32 + (size_t)row * g.ldo + n;
-                        const float v = T[rr * 33 + lane];
-                        *o = g.epi == GEMM_ADD_F32 ? *o + v : v;
-                    }
-                }
+                const int nrows = min(32, g.M - row0);
+                float *o = g.out_f32 + (size_t)row0 * g.ldo + n;
+                float old[32];  // the residual rows, all loads in flight before the first add
+#pragma unroll
+                for (int rr = 0; rr < 32; rr++)
+                    old[rr] = (g.epi == GEMM_ADD_F32 && rr < nrows && n < g.N) ? o[(size_t)rr * g.ldo] : 0.0f;
+#pragma unroll
+                for (int rr = 0; rr < 32; rr++)
+                    if (rr < nrows && n < g.N) o[(size_t)rr * g.ldo] = old[rr] + T[rr * 33 + lane];
                 __syncwarp();
             }
         }
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
     }
 }
 
@@ -259,13 +264,13 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld) {
+cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     if (((uintptr_t)base & 15) || ((size_t)ld * 2) % 16) return cudaErrorInvalidValue;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -273,13 +278,13 @@ cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_bf16_tiled_map(CUtensorMap *map, const void *base, int tiles, int rows, int tile_k) {
+cudaError_t make_bf16_tiled_map(CUtensorMap *map, const void *base, int tiles, int rows, int tile_k, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     if (((uintptr_t)base & 15) || tile_k % kBK) return cudaErrorInvalidValue;
     cuuint64_t dims[3] = {(cuuint64_t)tile_k, (cuuint64_t)rows, (cuuint64_t)tiles};
     cuuint64_t strides[2] = {(cuuint64_t)tile_k * 2, (cuuint64_t)rows * tile_k * 2};
-    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)kBM, 1};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -291,12 +296,20 @@ cudaError_t gemm_bf16_tn(const GemmArgs &args, cudaStream_t stream) {
     if (args.K <= 0 || args.K % kBK || args.M <= 0 || args.N <= 0) return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_bf16_tn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_bf16_tn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((args.N + kBN - 1) / kBN, (args.M + kBM - 1) / kBM);
-    gemm_bf16_tn_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(args);
+    // 128-column tiles when they fill the GPU at least once, else 64-column tiles (twice
+    // the CTAs, each with half the MMA and B traffic)
+    const int mt = (args.M + kBM - 1) / kBM;
+    if ((long long)mt * ((args.N + 127) / 128) >= 148) {
+        gemm_bf16_tn_kernel<128><<<dim3((args.N + 127) / 128, mt), kGemmThreads, kGemmSmem, stream>>>(args);
+    } else {
+        gemm_bf16_tn_kernel<64><<<dim3((args.N + 63) / 64, mt), kGemmThreads, kGemmSmem, stream>>>(args);
+    }
     return cudaGetLastError();
 }
 
@@ -317,7 +330,9 @@ extern "C" int slm_debug_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *
     GemmArgs g{};
     g.b_tile_k = 0;
     g.a_split = 0;
-    if (make_bf16_map(&g.a_map, A, M, K, K) != cudaSuccess || make_bf16_map(&g.b_map, B, N, K, K) != cudaSuccess) {
+    if (make_bf16_map(&g.a_map, A, M, K, K, kBM) != cudaSuccess ||
+        make_bf16_map(&g.b_map, B, N, K, K, kBRows) != cudaSuccess ||
+        make_bf16_map(&g.b_map_wide, B, N, K, K, kBM) != cudaSuccess) {
         set_detached_error("slm_debug_gemm_bf16: tensor map encoding failed (alignment?)");
         return SLM_EINVAL;
     }

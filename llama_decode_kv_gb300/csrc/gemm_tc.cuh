@@ -21,7 +21,8 @@ struct GemmArgs {
     CUtensorMap a_map;   // A [M][K] bf16, box 128 x 64 (the high part when a_split)
     CUtensorMap a_lo_map;  // with a_split: the low part, A = hi + lo to ~16 mantissa bits
     int a_split;
-    CUtensorMap b_map;   // B [N][K] bf16, box 128 x 64; 3-D [tiles][N][b_tile_k] when b_tile_k > 0
+    CUtensorMap b_map;   // B [N][K] bf16, box 64 rows x 64; 3-D [tiles][N][b_tile_k] when b_tile_k > 0
+    CUtensorMap b_map_wide;  // the same with boxes of 128 rows (128-column tiles load once)
     int b_tile_k;        // 0, or the K extent of each K tile of a K-tiled B (a multiple of 64)
     int M, N, K;
     int epi;
@@ -33,12 +34,13 @@ struct GemmArgs {
 };
 
 // Tensor map of a row-major [rows][cols] bf16 matrix (row stride ld elements, ld * 2 a
-// multiple of 16 bytes, base 16-byte aligned), 128 x 64 boxes, 128-byte swizzle.
-cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld);
+// multiple of 16 bytes, base 16-byte aligned), boxes of box_rows rows x 64 columns (128
+// for activations, 64 for weights), 128-byte swizzle.
+cudaError_t make_bf16_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, int box_rows = 128);
 
 // Tensor map of a K-tiled bf16 matrix [tiles][rows][tile_k] (tile_k a multiple of 64),
-// 64 x 128 x 1 boxes, 128-byte swizzle.
-cudaError_t make_bf16_tiled_map(CUtensorMap *map, const void *base, int tiles, int rows, int tile_k);
+// boxes of 64 columns x box_rows rows x 1, 128-byte swizzle.
+cudaError_t make_bf16_tiled_map(CUtensorMap *map, const void *base, int tiles, int rows, int tile_k, int box_rows);
 
 // Enqueue C = A . B^T with the given epilogue.  K must be a multiple of 64.
 cudaError_t gemm_bf16_tn(const GemmArgs &args, cudaStream_t stream);

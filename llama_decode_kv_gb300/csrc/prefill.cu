@@ -359,8 +359,11 @@ bool prefill_supported(const Model &m) {
            m.hidden % 8 == 0 && (m.head_dim == 64 || m.head_dim == 128) && (size_t)m.qkv.rows * 4 <= 48 * 1024;
 }
 
+// Two maps per weight matrix: boxes of 64 rows (64-column tiles) and of 128 rows.
 static cudaError_t weight_map(CUtensorMap *map, const Mat &M, int layer) {
-    return make_bf16_tiled_map(map, M.base + (long long)layer * M.layer_stride, M.nkt, M.rows, M.KBp);
+    cudaError_t e = make_bf16_tiled_map(map, M.base + (long long)layer * M.layer_stride, M.nkt, M.rows, M.KBp, 64);
+    if (e != cudaSuccess) return e;
+    return make_bf16_tiled_map(map + 1, M.base + (long long)layer * M.layer_stride, M.nkt, M.rows, M.KBp, 128);
 }
 
 cudaError_t prefill_prepare(const Model &m, PrefillPlan &p, int rows) {
@@ -373,15 +376,15 @@ cudaError_t prefill_prepare(const Model &m, PrefillPlan &p, int rows) {
                                      (int)attn_tc_smem<128>());
         if (e != cudaSuccess) return e;
     }
-    p.maps.resize((size_t)4 * m.n_layers + 1);
+    p.maps.resize(2 * ((size_t)4 * m.n_layers + 1));
     for (int l = 0; l < m.n_layers; l++) {
         cudaError_t e;
-        if ((e = weight_map(&p.maps[4 * l + 0], m.qkv, l)) != cudaSuccess) return e;
-        if ((e = weight_map(&p.maps[4 * l + 1], m.wo, l)) != cudaSuccess) return e;
-        if ((e = weight_map(&p.maps[4 * l + 2], m.w13, l)) != cudaSuccess) return e;
-        if ((e = weight_map(&p.maps[4 * l + 3], m.w2, l)) != cudaSuccess) return e;
+        if ((e = weight_map(&p.maps[2 * (4 * l + 0)], m.qkv, l)) != cudaSuccess) return e;
+        if ((e = weight_map(&p.maps[2 * (4 * l + 1)], m.wo, l)) != cudaSuccess) return e;
+        if ((e = weight_map(&p.maps[2 * (4 * l + 2)], m.w13, l)) != cudaSuccess) return e;
+        if ((e = weight_map(&p.maps[2 * (4 * l + 3)], m.w2, l)) != cudaSuccess) return e;
     }
-    cudaError_t e = weight_map(&p.maps[4 * m.n_layers], m.emb, 0);
+    cudaError_t e = weight_map(&p.maps[2 * (4 * m.n_layers)], m.emb, 0);
     if (e != cudaSuccess) return e;
     const int qd = m.n_heads * m.head_dim;
     if ((e = make_bf16_map(&p.xn_map, p.xn, rows, m.dim, m.dim)) != cudaSuccess) return e;
@@ -394,13 +397,14 @@ cudaError_t prefill_prepare(const Model &m, PrefillPlan &p, int rows) {
     return cudaSuccess;
 }
 
-static cudaError_t gemm(const CUtensorMap &a, const CUtensorMap &a_lo, const CUtensorMap &b, const Mat &M, int rows,
+static cudaError_t gemm(const CUtensorMap &a, const CUtensorMap &a_lo, const CUtensorMap *b, const Mat &M, int rows,
                         int epi, float *of, uint16_t *ob, uint16_t *ob_lo, int ldo, int *status, cudaStream_t s) {
     GemmArgs g{};
     g.a_map = a;
     g.a_lo_map = a_lo;
     g.a_split = 1;
-    g.b_map = b;
+    g.b_map = b[0];
+    g.b_map_wide = b[1];
     g.out_bf16_lo = ob_lo;
     g.b_tile_k = M.KBp;
     g.M = rows;
@@ -430,7 +434,7 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
         for (int l = 0; l < m.n_layers; l++) {
             const float *gn = m.norms + (size_t)l * 2 * m.dim;
             rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(p.x, gn, p.xn, xlo, m.dim, m.norm_eps);
-            PF_CK(gemm(p.xn_map, p.xn_lo_map, p.maps[4 * l + 0], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
+            PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 0)], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
                        m.qkv.rows, m.status, s));
             rope_append_kernel<true><<<T, 256, (size_t)m.qkv.rows * 4, s>>>(m, p.qkv, l, seq, p0);
             dim3 ag((T + 63) / 64, m.n_heads);
@@ -439,19 +443,19 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
             else
                 attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
             PF_CK(cudaGetLastError());
-            PF_CK(gemm(p.o_map, p.o_lo_map, p.maps[4 * l + 1], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
+            PF_CK(gemm(p.o_map, p.o_lo_map, &p.maps[2 * (4 * l + 1)], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
             rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(p.x, gn + m.dim, p.xn, xlo, m.dim, m.norm_eps);
-            PF_CK(gemm(p.xn_map, p.xn_lo_map, p.maps[4 * l + 2], m.w13, T, GEMM_SWIGLU, nullptr, p.h, p.h + hlo,
+            PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 2)], m.w13, T, GEMM_SWIGLU, nullptr, p.h, p.h + hlo,
                        m.hidden, m.status, s));
-            PF_CK(gemm(p.h_map, p.h_lo_map, p.maps[4 * l + 3], m.w2, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
+            PF_CK(gemm(p.h_map, p.h_lo_map, &p.maps[2 * (4 * l + 3)], m.w2, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
         }
         if (p0 + T == n) {  // logits of the last position (its normalised row goes to xn row 0)
             rmsnorm_bf16_kernel<<<1, 256, 0, s>>>(p.x + (size_t)(T - 1) * m.dim, m.norms + (size_t)m.n_layers * 2 * m.dim,
                                                   p.xn, xlo, m.dim, m.norm_eps);
             float *lg = last_logits ? last_logits : p.logits;
-            PF_CK(gemm(p.xn_map, p.xn_lo_map, p.maps[4 * m.n_layers], m.emb, 1, GEMM_STORE_F32, lg, nullptr, nullptr,
+            PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * m.n_layers)], m.emb, 1, GEMM_STORE_F32, lg, nullptr, nullptr,
                        m.vocab, m.status, s));
             argmax_kernel<<<1, 1024, 0, s>>>(lg, m.vocab, next_id, m.status);
             PF_CK(cudaGetLastError());

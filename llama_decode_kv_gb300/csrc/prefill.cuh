@@ -23,7 +23,7 @@ struct PrefillPlan {
     uint16_t *o = nullptr;     // [2][rows][H hd] attention output (hi, lo)
     uint16_t *h = nullptr;     // [2][rows][hidden] SwiGLU output (hi, lo)
     float *logits = nullptr;   // [vocab] when the caller wants no logits
-    std::vector<CUtensorMap> maps;  // per layer: qkv, wo, w13, w2; then the embedding
+    std::vector<CUtensorMap> maps;  // per layer: qkv, wo, w13, w2; then the embedding (each: 64-, 128-row boxes)
     CUtensorMap xn_map, o_map, h_map, xn_lo_map, o_lo_map, h_lo_map;
 };
 
