@@ -212,3 +212,46 @@ def test_batch16_tensor_core_k_split(slm):
     eng = _engine(slm, s, W)
     g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, steps, batch, rows)
     compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, rows, "bf16_tc_ksplit")
+
+
+def test_one_engine_serves_every_batch_size(slm):
+    # a max_batch 16 engine: steps of 1, 5 and 16 rows run the 1-, 8- and 16-row kernels
+    # (CUDA-core and tensor-core GEMVs) over the same weight layout and caches
+    s = synth.TINY.replace(max_batch=16, max_seq=64, weight_dtype=synth.DTYPE_BF16, kv_dtype=synth.DTYPE_BF16,
+                           dim=128, n_heads=4, n_kv_heads=2, head_dim=32, hidden=256, vocab=300)
+    W = synth.make_weights(s, seed=23)
+    rows = list(range(16))
+    lens = [4 + (3 * r) % 17 for r in rows]
+    prompts = [synth.make_prompt(s, r, lens[r]) for r in rows]
+    steps = 3
+    ref_ids, ref_logits = oracle_reference(s, prompts, 3 * steps, rows, seed=23)
+    eng = _engine(slm, s, W)
+    dev = torch.device("cuda")
+    g_logits = {r: [] for r in rows}
+    g_ids = {r: [] for r in rows}
+    cur = {}
+    for r in rows:
+        lg, nid = eng.prefill_checked(r, prompts[r], want_logits=True)
+        g_logits[r].append(lg.cpu().numpy())
+        g_ids[r].append(int(nid.item()))
+        cur[r] = ref_ids[r][0]
+    done = {r: 0 for r in rows}
+    # every row takes 3 * steps decode steps, in batches of 1, 5 and 16 rows in turn
+    k = 0
+    while any(done[r] < 3 * steps for r in rows):
+        width = (1, 5, 16)[k % 3]
+        k += 1
+        seqs = sorted((r for r in rows if done[r] < 3 * steps), key=lambda r: (done[r], r))[:width]
+        toks = torch.tensor([cur[r] for r in seqs], dtype=torch.int32, device=dev)
+        lg, nid = eng.decode_checked(seqs, toks, [lens[r] + done[r] for r in seqs], want_logits=True)
+        lg, nid = lg.cpu().numpy(), nid.cpu().numpy()
+        for i, r in enumerate(seqs):
+            done[r] += 1
+            g_logits[r].append(lg[i])
+            g_ids[r].append(int(nid[i]))
+            if done[r] < 3 * steps:
+                cur[r] = ref_ids[r][done[r]]
+    assert all(v == 3 * steps for v in done.values())
+    assert eng.sync() == 0, eng.last_error()
+    compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, rows, "mixed batch sizes")
+    eng.close()
