@@ -1372,6 +1372,13 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
                 if (P.next_ids) P.next_ids[b] = bi;
             }
         }
+        if (P.done_word) {  // host-memory ids: tell the host they are complete
+            compute_sync();
+            if (tid == 0) {
+                __threadfence_system();
+                *(volatile uint32_t *)P.done_word = P.tag;
+            }
+        }
     }
     trace_mark(P, tslot + 1, 2);
 }

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -49,7 +51,7 @@ struct slm_ctx {
     float *d_logits = nullptr;   // staging for host-requested logits [max_batch][vocab]
     int *d_ids = nullptr;        // staging for host-requested ids [max_batch]
     int *h_ids = nullptr;        // pinned
-    int *h_step = nullptr;       // mapped pinned [2][kMaxBatch]: host tokens, then ids, of a step
+    int *h_step = nullptr;       // mapped pinned [2][kMaxBatch] + 1: host tokens, ids, the done word
     int *d_step = nullptr;       //   its device address (the kernel reads / writes it directly)
     std::string err;
 };
@@ -498,7 +500,8 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         CK(c, cudaMemset(*b.dst, 0, b.bytes));
     }
     CK(c, cudaMallocHost((void **)&c->h_ids, (size_t)B * 4));
-    CK(c, cudaHostAlloc((void **)&c->h_step, (size_t)2 * kMaxBatch * 4, cudaHostAllocMapped));
+    CK(c, cudaHostAlloc((void **)&c->h_step, (size_t)(2 * kMaxBatch + 1) * 4, cudaHostAllocMapped));
+    c->h_step[2 * kMaxBatch] = 0;
     CK(c, cudaHostGetDevicePointer((void **)&c->d_step, c->h_step, 0));
     // tensor-core prefill buffers (blocks of up to 2048 prompt positions)
     if (prefill_supported(m)) {
@@ -668,12 +671,26 @@ extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids
     }
     P.logits = logits ? (log_dev ? logits : c->d_logits) : nullptr;
     P.next_ids = ids_dev ? next_ids : c->d_step + kMaxBatch;  // host ids: written straight to mapped memory
+    // host ids with device (or no) logits: the last CTA stamps a done word after the ids,
+    // and the host waits for it instead of for the whole launch to retire
+    const bool spin = !ids_dev && log_dev;
+    P.done_word = spin ? (uint32_t *)(c->d_step + 2 * kMaxBatch) : nullptr;
     P.do_logits = 1;
     int rc = launch(c, P, s);
     if (rc) return rc;
     for (int i = 0; i < batch; i++) c->len[P.seq[i]] = P.pos[i] + 1;
     if (!log_dev) CK(c, cudaMemcpyAsync(logits, c->d_logits, (size_t)batch * c->cfg.vocab * 4, cudaMemcpyDeviceToHost, s));
-    if (!tok_dev || !log_dev || !ids_dev) {
+    if (spin) {
+        const volatile uint32_t *done = (const volatile uint32_t *)(c->h_step + 2 * kMaxBatch);
+        const auto t0 = std::chrono::steady_clock::now();
+        bool seen = false;
+        while (!(seen = (*done == P.tag))) {  // bounded: an aborted step falls back to the stream
+            if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(3)) break;
+        }
+        std::atomic_thread_fence(std::memory_order_acquire);
+        if (!seen) CK(c, cudaStreamSynchronize(s));
+        memcpy(next_ids, c->h_step + kMaxBatch, (size_t)batch * 4);
+    } else if (!tok_dev || !log_dev || !ids_dev) {
         CK(c, cudaStreamSynchronize(s));
         if (!ids_dev) memcpy(next_ids, c->h_step + kMaxBatch, (size_t)batch * 4);
     }

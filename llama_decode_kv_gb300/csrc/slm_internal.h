@@ -108,6 +108,7 @@ struct StepParams {
     const int *tokens;              // device [batch]
     float *logits;                  // device [batch][vocab] or null
     int *next_ids;                  // device [batch] or null
+    uint32_t *done_word;            // null, or mapped host word set to `tag` once next_ids are written
     int do_logits;                  // 0: skip the vocabulary projection (prefill)
     uint32_t tag;                   // this launch's exchange tag (never 0)
     int grid;
