@@ -114,6 +114,22 @@ int slm_prefill(slm_ctx *ctx, int32_t seq, const int32_t *tokens, int32_t n, flo
                 int32_t *next_id, void *stream);
 
 /*
+ * slm_prefill_batch -- slm_prefill for several empty sequences in one call (the batched
+ * workloads prefill B prompts before decoding them together).  The prompts' linear
+ * layers run as GEMMs over all their positions at once; attention stays per sequence.
+ *   seqs: host int32[nseq], distinct empty slots (else SLM_EINVAL / SLM_ESTATE);
+ *     nseq in [1, max_batch].
+ *   lens: host int32[nseq], each in [1, max_seq] (else SLM_EINVAL / SLM_ECAPACITY).
+ *   tokens: device int32[sum of lens], the prompts concatenated in seqs order; ids out
+ *     of range are recorded in the device status word (slm_sync).
+ *   last_logits: NULL or device float[nseq][vocab]; next_ids: device int32[nseq].
+ *   Results equal nseq slm_prefill calls.  Asynchronous on `stream`; every pointer other
+ *   than seqs and lens must be device memory (else SLM_EINVAL).
+ */
+int slm_prefill_batch(slm_ctx *ctx, int32_t nseq, const int32_t *seqs, const int32_t *lens, const int32_t *tokens,
+                      float *last_logits, int32_t *next_ids, void *stream);
+
+/*
  * slm_decode_step -- one batched greedy decode step (nanochat "Engine.generate":
  * one token column for the whole batch per forward).
  *   batch in [1, max_batch].

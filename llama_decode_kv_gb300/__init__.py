@@ -50,6 +50,7 @@ _SIGS = {
     "slm_reset": (ctypes.c_int, [_P, _I32]),
     "slm_seq_len": (_I32, [_P, _I32]),
     "slm_fork": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
+    "slm_prefill_batch": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P]),
     "slm_sample": (ctypes.c_int, [_I32, _I32, _P, _I32, ctypes.c_float, _I32, ctypes.c_float, _P, _P, _P]),
     "slm_sync": (ctypes.c_int, [_P, _P]),
     "slm_destroy": (None, [_P]),
@@ -184,6 +185,15 @@ class Engine:
 
     def reset(self, seq: int = -1):
         self._check(slm_reset(self.ctx, seq), "slm_reset")
+
+    def prefill_batch(self, seqs: Sequence[int], tokens, lens: Sequence[int], last_logits=None, next_ids=None,
+                      stream=None) -> int:
+        """slm_prefill_batch: tokens = device int32 prompts concatenated in seqs order."""
+        n = len(seqs)
+        sq = (ctypes.c_int32 * n)(*seqs)
+        ln = (ctypes.c_int32 * n)(*[int(x) for x in lens])
+        return slm_prefill_batch(self.ctx, n, sq, ln, _ptr(tokens), _ptr(last_logits), _ptr(next_ids),
+                                 _stream_ptr(stream))
 
     def fork(self, src: int, dst_seqs: Sequence[int], stream=None) -> int:
         """Clone sequence src's cache into the empty sequences dst_seqs (status code)."""

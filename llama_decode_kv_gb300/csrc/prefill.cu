@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "gemm_tc.cuh"
 #include "prefill.cuh"
@@ -82,9 +84,12 @@ __global__ void rmsnorm_bf16_kernel(const float *x, const float *g, uint16_t *ou
 // in RoPE pairs (column 2i = dim i, column 2i + 1 = dim i + hd/2, the weights' stored
 // order).  The row is read into shared memory first and written back in natural order.
 template <bool KVBF16>
-__global__ void rope_append_kernel(const Model m, float *qkv, int layer, int seq, int p0) {
+__global__ void rope_append_kernel(const Model m, float *qkv, int layer, const PfSegs sg) {
     extern __shared__ float rowbuf[];  // [qkv.rows]
-    const int t = blockIdx.x, pos = p0 + t;
+    const int t = blockIdx.x;  // row of the block; its segment gives the sequence and position
+    int k = 0;
+    while (k + 1 < sg.n && t >= sg.row[k + 1]) k++;
+    const int seq = sg.seq[k], pos = sg.pos0[k] + (t - sg.row[k]);
     const int hd = m.head_dim, half = hd / 2, KV = m.n_kv_heads, G = m.n_heads / KV;
     const float *rope = m.rope + (size_t)pos * half * 2;
     float *row = qkv + (size_t)t * m.qkv.rows;
@@ -160,9 +165,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // pre-multiplied by log2(e) / sqrt(HD)), causal mask on the blocks that reach the rows'
 // own positions.  Q and P enter the MMAs as bf16.
 template <int HD>
-__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, const float *qkv, uint16_t *out,
-                                                              size_t lo_off, int layer, int seq, int p0, int T) {
+__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, const float *qkv_blk, uint16_t *out_blk,
+                                                              size_t lo_off, int layer, const PfSegs sg) {
     constexpr int QB = 64, KB = 64, LD = HD + 8;  // rows per CTA, keys per block, padded row (elements)
+    // segment blockIdx.z of the block: its rows, sequence and first position
+    const int sgi = blockIdx.z, seq = sg.seq[sgi], p0 = sg.pos0[sgi], T = sg.count[sgi];
+    if ((int)blockIdx.x * QB >= T) return;
+    const float *qkv = qkv_blk + (size_t)sg.row[sgi] * m.qkv.rows;
+    uint16_t *out = out_blk + (size_t)sg.row[sgi] * m.n_heads * HD;
     extern __shared__ __align__(16) uint16_t sm[];
     uint16_t *qs = sm;                  // [QB][LD]
     uint16_t *ks = qs + QB * LD;        // [KB][LD]
@@ -436,12 +446,18 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
             rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(p.x, gn, p.xn, xlo, m.dim, m.norm_eps);
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 0)], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
                        m.qkv.rows, m.status, s));
-            rope_append_kernel<true><<<T, 256, (size_t)m.qkv.rows * 4, s>>>(m, p.qkv, l, seq, p0);
-            dim3 ag((T + 63) / 64, m.n_heads);
+            PfSegs one{};
+            one.n = 1;
+            one.seq[0] = seq;
+            one.pos0[0] = p0;
+            one.count[0] = T;
+            one.row[0] = 0;
+            rope_append_kernel<true><<<T, 256, (size_t)m.qkv.rows * 4, s>>>(m, p.qkv, l, one);
+            dim3 ag((T + 63) / 64, m.n_heads, 1);
             if (m.head_dim == 64)
-                attn_prefill_tc_kernel<64><<<ag, 128, attn_tc_smem<64>(), s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
+                attn_prefill_tc_kernel<64><<<ag, 128, attn_tc_smem<64>(), s>>>(m, p.qkv, p.o, olo, l, one);
             else
-                attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, seq, p0, T);
+                attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, one);
             PF_CK(cudaGetLastError());
             PF_CK(gemm(p.o_map, p.o_lo_map, &p.maps[2 * (4 * l + 1)], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
@@ -460,6 +476,95 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
             argmax_kernel<<<1, 1024, 0, s>>>(lg, m.vocab, next_id, m.status);
             PF_CK(cudaGetLastError());
         }
+    }
+#undef PF_CK
+    return cudaSuccess;
+}
+
+// Several empty sequences at once: their prompts, concatenated in order, are cut into
+// blocks of up to p.rows rows; every GEMM and norm of a block runs over all its rows
+// (rows are independent there), RoPE / append and the causal attention run per segment
+// (one sequence's consecutive positions inside the block).  The logits of every sequence
+// whose last position falls in the block are computed together.
+cudaError_t prefill_run_batch(const Model &m, const PrefillPlan &p, int nseq, const int *seqs, const int *lens,
+                              const int *tokens, float *last_logits, int *next_ids, cudaStream_t s) {
+    const int qd = m.n_heads * m.head_dim;
+    cudaError_t e = cudaSuccess;
+#define PF_CK(x)                                   \
+    do {                                           \
+        if ((e = (x)) != cudaSuccess) return e;    \
+    } while (0)
+    long long total = 0;
+    for (int i = 0; i < nseq; i++) total += lens[i];
+    const size_t xlo = (size_t)p.rows * m.dim, olo = (size_t)p.rows * qd, hlo = (size_t)p.rows * m.hidden;
+    int si = 0, spos = 0;  // the next row to place: sequence si, its position spos
+    for (long long r0 = 0; r0 < total;) {
+        struct Seg { int seq, idx, pos0, count, row; };
+        Seg segs[kMaxBatch + 1];
+        int nsegs = 0, T = 0;
+        while (T < p.rows && si < nseq) {
+            const int take = std::min(lens[si] - spos, p.rows - T);
+            segs[nsegs++] = {seqs[si], si, spos, take, T};
+            T += take;
+            spos += take;
+            if (spos == lens[si]) {
+                si++;
+                spos = 0;
+            }
+        }
+        PfSegs tab{};
+        int maxcount = 0;
+        tab.n = nsegs;
+        for (int k = 0; k < nsegs; k++) {
+            tab.seq[k] = segs[k].seq;
+            tab.pos0[k] = segs[k].pos0;
+            tab.count[k] = segs[k].count;
+            tab.row[k] = segs[k].row;
+            maxcount = std::max(maxcount, segs[k].count);
+        }
+        embed_rows_kernel<<<T, 256, 0, s>>>(m, tokens + r0, p.x, m.status);
+        PF_CK(cudaGetLastError());
+        for (int l = 0; l < m.n_layers; l++) {
+            const float *gn = m.norms + (size_t)l * 2 * m.dim;
+            rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(p.x, gn, p.xn, xlo, m.dim, m.norm_eps);
+            PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 0)], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
+                       m.qkv.rows, m.status, s));
+            rope_append_kernel<true><<<T, 256, (size_t)m.qkv.rows * 4, s>>>(m, p.qkv, l, tab);
+            dim3 ag((maxcount + 63) / 64, m.n_heads, nsegs);  // every segment in one launch
+            if (m.head_dim == 64)
+                attn_prefill_tc_kernel<64><<<ag, 128, attn_tc_smem<64>(), s>>>(m, p.qkv, p.o, olo, l, tab);
+            else
+                attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, tab);
+            PF_CK(cudaGetLastError());
+            PF_CK(gemm(p.o_map, p.o_lo_map, &p.maps[2 * (4 * l + 1)], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
+                       m.status, s));
+            rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(p.x, gn + m.dim, p.xn, xlo, m.dim, m.norm_eps);
+            PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 2)], m.w13, T, GEMM_SWIGLU, nullptr, p.h, p.h + hlo,
+                       m.hidden, m.status, s));
+            PF_CK(gemm(p.h_map, p.h_lo_map, &p.maps[2 * (4 * l + 3)], m.w2, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
+                       m.status, s));
+        }
+        // sequences that end in this block: their last rows' final norms into xn rows
+        // 0..k-1, one logits GEMM, one argmax each
+        int first = -1, k = 0;
+        for (int j = 0; j < nsegs; j++) {
+            const Seg &g = segs[j];
+            if (g.pos0 + g.count != lens[g.idx]) continue;
+            if (first < 0) first = g.idx;
+            rmsnorm_bf16_kernel<<<1, 256, 0, s>>>(p.x + (size_t)(g.row + g.count - 1) * m.dim,
+                                                  m.norms + (size_t)m.n_layers * 2 * m.dim, p.xn + (size_t)k * m.dim, xlo,
+                                                  m.dim, m.norm_eps);
+            k++;
+        }
+        if (k > 0) {
+            float *lg = (last_logits ? last_logits : p.logits) + (last_logits ? (size_t)first * m.vocab : 0);
+            PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * m.n_layers)], m.emb, k, GEMM_STORE_F32, lg, nullptr,
+                       nullptr, m.vocab, m.status, s));
+            for (int j = 0; j < k; j++)
+                argmax_kernel<<<1, 1024, 0, s>>>(lg + (size_t)j * m.vocab, m.vocab, next_ids + first + j, m.status);
+            PF_CK(cudaGetLastError());
+        }
+        r0 += T;
     }
 #undef PF_CK
     return cudaSuccess;

@@ -22,7 +22,7 @@ struct PrefillPlan {
     float *qkv = nullptr;      // [rows][(H + 2 KV) hd]
     uint16_t *o = nullptr;     // [2][rows][H hd] attention output (hi, lo)
     uint16_t *h = nullptr;     // [2][rows][hidden] SwiGLU output (hi, lo)
-    float *logits = nullptr;   // [vocab] when the caller wants no logits
+    float *logits = nullptr;   // [max_batch][vocab] when the caller wants no logits
     std::vector<CUtensorMap> maps;  // per layer: qkv, wo, w13, w2; then the embedding (each: 64-, 128-row boxes)
     CUtensorMap xn_map, o_map, h_map, xn_lo_map, o_lo_map, h_lo_map;
 };
@@ -35,6 +35,18 @@ bool prefill_supported(const Model &m);
 cudaError_t prefill_prepare(const Model &m, PrefillPlan &p, int rows);
 
 // Enqueue the prefill of positions 0 .. n-1 of sequence `seq` (tokens on the device).
+// Segments of one prefill block: segment k is `count` consecutive positions from pos0 of
+// sequence seq, at block rows [row, row + count).
+struct PfSegs {
+    int n;
+    int seq[kMaxBatch + 1], pos0[kMaxBatch + 1], count[kMaxBatch + 1], row[kMaxBatch + 1];
+};
+
+// Prompts of nseq empty sequences, concatenated in `tokens` (device); last_logits null or
+// [nseq][vocab]; next_ids [nseq] (device).
+cudaError_t prefill_run_batch(const Model &m, const PrefillPlan &p, int nseq, const int *seqs, const int *lens,
+                              const int *tokens, float *last_logits, int *next_ids, cudaStream_t s);
+
 cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int *tokens, int n, float *last_logits,
                         int *next_id, cudaStream_t s);
 

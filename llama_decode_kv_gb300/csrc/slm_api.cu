@@ -513,7 +513,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         } pb[] = {
             {(void **)&pp.x, (size_t)rows * dim * 4},        {(void **)&pp.xn, (size_t)rows * dim * 2 * 2},
             {(void **)&pp.qkv, (size_t)rows * qkv_rows * 4}, {(void **)&pp.o, (size_t)rows * qd * 2 * 2},
-            {(void **)&pp.h, (size_t)rows * hid * 2 * 2},    {(void **)&pp.logits, (size_t)V * 4},
+            {(void **)&pp.h, (size_t)rows * hid * 2 * 2},    {(void **)&pp.logits, (size_t)B * V * 4},
         };
         for (auto &b : pb) {
             if ((rc = dev_alloc(c, b.dst, b.bytes))) return rc;
@@ -693,6 +693,45 @@ extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids
     } else if (!tok_dev || !log_dev || !ids_dev) {
         CK(c, cudaStreamSynchronize(s));
         if (!ids_dev) memcpy(next_ids, c->h_step + kMaxBatch, (size_t)batch * 4);
+    }
+    return SLM_OK;
+}
+
+extern "C" int slm_prefill_batch(slm_ctx *c, int32_t nseq, const int32_t *seqs, const int32_t *lens,
+                                 const int32_t *tokens, float *last_logits, int32_t *next_ids, void *stream) {
+    if (!c) return SLM_EINVAL;
+    if (!seqs || !lens || !tokens || !next_ids) return fail(c, SLM_EINVAL, "seqs, lens, tokens and next_ids must be non-NULL");
+    if (nseq < 1 || nseq > c->cfg.max_batch) return fail(c, SLM_EINVAL, "nseq %d outside [1, %d]", nseq, c->cfg.max_batch);
+    if (!is_device_ptr(tokens) || !is_device_ptr(next_ids) || (last_logits && !is_device_ptr(last_logits)))
+        return fail(c, SLM_EINVAL, "tokens, last_logits and next_ids must be device memory");
+    bool tc = c->prefill_tc;
+    for (int i = 0; i < nseq; i++) {
+        const int q = seqs[i];
+        if (q < 0 || q >= c->cfg.max_batch) return fail(c, SLM_EINVAL, "seq %d out of range", q);
+        for (int j = 0; j < i; j++)
+            if (seqs[j] == q) return fail(c, SLM_EINVAL, "seq %d repeated", q);
+        if (c->len[q] != 0) return fail(c, SLM_ESTATE, "sequence %d is not empty (%d positions)", q, c->len[q]);
+        if (lens[i] < 1) return fail(c, SLM_EINVAL, "prompt length %d < 1", lens[i]);
+        if (lens[i] > c->cfg.max_seq)
+            return fail(c, SLM_ECAPACITY, "prompt of %d tokens exceeds max_seq %d", lens[i], c->cfg.max_seq);
+        if (lens[i] < kTensorPrefillMin) tc = false;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if (tc) {
+        cudaError_t e = prefill_run_batch(c->m, c->plan, nseq, seqs, lens, tokens, last_logits, next_ids, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, SLM_ECUDA, "batched tensor-core prefill failed: %s", cudaGetErrorString(e));
+        }
+        for (int i = 0; i < nseq; i++) c->len[seqs[i]] = lens[i];
+        return SLM_OK;
+    }
+    size_t off = 0;  // short prompts or no tensor-core path: one sequence at a time
+    for (int i = 0; i < nseq; i++) {
+        const int rc = slm_prefill(c, seqs[i], tokens + off, lens[i],
+                                   last_logits ? last_logits + (size_t)i * c->cfg.vocab : nullptr, next_ids + i, stream);
+        if (rc) return rc;
+        off += (size_t)lens[i];
     }
     return SLM_OK;
 }

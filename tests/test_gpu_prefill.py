@@ -73,3 +73,57 @@ def test_tensor_prefill_equals_token_by_token_prefill_closely(slm):
     la, lb = la.cpu().numpy(), lb[0].cpu().numpy()
     assert np.abs(la - lb).max() <= 2e-2 * np.abs(lb).max()
     assert a.sync() == 0 and b.sync() == 0
+
+
+def test_batched_prefill_equals_one_prefill_per_sequence(slm):
+    # max_seq 128: prefill blocks of 128 rows, so the five prompts (318 positions) are cut
+    # into three blocks with sequences crossing block edges
+    s = SHAPE.replace(max_seq=128, max_batch=6)
+    W = synth.make_weights(s, seed=31)
+    seqs, lens = [4, 0, 2, 5, 1], [50, 90, 128, 17, 33]
+    prompts = [synth.make_prompt(s, q, n) for q, n in zip(seqs, lens)]
+    dev = torch.device("cuda")
+    a = slm.Engine(s, W)
+    toks = torch.as_tensor(np.concatenate(prompts).astype(np.int32)).to(dev)
+    lg = torch.zeros((len(seqs), s.vocab), dtype=torch.float32, device=dev)
+    ids = torch.zeros(len(seqs), dtype=torch.int32, device=dev)
+    assert a.prefill_batch(seqs, toks, lens, lg, ids) == 0, a.last_error()
+    assert a.sync() == 0, a.last_error()
+    b = slm.Engine(s, W)
+    for i, (q, p) in enumerate(zip(seqs, prompts)):
+        lgb, nid = b.prefill_checked(q, p, want_logits=True)
+        assert int(ids[i].item()) == int(nid.item())
+        # the same GEMM rows, in other tiles: equal up to the order of fp32 sums
+        np.testing.assert_allclose(lg[i].cpu().numpy(), lgb.cpu().numpy(), rtol=0, atol=1e-4)
+        assert a.seq_len(q) == b.seq_len(q) == len(p)
+        for layer in range(s.n_layers):
+            ka, va = a.kv(layer, q)
+            kb, vb = b.kv(layer, q)
+            np.testing.assert_allclose(ka, kb, rtol=0, atol=1e-2 * np.abs(kb).max())
+            np.testing.assert_allclose(va, vb, rtol=0, atol=1e-2 * np.abs(vb).max())
+    assert b.sync() == 0
+    # and against the oracle
+    m = oracle.Model(s, W)
+    for i, (q, p) in enumerate(zip(seqs, prompts)):
+        ref, rid = m.prefill(q, p)
+        check_logits(lg[i].cpu().numpy(), ref, 2e-2, f"batched prefill seq {q}")
+        check_id(int(ids[i].item()), ref, rid, f"batched prefill seq {q}")
+    a.close()
+    b.close()
+
+
+def test_batched_prefill_refuses_bad_arguments(slm):
+    s = SHAPE.replace(max_seq=64, max_batch=3)
+    eng = slm.Engine(s, synth.make_weights(s, seed=3))
+    dev = torch.device("cuda")
+    toks = torch.zeros(64, dtype=torch.int32, device=dev)
+    ids = torch.zeros(3, dtype=torch.int32, device=dev)
+    EINVAL, ECAPACITY, ESTATE = -1, -3, -5
+    assert eng.prefill_batch([0, 0], toks, [20, 20], None, ids) == EINVAL
+    assert eng.prefill_batch([0, 3], toks, [20, 20], None, ids) == EINVAL
+    assert eng.prefill_batch([0], toks, [65], None, ids) == ECAPACITY
+    assert eng.prefill_batch([0], toks.cpu(), [20], None, ids) == EINVAL  # host tokens
+    eng.prefill_checked(1, synth.make_prompt(s, 1, 20), want_logits=False)
+    assert eng.prefill_batch([0, 1], toks, [20, 20], None, ids) == ESTATE
+    assert eng.seq_len(0) == 0
+    eng.close()
