@@ -223,6 +223,16 @@ int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, f
                       float *v_host);
 
 /*
+ * slm_debug_plan -- test hook: the work split and shared-memory layout slm_create would
+ * choose for `config` on a GPU with `sms` SMs, computed on the host (no device needed).
+ * out: int32[47] = grid, roles, role0[5], own_ld, acc_bytes, xs_bytes, ring_slots,
+ * dynamic shared-memory bytes, then for the embedding, QKV, Wo, W1/W3 and W2 matrices
+ * each: rows, K, KB, KBp, nkt, rows_per_unit, rows_per_chunk.  Returns SLM_OK, or the
+ * error slm_create would return for the plan (text in slm_last_error(NULL)).
+ */
+int slm_debug_plan(const slm_config *config, int32_t sms, int32_t *out, int32_t out_len);
+
+/*
  * slm_debug_trace -- timeline hook (in the spirit of kasahare's "--timing" and
  * forward_traced): with enable != 0, every following step records, for each CTA of
  * the decode kernel and each phase (5 per layer: QKV, attention, Wo, W1/W3, W2; then

@@ -59,6 +59,7 @@ _SIGS = {
     "slm_debug_copy_kv": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
     "slm_debug_fill_kv": (ctypes.c_int, [_P, ctypes.c_float]),
     "slm_debug_trace": (ctypes.c_int, [_P, _I32, _P, ctypes.c_size_t]),
+    "slm_debug_plan": (ctypes.c_int, [ctypes.POINTER(slm_config), _I32, _P, _I32]),
     "slm_debug_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
@@ -135,6 +136,22 @@ def sample(logits, temperature: float, top_k: int, top_p: float, uniforms, next_
     batch, ld = int(logits.shape[0]), int(logits.shape[1])
     return slm_sample(batch, ld, _ptr(logits), ld, float(temperature), int(top_k), float(top_p), _ptr(uniforms),
                       _ptr(next_ids), _stream_ptr(stream))
+
+
+def plan(shape, sms: int = 152) -> dict:
+    """slm_debug_plan: the engine layout for a shape, computed on the host (no GPU)."""
+    cfg = config_from_shape(shape)
+    out = np.zeros(47, dtype=np.int32)
+    rc = slm_debug_plan(ctypes.byref(cfg), sms, out.ctypes.data, out.size)
+    if rc != 0:
+        raise SlmError(rc, "slm_debug_plan", slm_last_error(None).decode())
+    v = [int(x) for x in out]
+    d = {"grid": v[0], "roles": v[1], "role0": v[2:7], "own_ld": v[7], "acc_bytes": v[8], "xs_bytes": v[9],
+         "ring_slots": v[10], "smem": v[11]}
+    for i, name in enumerate(("emb", "qkv", "wo", "w13", "w2")):
+        r = v[12 + 7 * i: 19 + 7 * i]
+        d[name] = dict(zip(("rows", "K", "KB", "KBp", "nkt", "rows_per_unit", "rows_per_chunk"), r))
+    return d
 
 
 class Engine:

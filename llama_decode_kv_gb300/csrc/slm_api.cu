@@ -261,21 +261,10 @@ extern "C" void slm_destroy(slm_ctx *ctx) {
     delete ctx;
 }
 
-static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, size_t nbytes) {
-    std::string why;
-    if (!config_ok(cfg, why)) return fail(c, SLM_EINVAL, "bad config: %s", why.c_str());
+// The engine's work split and shared-memory layout for `sms` CTAs (one per SM): pure
+// arithmetic on the config, no device calls (slm_debug_plan runs it on the host).
+static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
     const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4;
-    const size_t n_w = weight_count(cfg);
-    if (nbytes != n_w * esz)
-        return fail(c, SLM_EINVAL, "weights are %zu bytes, the config needs %zu", nbytes, n_w * esz);
-    c->cfg = *cfg;
-    CK(c, cudaGetDevice(&c->device));
-    int sms = 0;
-    CK(c, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
-    int coop = 0;
-    CK(c, cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device));
-    if (!coop) return fail(c, SLM_EUNSUPPORTED, "device lacks cooperative launch");
-
     const int dim = cfg->dim, H = cfg->n_heads, KV = cfg->n_kv_heads, hd = cfg->head_dim;
     const int hid = cfg->hidden, V = cfg->vocab, L = cfg->n_layers, B = cfg->max_batch;
     const int qd = H * hd, kvd = KV * hd, qkv_rows = qd + 2 * kvd;
@@ -369,6 +358,32 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         c->ring_slots = slots;
         c->smem = decode_smem_bytes(B, c->own_ld, c->acc_bytes, c->xs_bytes, slots);
     }
+    return SLM_OK;
+}
+
+static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, size_t nbytes) {
+    std::string why;
+    if (!config_ok(cfg, why)) return fail(c, SLM_EINVAL, "bad config: %s", why.c_str());
+    const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4;
+    const size_t n_w = weight_count(cfg);
+    if (nbytes != n_w * esz)
+        return fail(c, SLM_EINVAL, "weights are %zu bytes, the config needs %zu", nbytes, n_w * esz);
+    c->cfg = *cfg;
+    CK(c, cudaGetDevice(&c->device));
+    int sms = 0;
+    CK(c, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device));
+    int coop = 0;
+    CK(c, cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device));
+    if (!coop) return fail(c, SLM_EUNSUPPORTED, "device lacks cooperative launch");
+    int rc = plan_engine(c, cfg, sms);
+    if (rc) return rc;
+    const int dim = cfg->dim, H = cfg->n_heads, KV = cfg->n_kv_heads, hd = cfg->head_dim;
+    const int hid = cfg->hidden, V = cfg->vocab, L = cfg->n_layers, B = cfg->max_batch;
+    const int qd = H * hd, kvd = KV * hd, qkv_rows = qd + 2 * kvd;
+    Model &m = c->m;
+    const int grid = c->grid;
+    (void)qkv_rows;
+    (void)grid;
     int per_sm = 0;
     CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
     if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
@@ -453,7 +468,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
             rope[((size_t)p * (hd / 2) + i) * 2 + 1] = (float)std::sin(a);
         }
     void *dblock = nullptr;
-    int rc = dev_alloc(c, &dblock, total);
+    rc = dev_alloc(c, &dblock, total);
     if (rc) return rc;
     CK(c, cudaMemcpy(dblock, h.data(), total, cudaMemcpyHostToDevice));
     uint8_t *d = (uint8_t *)dblock;
@@ -525,6 +540,47 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     c->len.assign(B, 0);
     CK(c, cudaDeviceSynchronize());
     return SLM_OK;
+}
+
+extern "C" int slm_debug_plan(const slm_config *config, int32_t sms, int32_t *out, int32_t out_len) {
+    if (!config || !out || sms < 1 || out_len < 47) {
+        set_detached_error("slm_debug_plan: config, out (47 entries) and sms >= 1 are required");
+        return SLM_EINVAL;
+    }
+    slm_ctx *c = new (std::nothrow) slm_ctx();
+    if (!c) return SLM_ENOMEM;
+    std::string why;
+    int rc;
+    if (!config_ok(config, why)) {
+        rc = fail(c, SLM_EINVAL, "bad config: %s", why.c_str());
+    } else {
+        c->cfg = *config;
+        rc = plan_engine(c, config, sms);
+    }
+    if (rc == SLM_OK) {
+        int k = 0;
+        out[k++] = c->grid;
+        out[k++] = c->roles;
+        for (int r = 0; r < 5; r++) out[k++] = c->role0[r];
+        out[k++] = c->own_ld;
+        out[k++] = c->acc_bytes;
+        out[k++] = c->xs_bytes;
+        out[k++] = c->ring_slots;
+        out[k++] = (int32_t)c->smem;
+        for (const Mat *M : {&c->m.emb, &c->m.qkv, &c->m.wo, &c->m.w13, &c->m.w2}) {
+            out[k++] = M->rows;
+            out[k++] = M->K;
+            out[k++] = M->KB;
+            out[k++] = M->KBp;
+            out[k++] = M->nkt;
+            out[k++] = M->rows_per_unit;
+            out[k++] = M->rows_per_chunk;
+        }
+    } else {
+        set_detached_error(c->err.c_str());
+    }
+    slm_destroy(c);
+    return rc;
 }
 
 extern "C" int slm_create(const slm_config *config, const void *weights, size_t nbytes, slm_ctx **out) {
