@@ -402,9 +402,19 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = peaks()
     traffic = profile_traffic()
 
-    # end to end through the C ABI with host buffers (copies inside the timed region)
-    tok_h = np.array([int(toks[state["cur"]].item())], dtype=np.int32)
+    # end to end through the C ABI with host buffers (copies inside the timed region), over
+    # the same contexts as the device-timed steps: the sequence is prefilled again and
+    # given the same warm-up
+    eng.reset(0)
+    _, nid = eng.prefill_checked(0, prompt, want_logits=False)
+    tok_h = np.array([int(nid.item())], dtype=np.int32)
     ids_h = np.empty(1, dtype=np.int32)
+    state["pos"] = len(prompt)
+    for _ in range(max(args.warmup, 3)):
+        if eng.decode_step([0], tok_h, [state["pos"]], None, ids_h) != 0:
+            raise RuntimeError(f"slm_decode_step (host buffers): {eng.last_error()}")
+        tok_h[0] = ids_h[0]
+        state["pos"] += 1
     e2e_steps = args.steps
     barrier(world)
     t0 = time.perf_counter()
