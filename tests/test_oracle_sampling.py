@@ -1,13 +1,14 @@
 """Pins for the sampling oracle (``oracle/sampling.py``): the page's worked top-2
 example, greedy ties, closed forms for temperature and top-p, and exact frequencies of
-the inverse-CDF draw over a grid of uniforms."""
+the inverse-CDF draw over a grid of uniforms.  Each pin is a ``check_*`` function of the
+module under test, so that the mutation test can run them against planted mistakes."""
 import math
 import os
 
 import numpy as np
 import pytest
 
-from oracle import sampling
+from oracle import sampling as _sampling
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "sampling_top2_example.txt")
 
@@ -20,7 +21,7 @@ def _example():
     return names, p, p2
 
 
-def test_top2_example_of_the_page():
+def check_top2_example_of_the_page(sampling):
     # logits = log p reproduce the page's distribution at temperature 1
     names, p, p2 = _example()
     logits = np.log(p).astype(np.float32)
@@ -34,7 +35,7 @@ def test_top2_example_of_the_page():
         assert got == ("mat" if u < 0.6 - 1e-6 else "floor") or abs(u - 0.6) < 1e-6
 
 
-def test_greedy_is_the_first_largest():
+def check_greedy_is_the_first_largest(sampling):
     x = np.array([0.5, 2.0, -1.0, 2.0, 1.9], dtype=np.float32)
     for u in (0.0, 0.5, 0.999):
         assert sampling.sample(x, 0.0, 0, 1.0, u) == 1
@@ -44,13 +45,13 @@ def test_greedy_is_the_first_largest():
         assert sampling.sample(x, 2.5, 1, 1.0, u) == 1
 
 
-def test_top_k_order_breaks_ties_by_lower_index():
+def check_top_k_order_breaks_ties_by_lower_index(sampling):
     x = np.array([1.0, 3.0, 3.0, 0.0, 3.0], dtype=np.float32)
     order, _ = sampling.candidates(x, 1.0, 4, 1.0)
     assert order == [1, 2, 4, 0]
 
 
-def test_temperature_is_a_power_of_the_distribution():
+def check_temperature_is_a_power_of_the_distribution(sampling):
     # softmax(l / T) = p^(1/T) / sum p^(1/T) for l = log p (closed form)
     _, p, _ = _example()
     logits = np.log(p).astype(np.float32)
@@ -66,7 +67,7 @@ def test_temperature_is_a_power_of_the_distribution():
     assert w07[0] / w07.sum() > 0.45 > w15[0] / w15.sum()
 
 
-def test_top_p_keeps_the_shortest_prefix_that_reaches_p():
+def check_top_p_keeps_the_shortest_prefix_that_reaches_p(sampling):
     _, p, _ = _example()
     logits = np.log(p).astype(np.float32)
     for top_p, keep in ((0.3, 1), (0.45, 1), (0.5, 2), (0.75, 2), (0.8, 3), (0.95, 4), (1.0, 4)):
@@ -77,7 +78,7 @@ def test_top_p_keeps_the_shortest_prefix_that_reaches_p():
         sampling.candidates(logits, 1.0, 0, 0.9)
 
 
-def test_inverse_cdf_frequencies_are_exact_on_a_grid():
+def check_inverse_cdf_frequencies_are_exact_on_a_grid(sampling):
     # n equally spaced u's: candidate i is drawn for the u's inside its CDF interval, so
     # its count is within one of n * p_i
     rng = np.random.default_rng(5)
@@ -93,3 +94,27 @@ def test_inverse_cdf_frequencies_are_exact_on_a_grid():
         assert set(counts) <= set(order)
         for i, pi in zip(order, probs):
             assert abs(counts.get(i, 0) - n * pi) <= 1.0 + 1e-9, (i, counts.get(i, 0), n * pi)
+
+
+def test_top2_example_of_the_page():
+    check_top2_example_of_the_page(_sampling)
+
+
+def test_greedy_is_the_first_largest():
+    check_greedy_is_the_first_largest(_sampling)
+
+
+def test_top_k_order_breaks_ties_by_lower_index():
+    check_top_k_order_breaks_ties_by_lower_index(_sampling)
+
+
+def test_temperature_is_a_power_of_the_distribution():
+    check_temperature_is_a_power_of_the_distribution(_sampling)
+
+
+def test_top_p_keeps_the_shortest_prefix_that_reaches_p():
+    check_top_p_keeps_the_shortest_prefix_that_reaches_p(_sampling)
+
+
+def test_inverse_cdf_frequencies_are_exact_on_a_grid():
+    check_inverse_cdf_frequencies_are_exact_on_a_grid(_sampling)
