@@ -233,6 +233,18 @@ int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, f
 int slm_debug_plan(const slm_config *config, int32_t sms, int32_t *out, int32_t out_len);
 
 /*
+ * slm_debug_cluster -- test hook: how this engine runs single-row decode steps.  Returns
+ * 1 when they run on the cluster kernel (attention clusters, one per kv head, and FFN
+ * clusters; the layout follows the block equations of kasahare 0.4.0 / simple-llm,
+ * "Architecture", split so that a layer needs two grid-wide hand-offs), 0 when they run
+ * on the persistent kernel, or a negative SLM_E* code.  out (may be NULL): int32[12] =
+ * cluster size C, attention clusters NA, FFN clusters NF, grid, hidden units per FFN
+ * cluster, ring slots, dynamic shared-memory bytes, units per chunk of the QKV, Wo,
+ * W1/W3, W2 and logits phases.
+ */
+int slm_debug_cluster(const slm_ctx *ctx, int32_t *out, int32_t out_len);
+
+/*
  * slm_debug_trace -- timeline hook (in the spirit of kasahare's "--timing" and
  * forward_traced): with enable != 0, every following step records, for each CTA of
  * the decode kernel and each phase (5 per layer: QKV, attention, Wo, W1/W3, W2; then

@@ -60,6 +60,7 @@ _SIGS = {
     "slm_debug_fill_kv": (ctypes.c_int, [_P, ctypes.c_float]),
     "slm_debug_trace": (ctypes.c_int, [_P, _I32, _P, ctypes.c_size_t]),
     "slm_debug_plan": (ctypes.c_int, [ctypes.POINTER(slm_config), _I32, _P, _I32]),
+    "slm_debug_cluster": (ctypes.c_int, [_P, _P, _I32]),
     "slm_debug_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
@@ -235,6 +236,19 @@ class Engine:
         if rc < 0:
             raise SlmError(rc, "slm_debug_copy_kv", self.last_error())
         return k, v
+
+    def cluster_plan(self):
+        """None when single-row steps run on the persistent kernel, else a dict of the
+        cluster kernel's plan (slm_debug_cluster)."""
+        out = np.zeros(12, dtype=np.int32)
+        rc = slm_debug_cluster(self.ctx, out.ctypes.data, out.size)
+        if rc < 0:
+            raise SlmError(rc, "slm_debug_cluster", self.last_error())
+        if rc == 0:
+            return None
+        keys = ("C", "NA", "NF", "grid", "hpc", "ring_slots", "smem", "upc_qkv", "upc_wo", "upc_w13",
+                "upc_w2", "upc_emb")
+        return dict(zip(keys, (int(v) for v in out)))
 
     def trace(self, enable: bool = True, fetch: bool = False):
         """Turn the phase timeline on/off; with fetch, return the last step's record as

@@ -26,6 +26,9 @@ namespace slm {
 cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream);
 cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm);
 size_t decode_smem_bytes(int max_batch, int own_ld, int acc_bytes, int xs_bytes, int ring_slots);
+cudaError_t cluster_capacity(int weight_bf16, size_t smem, int C, int *clusters);
+cudaError_t cluster_kernel_attrs(int weight_bf16, size_t smem, int C);
+cudaError_t launch_decode_cluster(const ClusterParams &P, size_t smem, cudaStream_t stream);
 }  // namespace slm
 
 using namespace slm;
@@ -53,6 +56,10 @@ struct slm_ctx {
     int *h_ids = nullptr;        // pinned
     int *h_step = nullptr;       // mapped pinned [2][kMaxBatch] + 1: host tokens, ids, the done word
     int *d_step = nullptr;       //   its device address (the kernel reads / writes it directly)
+    // Single-row steps on thread-block clusters (decode_cluster.cu), when the plan allows.
+    bool cl_on = false;
+    ClusterParams cp{};          // the engine part (model, geometry, buffers, layout)
+    size_t cl_smem = 0;
     std::string err;
 };
 
@@ -361,6 +368,107 @@ static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
     return SLM_OK;
 }
 
+// The cluster plan of an engine (see ClusterParams): clusters of C CTAs, `clusters` of
+// them resident at once.  Pure arithmetic on the config and the engine plan; leaves
+// cl_on false (with the reason in `why`) when the shape does not suit the cluster kernel.
+static void plan_cluster(slm_ctx *c, int clusters, int C, std::string &why) {
+    const slm_config *cfg = &c->cfg;
+    const Model &m = c->m;
+    c->cl_on = false;
+    if (const char *e = getenv("SLM_NO_CLUSTER"))
+        if (atoi(e) != 0) {
+            why = "disabled by SLM_NO_CLUSTER";
+            return;
+        }
+    const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4, kvesz = cfg->kv_dtype == SLM_BF16 ? 2 : 4;
+    const int dim = cfg->dim, H = cfg->n_heads, KV = cfg->n_kv_heads, hd = cfg->head_dim, hid = cfg->hidden;
+    const int G = H / KV, qd = H * hd, kvd = KV * hd;
+    const double layer_bytes = ((double)(qd + 2 * kvd) * dim + (double)dim * qd + 3.0 * hid * dim) * esz;
+    if (layer_bytes > kRolesMaxLayerBytes) {
+        why = "layers too large: each phase needs every SM's bandwidth";
+        return;
+    }
+    if (dim > 8 * kComputeThreads) {
+        why = "dim above the kernel's per-thread gain registers";
+        return;
+    }
+    if ((C != 8 && C != 16) || G > kClusterMaxG || hd > kClusterMaxHd || G * hd > kComputeThreads ||
+        (size_t)G * ((cfg->max_seq + C - 1) / C) > 4 * (size_t)kComputeThreads) {
+        why = "cluster size or head geometry outside the kernel's limits";
+        return;
+    }
+    if (clusters < KV + 1) {
+        why = "not enough resident clusters for one attention cluster per kv head plus an FFN cluster";
+        return;
+    }
+    ClusterParams &P = c->cp;
+    P.C = C;
+    P.NA = KV;
+    int NF = std::min(clusters - KV, hid);
+    P.hpc = (hid + NF - 1) / NF;
+    P.NF = (hid + P.hpc - 1) / P.hpc;
+    P.grid = (P.NA + P.NF) * C;
+    P.wo_kbp = (int)round_up((size_t)G * hd, kPadElems);
+    P.w2_kbp = (int)round_up((size_t)P.hpc, kPadElems);
+    // units per chunk: at most 8 rows (one row group), at most one ring slot, about one
+    // chunk per warp
+    auto upc = [&](int units_per_cta, int rpu, size_t rowbytes) {
+        const int fit = std::min(8 / rpu, (int)(kChunkBytes / (rowbytes * rpu)));
+        const int want = (units_per_cta + kComputeWarps - 1) / kComputeWarps;
+        return std::max(1, std::min(fit, want));
+    };
+    const size_t rb_qkv = (size_t)m.qkv.KBp * esz, rb_w13 = (size_t)m.w13.KBp * esz, rb_emb = (size_t)m.emb.KBp * esz;
+    const size_t rb_wo = (size_t)P.wo_kbp * esz, rb_w2 = (size_t)P.w2_kbp * esz;
+    for (size_t rb : {rb_qkv * 2, rb_w13 * 2, rb_emb, rb_wo, rb_w2})
+        if (rb > (size_t)kChunkBytes) {
+            why = "a unit of rows exceeds one ring slot";
+            return;
+        }
+    P.upc_qkv = upc(((G + 2) * hd / 2 + C - 1) / C, 2, rb_qkv);
+    P.upc_wo = upc((dim + C - 1) / C, 1, rb_wo);
+    P.upc_w13 = upc((P.hpc + C - 1) / C, 2, rb_w13);
+    P.upc_w2 = upc((dim + C - 1) / C, 1, rb_w2);
+    P.upc_emb = upc((cfg->vocab + P.grid - 1) / P.grid, 1, rb_emb);
+    // shared memory
+    const int tcap = (cfg->max_seq + C - 1) / C;
+    P.stage_rows = std::min(tcap, kClusterStageMax);
+    P.xs_floats = std::max({m.qkv.KBp, m.w13.KBp, m.emb.KBp, P.wo_kbp});
+    size_t off = 1024;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = round_up(off + bytes, 128);
+        return (int)o;
+    };
+    P.off_xraw = take((size_t)dim * 4);
+    P.off_xs = take((size_t)P.xs_floats * 4);
+    P.off_hb = take((size_t)P.w2_kbp * 4);
+    P.off_qkv = take((size_t)(G + 2) * hd * 4);
+    P.off_st = take((size_t)C * G * (hd + 2) * 4);
+    P.off_p = take((size_t)G * tcap * 4);
+    P.off_k = take((size_t)P.stage_rows * (hd * kvesz + 16));
+    P.off_v = take((size_t)P.stage_rows * (hd * kvesz + 16));
+    const size_t blk = (size_t)(dim + C - 1) / C;
+    P.off_hop = take(std::max({(size_t)P.NF * blk, (size_t)P.NA * dim, (size_t)2 * P.grid,
+                               (size_t)m.emb.KBp * esz / 4}) * 4);  // also the staged embedding row
+    P.off_gain = take((size_t)dim * 4);
+    // dot products of the largest slice (or the attention's weighted values)
+    const size_t yv = std::max({(size_t)2 * (((G + 2) * hd / 2 + C - 1) / C), blk, (size_t)2 * ((P.hpc + C - 1) / C),
+                                (size_t)(cfg->vocab + P.grid - 1) / P.grid, (size_t)G * hd});
+    P.off_yv = take(yv * 4);
+    P.off_rope = take((size_t)hd * 4);
+    P.off_utab = take((size_t)2 * (((G + 2) * hd / 2 + C - 1) / C) * 4);
+    P.off_ring = (int)round_up(off, 1024);
+    int slots = P.off_ring < (int)kSmemLimit ? (int)((kSmemLimit - P.off_ring) / kChunkBytes) : 0;
+    slots = std::min(kMaxRingSlots, slots / 8 * 8);
+    if (slots < 8) {
+        why = "shared memory leaves fewer than 8 ring slots";
+        return;
+    }
+    P.ring_slots = slots;
+    c->cl_smem = (size_t)P.off_ring + (size_t)slots * kChunkBytes;
+    c->cl_on = true;
+}
+
 static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, size_t nbytes) {
     std::string why;
     if (!config_ok(cfg, why)) return fail(c, SLM_EINVAL, "bad config: %s", why.c_str());
@@ -387,6 +495,25 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     int per_sm = 0;
     CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
     if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
+    {
+        // clusters of 16 CTAs (measured faster at the SmolLM2 shape: less work per CTA
+        // in each phase), else 8; SLM_CLUSTER_SIZE picks one
+        int sizes[2] = {16, 8}, n = 2;
+        if (const char *e = getenv("SLM_CLUSTER_SIZE")) {
+            sizes[0] = atoi(e);
+            n = 1;
+        }
+        std::string why;
+        c->cl_on = false;
+        for (int i = 0; i < n && !c->cl_on; i++) {
+            int clusters = 0;
+            if (cluster_capacity(m.weight_bf16, kSmemLimit, sizes[i], &clusters) == cudaSuccess)
+                plan_cluster(c, clusters, sizes[i], why);
+            else
+                cudaGetLastError();
+        }
+        if (c->cl_on) CK(c, cluster_kernel_attrs(m.weight_bf16, c->cl_smem, c->cp.C));
+    }
 
     // ---- weights: repack on the host, then one copy to the device
     std::vector<uint8_t> src;
@@ -406,7 +533,14 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     size_t off_wo = round_up(off_qkv + (size_t)L * m.qkv.layer_stride, al);
     size_t off_w13 = round_up(off_wo + (size_t)L * m.wo.layer_stride, al);
     size_t off_w2 = round_up(off_w13 + (size_t)L * m.w13.layer_stride, al);
-    size_t off_norm = round_up(off_w2 + (size_t)L * m.w2.layer_stride, al);
+    // cluster kernel copies: Wo by head group, W2 by hidden slice
+    const int Gq = H / KV;
+    ClusterParams &cp = c->cp;
+    const long long wo_g_stride = c->cl_on ? (long long)KV * dim * cp.wo_kbp * esz : 0;
+    const long long w2_c_stride = c->cl_on ? (long long)cp.NF * dim * cp.w2_kbp * esz : 0;
+    size_t off_wog = round_up(off_w2 + (size_t)L * m.w2.layer_stride, al);
+    size_t off_w2c = round_up(off_wog + (size_t)L * wo_g_stride, al);
+    size_t off_norm = round_up(off_w2c + (size_t)L * w2_c_stride, al);
     size_t off_rope = round_up(off_norm + ((size_t)L * 2 + 1) * dim * 4, al);
     size_t total = round_up(off_rope + (size_t)cfg->max_seq * (hd / 2) * 2 * 4, al);
     std::vector<uint8_t> h;
@@ -444,7 +578,15 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
             pack_head(r0 + G * hd, wk + (size_t)g * hd * dim * esz);
             pack_head(r0 + (G + 1) * hd, wv + (size_t)g * hd * dim * esz);
         }
-        pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, take((size_t)dim * qd), dim, esz);
+        const uint8_t *wo_src = take((size_t)dim * qd);
+        pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, wo_src, dim, esz);
+        if (c->cl_on) {  // [kv head g][dim][wo_kbp]: columns g G hd .. (g + 1) G hd - 1 of Wo
+            uint8_t *dst = h.data() + off_wog + (size_t)l * wo_g_stride;
+            const size_t gw = (size_t)Gq * hd;
+            for (int g = 0; g < KV; g++)
+                for (int r = 0; r < dim; r++)
+                    memcpy(dst + (((size_t)g * dim + r) * cp.wo_kbp) * esz, wo_src + ((size_t)r * qd + g * gw) * esz, gw * esz);
+        }
         const uint8_t *fn = take(dim);
         for (int i = 0; i < dim; i++) norms[(size_t)l * 2 * dim + dim + i] = widen(fn, esz, i);
         const uint8_t *w1 = take((size_t)hid * dim);
@@ -454,7 +596,17 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
             pack_rows(w13, m.w13, 2 * j, w1 + (size_t)j * dim * esz, 1, esz);
             pack_rows(w13, m.w13, 2 * j + 1, w3 + (size_t)j * dim * esz, 1, esz);
         }
-        pack_rows(h.data() + off_w2 + (size_t)l * m.w2.layer_stride, m.w2, 0, take((size_t)dim * hid), dim, esz);
+        const uint8_t *w2_src = take((size_t)dim * hid);
+        pack_rows(h.data() + off_w2 + (size_t)l * m.w2.layer_stride, m.w2, 0, w2_src, dim, esz);
+        if (c->cl_on) {  // [FFN cluster f][dim][w2_kbp]: columns f hpc .. (f + 1) hpc - 1 of W2
+            uint8_t *dst = h.data() + off_w2c + (size_t)l * w2_c_stride;
+            for (int f = 0; f < cp.NF; f++) {
+                const int h0 = f * cp.hpc, n = std::min(hid, h0 + cp.hpc) - h0;
+                for (int r = 0; r < dim; r++)
+                    memcpy(dst + (((size_t)f * dim + r) * cp.w2_kbp) * esz, w2_src + ((size_t)r * hid + h0) * esz,
+                           (size_t)n * esz);
+            }
+        }
     }
     const uint8_t *on = take(dim);
     for (int i = 0; i < dim; i++) norms[(size_t)L * 2 * dim + i] = widen(on, esz, i);
@@ -479,6 +631,12 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     m.w2.base = d + off_w2;
     m.norms = (const float *)(d + off_norm);
     m.rope = (const float *)(d + off_rope);
+    if (c->cl_on) {
+        cp.wo_g = d + off_wog;
+        cp.wo_layer_stride = wo_g_stride;
+        cp.w2_c = d + off_w2c;
+        cp.w2_layer_stride = w2_c_stride;
+    }
 
     // ---- KV cache and scratch
     const size_t kvesz = m.kv_bf16 ? 2 : 4;
@@ -513,6 +671,20 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     for (auto &b : bufs) {
         if ((rc = dev_alloc(c, b.dst, b.bytes))) return rc;
         CK(c, cudaMemset(*b.dst, 0, b.bytes));
+    }
+    if (c->cl_on) {
+        struct {
+            void **dst;
+            size_t bytes;
+        } cb[] = {
+            {(void **)&cp.p_att, Lz * cp.NA * dim * 8},
+            {(void **)&cp.p_ffn, Lz * cp.NF * dim * 8},
+            {(void **)&cp.amax, (size_t)cp.grid * 2 * 8},
+        };
+        for (auto &b : cb) {
+            if ((rc = dev_alloc(c, b.dst, b.bytes))) return rc;
+            CK(c, cudaMemset(*b.dst, 0, b.bytes));
+        }
     }
     CK(c, cudaMallocHost((void **)&c->h_ids, (size_t)B * 4));
     CK(c, cudaHostAlloc((void **)&c->h_step, (size_t)(2 * kMaxBatch + 1) * 4, cudaHostAllocMapped));
@@ -666,10 +838,30 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
 }
 
 static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
+    if (++c->launch_seq == 0) c->launch_seq = 1;  // tag 0 marks never-written words
+    if (c->cl_on && P.batch == 1) {
+        ClusterParams Q = c->cp;
+        Q.m = c->m;
+        Q.seq = P.seq[0];
+        Q.pos = P.pos[0];
+        Q.tokens = P.tokens;
+        Q.logits = P.logits;
+        Q.next_ids = P.next_ids;
+        Q.done_word = P.done_word;
+        Q.do_logits = P.do_logits;
+        Q.tag = c->launch_seq;
+        Q.trace = c->trace_on ? c->d_trace : nullptr;
+        cudaError_t e = launch_decode_cluster(Q, c->cl_smem, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, SLM_ECUDA, "cluster decode launch failed: %s", cudaGetErrorString(e));
+        }
+        P.tag = Q.tag;
+        return SLM_OK;
+    }
     P.m = c->m;
     P.grid = c->grid;
     P.wide_groups = c->m.w13.rows_per_chunk >= 4;  // the largest layer matrix sets the group width
-    if (++c->launch_seq == 0) c->launch_seq = 1;  // tag 0 marks never-written words
     P.tag = c->launch_seq;
     P.trace = c->trace_on ? c->d_trace : nullptr;
     P.ring_slots = c->ring_slots;
@@ -975,6 +1167,18 @@ extern "C" int slm_debug_trace(slm_ctx *c, int32_t enable, unsigned long long *o
         CK(c, cudaMemcpy(out_host, c->d_trace, n * 8, cudaMemcpyDeviceToHost));
     }
     return (int)c->grid;
+}
+
+extern "C" int slm_debug_cluster(const slm_ctx *c, int32_t *out, int32_t out_len) {
+    if (!c) return SLM_EINVAL;
+    if (out && out_len < 12) return SLM_EINVAL;
+    if (out) {
+        const ClusterParams &p = c->cp;
+        const int32_t v[12] = {p.C, p.NA, p.NF, p.grid, p.hpc, p.ring_slots, (int32_t)c->cl_smem,
+                               p.upc_qkv, p.upc_wo, p.upc_w13, p.upc_w2, p.upc_emb};
+        for (int i = 0; i < 12; i++) out[i] = c->cl_on ? v[i] : 0;
+    }
+    return c->cl_on ? 1 : 0;
 }
 
 extern "C" int slm_debug_fill_kv(slm_ctx *c, float value) {

@@ -144,6 +144,52 @@ __host__ __device__ inline size_t ring_offset(int max_batch, int own_ld, int acc
     return (own_offset(xs_bytes) + own_bytes(max_batch, own_ld) + (size_t)acc_bytes + 1023) / 1024 * 1024;
 }
 
+// ------------------------------------------------------------------ cluster decode kernel
+// Single-row steps of small models run on thread-block clusters (decode_cluster.cu):
+// clusters [0, NA) are attention clusters, one per kv head (its query heads' QKV rows,
+// RoPE, append, attention over the cached positions split across the cluster, Wo as a
+// split-K partial over the head group's columns); clusters [NA, NA + NF) are FFN
+// clusters, each owning a slice of the hidden units (W1/W3 rows, SwiGLU, W2 as a split-K
+// partial over the slice).  Inside a cluster, vectors move through distributed shared
+// memory (st.async + mbarrier); between the two kinds of cluster, through tagged words in
+// global memory.
+constexpr int kClusterMax = 16;           // cluster size limit (non-portable above 8)
+constexpr int kClusterMaxG = 8;           // query heads per kv head
+constexpr int kClusterMaxHd = 128;        // head_dim
+constexpr int kClusterStageMax = 64;      // cached positions per CTA staged in shared memory
+
+struct ClusterParams {
+    Model m;
+    int C, NA, NF, grid;
+    int hpc;                     // hidden units per FFN cluster: cluster c owns [c hpc, (c + 1) hpc) ∩ [0, hidden)
+    // Wo by head group: [layer][kv head g][dim rows][wo_kbp] (columns g G hd .. (g + 1) G hd - 1)
+    const uint8_t *wo_g;
+    long long wo_layer_stride;
+    int wo_kbp;
+    // W2 by hidden slice: [layer][cluster c][dim rows][w2_kbp] (columns c hpc .. (c + 1) hpc - 1)
+    const uint8_t *w2_c;
+    long long w2_layer_stride;
+    int w2_kbp;
+    int upc_qkv, upc_wo, upc_w13, upc_w2, upc_emb;  // work units per ring chunk, per phase
+    uint64_t *p_att;             // [n_layers][NA][dim] tagged words: attention cluster partials
+    uint64_t *p_ffn;             // [n_layers][NF][dim] tagged words: FFN cluster partials
+    uint64_t *amax;              // [grid][2] tagged words: per-CTA argmax candidates
+    int ring_slots;
+    int stage_rows;              // cached positions per CTA copied to shared memory
+    int xs_floats;               // activation tile length
+    // shared-memory offsets (bytes)
+    int off_xraw, off_xs, off_hb, off_qkv, off_st, off_p, off_k, off_v, off_hop, off_gain, off_yv, off_rope, off_utab, off_ring;
+    // the step (one row)
+    int seq, pos;
+    const int *tokens;
+    float *logits;
+    int *next_ids;
+    uint32_t *done_word;
+    int do_logits;
+    uint32_t tag;
+    unsigned long long *trace;
+};
+
 // Cache replication (cache_ops.cu): positions [0, len) of sequence src into dst[0..n).
 struct ForkArgs {
     int dst[kMaxBatch];
