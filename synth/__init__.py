@@ -82,7 +82,9 @@ LLAMA1B = Shape(dim=2048, n_layers=16, n_heads=32, n_kv_heads=8, head_dim=64,
                 hidden=8192, vocab=128256, max_seq=2304, max_batch=8,
                 rope_theta=500000.0, weight_dtype=DTYPE_BF16, kv_dtype=DTYPE_BF16)
 
-# The five workloads.  Step counting: a prompt of P tokens is prefilled, its argmax is
+LONG_2L = LLAMA1B.replace(n_layers=2, hidden=512, vocab=2048, max_batch=4, max_seq=32832)
+
+# The five workloads (plus a reduced long-context one the oracle can finish).  Step counting: a prompt of P tokens is prefilled, its argmax is
 # the first generated token, and every further token costs one decode step.
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", TINY, batch=1, prompt_len=5, decode_steps=7,
@@ -96,6 +98,14 @@ WORKLOADS: Dict[str, Workload] = {
                            decode_steps=256),
     "llama1b_long": Workload("llama1b_long", LLAMA1B.replace(max_batch=4, max_seq=32832),
                              batch=4, prompt_len=32768, decode_steps=64),
+    # The long-context workload's attention at full size with a model small enough for
+    # the oracle to prefill 4 x 32,768 positions offline: the Llama-3.2-1B attention
+    # geometry (32 query heads, 8 kv heads, head_dim 64, dim 2048, theta 500000, bf16
+    # KV) in 2 layers, with a small FFN and vocabulary.
+    "llama1b_long_2l": Workload("llama1b_long_2l", LONG_2L, batch=4, prompt_len=32768,
+                                decode_steps=8,
+                                note="Llama-3.2-1B attention geometry, 2 layers, hidden 512, "
+                                     "vocab 2048: 4 x 32768-token prompts + 8 decode steps"),
 }
 
 

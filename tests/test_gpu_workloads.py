@@ -3,11 +3,14 @@
 The oracle needs too long at these sizes to run inside a test (about half an hour per
 Llama-3.2-1B-shaped row), so `tests/golden/make_goldens.py` (which calls only the
 oracle) stored, per checked row and step, the greedy id, the top-2 gap, max|logit|, the
-top-8 logits and the logits at 64 fixed vocabulary indices.  The GPU runs the whole
+top-8 logits and the logits at 64 fixed vocabulary indices, plus the whole logits
+vector at a few steps (`full_steps`: the prefill, the first, a middle and the last
+decode step).  The GPU runs the whole
 workload -- every row of the batch, full prompt, every decode step, in the launch
 configuration the benchmark uses -- with the checked rows fed the oracle's ids (teacher
 forcing) and the others their own, and is compared on those stored values:
-logits within tol * max|logit| (tol 2e-2: bf16 KV cache), ids equal wherever the
+logits within tol * max|logit| (tol 2e-2: bf16 KV cache) -- over the whole vocabulary
+at the `full_steps`, on the stored values elsewhere -- and ids equal wherever the
 oracle's top-2 gap exceeds 1e-2.
 """
 import functools
@@ -47,12 +50,20 @@ def golden(prefix, row):
     return dict(np.load(path))
 
 
-def check_step(gpu_logits_sampled, gpu_top_vals, gpu_id, g, s, tol, what):
+def check_step(gpu_logits_sampled, gpu_top_vals, gpu_id, g, s, tol, what, gpu_full=None):
     """gpu_logits_sampled: GPU logits at g['sample_idx']; gpu_top_vals: GPU logits at the
-    oracle's top-8 indices."""
+    oracle's top-8 indices; gpu_full: the whole GPU vector, compared element by element
+    when step s is one of the golden's full_steps."""
     scale = float(g["maxabs"][s])
     err = max(float(np.abs(gpu_logits_sampled - g["sampled"][s]).max()),
               float(np.abs(gpu_top_vals - g["top_val"][s]).max()))
+    full = list(g["full_steps"]) if "full_steps" in g else []
+    if s in full:
+        assert gpu_full is not None, f"{what}: the whole vector is needed at step {s}"
+        ref = g["full"][full.index(s)]
+        assert gpu_full.shape == ref.shape
+        assert float(np.abs(ref).max()) == scale
+        err = max(err, float(np.abs(gpu_full.astype(np.float64) - ref.astype(np.float64)).max()))
     assert err <= tol * scale, f"{what}: max|d logit| {err:.3e} > {tol} * {scale:.3e}"
     want = int(g["ids"][s])
     if g["gap"][s] > GAP:
@@ -85,7 +96,7 @@ def run_workload(slm, wl, kind, prefix, checked_rows, shape=None):
         g_id = int(nid.item())
         if r in gold:
             worst = max(worst, check_step(lg[sidx[r]].cpu().numpy(), lg[tidx[r][0]].cpu().numpy(), g_id,
-                                          gold[r], 0, 2e-2, f"{prefix} row {r} prefill"))
+                                          gold[r], 0, 2e-2, f"{prefix} row {r} prefill", lg.cpu().numpy()))
             cur[r] = int(gold[r]["ids"][0])
         else:
             cur[r] = g_id
@@ -96,9 +107,10 @@ def run_workload(slm, wl, kind, prefix, checked_rows, shape=None):
         ids_h = ids.cpu().numpy()
         for i, r in enumerate(seqs):
             if r in gold:
+                full = step + 1 in list(gold[r]["full_steps"])
                 worst = max(worst, check_step(lg[i][sidx[r]].cpu().numpy(), lg[i][tidx[r][step + 1]].cpu().numpy(),
                                               int(ids_h[i]), gold[r], step + 1, 2e-2,
-                                              f"{prefix} row {r} step {step}"))
+                                              f"{prefix} row {r} step {step}", lg[i].cpu().numpy() if full else None))
                 cur[r] = int(gold[r]["ids"][step + 1])
             else:
                 cur[r] = int(ids_h[i])
@@ -184,3 +196,64 @@ def test_llama1b_long_context_workload(slm):
     assert np.abs(step_logits - lg2).max() <= 2e-2 * np.abs(lg2).max()
     assert e2.sync() == 0
     e2.close()
+
+
+@pytest.mark.slow
+def test_long_context_2layer_against_oracle(slm):
+    """4 rows x (32768-token prompt + 8 greedy decode steps) with the Llama-3.2-1B attention
+    geometry (32 query heads, 8 kv heads, head_dim 64, bf16 KV, theta 500000) in a 2-layer
+    model small enough for the oracle to prefill offline (tests/golden/long2l_row*.npz).
+    The prompts go through the batched tensor-core prefill, the steps through the decode
+    kernel's split-K attention over 32k cached positions (long chunks per work item);
+    every logit of every row and step is compared with the oracle's (teacher forcing),
+    ids under the gap rule.  The invariant behind it: cached generation equals the plain
+    recomputation (GOTOken, "About one token per second")."""
+    wl = synth.WORKLOADS["llama1b_long_2l"]
+    s = wl.shape
+    W = synth.make_weights(s)
+    gold = {r: golden("long2l", r) for r in range(wl.batch)}
+    for r, g in gold.items():
+        assert str(g["weights_sha256"]) == synth.digest(W)
+        assert list(g["full_steps"]) == list(range(wl.decode_steps + 1))
+    prompts = [synth.make_prompt(s, r, wl.prompt_len) for r in range(wl.batch)]
+    for r, g in gold.items():
+        assert np.array_equal(g["prompt"], prompts[r])
+    eng = slm.Engine(s, W)
+    dev = torch.device("cuda")
+    toks = torch.as_tensor(np.concatenate(prompts).astype(np.int32), device=dev)
+    last = torch.empty((wl.batch, s.vocab), dtype=torch.float32, device=dev)
+    ids = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+    eng._check(eng.prefill_batch(list(range(wl.batch)), toks, [wl.prompt_len] * wl.batch, last, ids),
+               "slm_prefill_batch")
+    lg0 = last.cpu().numpy()
+    ids0 = ids.cpu().numpy()
+    worst = 0.0
+    for r in range(wl.batch):
+        g = gold[r]
+        worst = max(worst, check_step(lg0[r][g["sample_idx"]], lg0[r][g["top_idx"][0]], int(ids0[r]), g, 0,
+                                      2e-2, f"long2l row {r} prefill", lg0[r]))
+    cur = [int(gold[r]["ids"][0]) for r in range(wl.batch)]
+    for step in range(wl.decode_steps):
+        t = torch.tensor(cur, dtype=torch.int32, device=dev)
+        lg, nid = eng.decode_checked(list(range(wl.batch)), t, [wl.prompt_len + step] * wl.batch, want_logits=True)
+        lgh = lg.cpu().numpy()
+        nidh = nid.cpu().numpy()
+        for r in range(wl.batch):
+            g = gold[r]
+            worst = max(worst, check_step(lgh[r][g["sample_idx"]], lgh[r][g["top_idx"][step + 1]], int(nidh[r]), g,
+                                          step + 1, 2e-2, f"long2l row {r} step {step}", lgh[r]))
+        cur = [int(gold[r]["ids"][step + 1]) for r in range(wl.batch)]
+    assert eng.sync() == 0, eng.last_error()
+    # single rows of the same sequences (the cluster kernel, when it serves this shape)
+    for r in (0, 3):
+        eng.reset(r)
+        lgp, nid = eng.prefill_checked(r, prompts[r], want_logits=True)
+        check_step(lgp.cpu().numpy()[gold[r]["sample_idx"]], lgp.cpu().numpy()[gold[r]["top_idx"][0]],
+                   int(nid.item()), gold[r], 0, 2e-2, f"long2l row {r} single prefill", lgp.cpu().numpy())
+        t = torch.tensor([int(gold[r]["ids"][0])], dtype=torch.int32, device=dev)
+        lg1, nid1 = eng.decode_checked([r], t, [wl.prompt_len], want_logits=True)
+        check_step(lg1[0].cpu().numpy()[gold[r]["sample_idx"]], lg1[0].cpu().numpy()[gold[r]["top_idx"][1]],
+                   int(nid1[0].item()), gold[r], 1, 2e-2, f"long2l row {r} single step", lg1[0].cpu().numpy())
+    assert eng.sync() == 0, eng.last_error()
+    eng.close()
+    assert worst < 2e-2
