@@ -60,6 +60,48 @@ VARIANTS = {
 }
 
 
+SINGLE_ROW_VARIANTS = dict(VARIANTS, fp32_weights_bf16_kv=dict(kv_dtype=synth.DTYPE_BF16))
+
+
+@pytest.mark.parametrize("name", sorted(SINGLE_ROW_VARIANTS))
+def test_shape_variants_single_row(slm, name):
+    """Single-row steps (the cluster kernel: attention clusters per kv head, FFN clusters)
+    on every head geometry, against the oracle, rows decoded one at a time with ragged
+    contexts."""
+    s = synth.TINY.replace(max_batch=3, max_seq=96, **SINGLE_ROW_VARIANTS[name])
+    W = synth.make_weights(s, seed=13)
+    lens = [2, 17, 45]
+    prompts = [synth.make_prompt(s, r, lens[r]) for r in range(3)]
+    steps = 5
+    ref_ids, ref_logits = oracle_reference(s, prompts, steps, [0, 1, 2], seed=13)
+    eng = _engine(slm, s, W)
+    assert eng.cluster_plan() is not None, "single-row steps of this shape should run on the cluster kernel"
+    tol = tolerance(s)
+    dev = torch.device("cuda")
+    for r in range(3):
+        lg, nid = eng.prefill_checked(r, prompts[r], want_logits=True)
+        check_logits(lg.cpu().numpy(), ref_logits[r][0], tol, f"{name} row {r} prefill")
+        check_id(int(nid.item()), ref_logits[r][0], ref_ids[r][0], f"{name} row {r} prefill")
+        for st in range(steps):
+            tok = torch.tensor([ref_ids[r][st]], dtype=torch.int32, device=dev)
+            lg, ids = eng.decode_checked([r], tok, [lens[r] + st], want_logits=True)
+            check_logits(lg[0].cpu().numpy(), ref_logits[r][st + 1], tol, f"{name} row {r} step {st}")
+            check_id(int(ids[0].item()), ref_logits[r][st + 1], ref_ids[r][st + 1], f"{name} row {r} step {st}")
+    assert eng.sync() == 0, eng.last_error()
+    # the appended slots hold the oracle's keys and values
+    o = oracle.Model(s.replace(max_batch=1), W)
+    o.prefill(0, prompts[2])
+    for st in range(steps):
+        o.decode_step([0], [ref_ids[2][st]], [lens[2] + st])
+    for layer in range(s.n_layers):
+        gk, gv = eng.kv(layer, 2)
+        ok, ov = o.kv(layer, 0)
+        atol = (2e-2 if s.kv_dtype == synth.DTYPE_BF16 else 1e-4)
+        assert np.allclose(gk, ok, atol=atol * max(1.0, np.abs(ok).max()))
+        assert np.allclose(gv, ov, atol=atol * max(1.0, np.abs(ov).max()))
+    eng.close()
+
+
 @pytest.mark.parametrize("name", sorted(VARIANTS))
 def test_shape_variants_batched_ragged(slm, name):
     s = synth.TINY.replace(max_batch=3, max_seq=96, **VARIANTS[name])
