@@ -142,6 +142,13 @@ int slm_prefill_batch(slm_ctx *ctx, int32_t nseq, const int32_t *seqs, const int
  *   Row i appends its k, v at slot positions[i]; its length becomes positions[i] + 1.
  *   Asynchronous on `stream` when tokens, logits and next_ids are device memory (the
  *   ids can feed the next step without a device-to-host copy); synchronous otherwise.
+ *   Single-row steps of small models run on the cluster kernel (slm_debug_cluster),
+ *   the others on the persistent kernel; the results are the same computation.
+ *   Device-side faults (a bounded wait ran out, NaN logits, a bad token) set the
+ *   context's status word: every result of that step and of later steps is invalid
+ *   until slm_sync reads and clears it.  A synchronous call (host buffers) reports it
+ *   itself, as SLM_ETIMEOUT or SLM_EDEVICE; an asynchronous call cannot, so check with
+ *   slm_sync.
  */
 int slm_decode_step(slm_ctx *ctx, int32_t batch, const int32_t *seq_ids, const int32_t *tokens,
                     const int32_t *positions, float *logits, int32_t *next_ids, void *stream);
@@ -184,8 +191,13 @@ int slm_fork(slm_ctx *ctx, int32_t src, int32_t n_dst, const int32_t *dst_seqs, 
  *     (index order without top-k), whose running sum of softmax(logit / temperature)
  *     weights exceeds uniforms[row] times their total.
  *   next_ids: device int32[batch].
- *   Asynchronous on `stream` (one kernel launch).  Errors (text in slm_last_error(NULL)):
- *   SLM_EINVAL (NULL or host pointers, sizes, parameters), SLM_ECUDA.
+ *   Asynchronous on `stream`.  With top_k >= 1 over a large vocabulary the rows are
+ *   split over several CTAs, whose candidates are merged through a stream-ordered
+ *   scratch buffer (cudaMallocAsync / cudaFreeAsync on `stream`, up to 32 KB per row); if
+ *   that allocation fails the call falls back to one CTA per row and allocates nothing.
+ *   Callers that must not allocate can pass top_k = 0 (or temperature 0), which never
+ *   allocates.  Errors (text in slm_last_error(NULL)): SLM_EINVAL (NULL or host
+ *   pointers, sizes, parameters), SLM_ECUDA.
  */
 int slm_sample(int32_t batch, int32_t vocab, const float *logits, int32_t ld, float temperature, int32_t top_k,
                float top_p, const float *uniforms, int32_t *next_ids, void *stream);
@@ -231,6 +243,17 @@ int slm_debug_copy_kv(slm_ctx *ctx, int32_t layer, int32_t seq, int32_t n_pos, f
  * error slm_create would return for the plan (text in slm_last_error(NULL)).
  */
 int slm_debug_plan(const slm_config *config, int32_t sms, int32_t *out, int32_t out_len);
+
+/*
+ * slm_debug_faults -- test hook for the failure paths (no page counterpart: the bounded
+ * waits exist so that a lost hand-off ends the step with an error instead of hanging the
+ * GPU).  wait_ns: limit of each bounded device-side wait of the decode kernels from the
+ * next step on (0 restores the default of 1 s); lost_publish = 1 makes one CTA skip one
+ * publish of the first layer's residual in every following step, so that its consumers'
+ * waits run out.  The step then finishes without hanging; its results are invalid and
+ * slm_sync returns SLM_ETIMEOUT (and clears the status).  Returns SLM_OK or SLM_EINVAL.
+ */
+int slm_debug_faults(slm_ctx *ctx, unsigned long long wait_ns, int32_t lost_publish);
 
 /*
  * slm_debug_cluster -- test hook: how this engine runs single-row decode steps.  Returns
@@ -290,7 +313,9 @@ size_t slm_attention_workspace_bytes(int32_t batch, int32_t n_heads, int32_t n_k
  * (flash-decoding).  The query is used as given (RoPE already applied).
  *   q: device fp32 [batch][n_heads][head_dim].
  *   k_cache, v_cache: device [batch][n_kv_heads][capacity][head_dim] of kv_dtype
- *     (SLM_F32 or SLM_BF16); only positions < ctx_len[b] are read.
+ *     (SLM_F32 or SLM_BF16), each 16-byte aligned (rows are read 16 bytes at a time;
+ *     an offset view fails with SLM_EINVAL before anything is launched); only
+ *     positions < ctx_len[b] are read.
  *   ctx_len: host int32[batch], each in [1, capacity].
  *   out: device fp32 [batch][n_heads][head_dim].
  *   workspace: device memory, 256-byte aligned, at least
@@ -319,8 +344,8 @@ int slm_attention_decode(int32_t batch, int32_t n_heads, int32_t n_kv_heads, int
  *   (slm_attention_workspace_bytes) exceeds it fail with SLM_EINVAL and a message.
  *   The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *   routine.  The first call on a device looks up the array's device address (once
- *   per device, with that device current); make that first call before any stream
- *   capture.  Every call shares the array and it keeps the last call's contents: the
+ *   per device, with that device current, and again if the device's context changed
+ *   since, e.g. after cudaDeviceReset); make that first call before any stream capture.  Every call shares the array and it keeps the last call's contents: the
  *   call clears the arrival counters itself, but calls whose work overlaps on the GPU
  *   (e.g. on two unordered streams) race on the array.
  */

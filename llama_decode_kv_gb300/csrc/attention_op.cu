@@ -158,6 +158,8 @@ extern "C" int slm_attention_decode(int32_t batch, int32_t n_heads, int32_t n_kv
         return attn_fail(SLM_EINVAL, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
     if ((uintptr_t)workspace % 256)
         return attn_fail(SLM_EINVAL, "workspace must be 256-byte aligned");
+    if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return attn_fail(SLM_EINVAL, "k_cache and v_cache must be 16-byte aligned (rows are read 16 bytes at a time)");
     P.q = q;
     P.k = (const uint8_t *)k_cache;
     P.v = (const uint8_t *)v_cache;
@@ -178,22 +180,45 @@ static constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 
 static std::mutex g_scratch_mu;
-static void *g_scratch_ptr[64];  // device address of g_attn_scratch, per device ordinal
+static void *g_scratch_ptr[64];  // device address of g_attn_scratch, per device ordinal ...
+static void *g_scratch_ctx[64];  // ... valid for the context it was looked up in
+
+// The context current on this thread (the driver's cuCtxGetCurrent, reached through the
+// runtime), or null.
+static void *current_context() {
+    using GetCurrent = int (*)(void **);
+    static GetCurrent fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return (GetCurrent)f;
+    }();
+    void *ctx = nullptr;
+    if (!fn || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
 
 // The host cannot use g_attn_scratch's name as a device address; look the address up
-// once per device, with that device current.
+// once per device, with that device current, and again whenever the device's context
+// changed since (a reset context reloads the module, and the array may move).
 static int scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return attn_fail(SLM_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return attn_fail(SLM_EUNSUPPORTED, "device ordinal %d above 63", dev);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    void *ctx = current_context();
+    if (!g_scratch_ptr[dev] || !ctx || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_attn_scratch);
         if (e != cudaSuccess || !p)
             return attn_fail(SLM_ECUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = current_context();  // the lookup made the primary context current
     }
     *out = g_scratch_ptr[dev];
     return SLM_OK;
@@ -209,6 +234,8 @@ extern "C" int slm_attention_decode_noalloc(int32_t batch, int32_t n_heads, int3
     if (rc) return rc;
     if (!q || !k_cache || !v_cache || !out)
         return attn_fail(SLM_EINVAL, "q, k_cache, v_cache and out must be non-NULL");
+    if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return attn_fail(SLM_EINVAL, "k_cache and v_cache must be 16-byte aligned (rows are read 16 bytes at a time)");
     size_t need = slm_attention_workspace_bytes(batch, n_heads, n_kv_heads, head_dim);
     if (need > kNoAllocScratchBytes)
         return attn_fail(SLM_EINVAL,

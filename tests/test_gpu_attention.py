@@ -98,3 +98,24 @@ def test_attention_op_rejects_bad_arguments(slm):
     assert b"workspace" in slm.slm_last_error(None)
     assert slm.attention_decode(qd, kd, vd, [3, 2], out, ws, slm.SLM_F32) == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_misaligned_cache_is_refused_before_launch(slm, noalloc):
+    """Cache rows are read 16 bytes at a time: a cache pointer off a 16-byte boundary (an
+    offset view of a larger buffer) is refused with SLM_EINVAL and nothing is launched."""
+    B, H, KV, hd, cap = 1, 4, 2, 16, 8
+    q = torch.zeros((B, H, hd), device="cuda")
+    base = torch.zeros(B * KV * cap * hd + 1, device="cuda")
+    k = base[1:].view(B, KV, cap, hd)  # 4 bytes past an aligned address
+    v = torch.zeros((B, KV, cap, hd), device="cuda")
+    out = torch.full((B, H, hd), 7.0, device="cuda")
+    if noalloc:
+        rc = slm.attention_decode_noalloc(q, k, v, [cap], out, slm.SLM_F32)
+    else:
+        ws = torch.empty(slm.slm_attention_workspace_bytes(B, H, KV, hd), dtype=torch.uint8, device="cuda")
+        rc = slm.attention_decode(q, k, v, [cap], out, ws, slm.SLM_F32)
+    assert rc == slm.SLM_EINVAL
+    assert b"16-byte aligned" in slm.slm_last_error(None)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())

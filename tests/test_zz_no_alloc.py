@@ -5,12 +5,15 @@ all of it up front, or a latency-critical loop that must not call cudaMalloc (it
 synchronise the device).  slm_attention_decode_noalloc serves them: it keeps its split-K
 scratch in a fixed array inside the library.  This file checks it against the
 workspace entry point (slm_attention_decode) through the C ABI, on two calls in a row
-with different shapes, and that a shape too large for the fixed array is refused.
+with different shapes, and directly against the oracle's attention on sampled heads
+(so the check does not rest on the other entry point alone), and that a shape too
+large for the fixed array is refused.
 It is collected last so that a failure here never hides the other tests.
 """
 import numpy as np
 import pytest
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -65,6 +68,19 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(slm):
         assert not np.isnan(got).any()
         scale = float(np.abs(ref).max())
         assert np.allclose(got, ref, rtol=1e-4, atol=2e-5 * scale)
+    # the oracle, on a few (row, head) pairs of each call (q used as given: RoPE applied)
+    rng = np.random.default_rng(3)
+    for (B, H, KV, hd, bf16, lens), (q, k, v), got in zip(CASES, inputs, outs):
+        qh, kh, vh, gh = q.cpu().numpy(), k.cpu().numpy(), v.cpu().numpy(), got.cpu().numpy()
+        if bf16:
+            kh = synth.bf16_to_f32(kh.view(np.uint16))
+            vh = synth.bf16_to_f32(vh.view(np.uint16))
+        for b in range(B):
+            for h in rng.choice(H, 2, replace=False):
+                g = h // (H // KV)
+                want = oracle.attend(qh[b, h], kh[b, g, :lens[b]], vh[b, g, :lens[b]])
+                sc = max(1e-3, float(np.abs(want).max()))
+                assert np.allclose(gh[b, h], want, rtol=1e-4, atol=2e-5 * sc), (b, h)
 
 
 def test_noalloc_refuses_shapes_beyond_its_array(slm):
