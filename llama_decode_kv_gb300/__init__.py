@@ -61,6 +61,7 @@ _SIGS = {
     "slm_debug_trace": (ctypes.c_int, [_P, _I32, _P, ctypes.c_size_t]),
     "slm_debug_plan": (ctypes.c_int, [ctypes.POINTER(slm_config), _I32, _P, _I32]),
     "slm_debug_cluster": (ctypes.c_int, [_P, _P, _I32]),
+    "slm_debug_faults": (ctypes.c_int, [_P, ctypes.c_ulonglong, _I32]),
     "slm_debug_gemm_bf16": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P, _P]),
     "slm_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "slm_attention_decode": (ctypes.c_int, [_I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P,
@@ -236,6 +237,11 @@ class Engine:
         if rc < 0:
             raise SlmError(rc, "slm_debug_copy_kv", self.last_error())
         return k, v
+
+    def debug_faults(self, wait_ns: int = 0, lost_publish: int = 0):
+        """Shorten the device-side wait limit (0: default) and/or make one publish go
+        missing in the following steps (slm_debug_faults)."""
+        self._check(slm_debug_faults(self.ctx, int(wait_ns), int(lost_publish)), "slm_debug_faults")
 
     def cluster_plan(self):
         """None when single-row steps run on the persistent kernel, else a dict of the

@@ -159,7 +159,7 @@ __device__ bool c_wait_slot(const Model &m, uint64_t *bar, uint32_t parity) {
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (ld_volatile_int(m.abort_flag)) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > m.wait_ns) {
             raise_abort(m, kStRingTimeout);
             return false;
         }
@@ -174,7 +174,7 @@ __device__ bool c_wait_xb(const Model &m, uint64_t *bar, uint32_t parity) {
         if (mbar_try_cl(bar, parity)) return true;
         if ((it & 15) == 15) {
             if (ld_volatile_int(m.abort_flag)) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > m.wait_ns) {
                 raise_abort(m, kStExchangeTimeout);
                 return false;
             }
@@ -223,7 +223,7 @@ __device__ bool poll_flat(const ClusterParams &P, const uint64_t *src, int n, in
                     ok = false;
                     break;
                 }
-                if (global_ns() - t0 > kWaitLimitNs) {
+                if (global_ns() - t0 > P.m.wait_ns) {
                     raise_abort(P.m, kStExchangeTimeout);
                     ok = false;
                     break;
@@ -697,7 +697,8 @@ __device__ __forceinline__ void logits_tail(const ClusterParams &P, CS &S, const
         if (lane == 0) {
             if (i == 0x7fffffff) i = 0;  // all NaN, or an aborted step: the status word records it
             if (P.next_ids) P.next_ids[0] = i;
-            if (P.done_word) {
+            if (P.done_word) {  // host-memory ids: tell the host they are complete, with the status
+                ((volatile uint32_t *)P.done_word)[1] = (uint32_t)ld_volatile_int(m.status);
                 __threadfence_system();
                 *(volatile uint32_t *)P.done_word = P.tag;
             }
@@ -712,13 +713,12 @@ __device__ __forceinline__ void logits_tail(const ClusterParams &P, CS &S, const
 // remain; the dot products go to S.yv, a barrier, then one thread per output item runs the
 // epilogue.
 template <bool WBF16, int C>
-__device__ __forceinline__ void compute_cta(const ClusterParams &P, CS &S, const Who &w) {
+__device__ __forceinline__ void compute_cta(const ClusterParams &P, CS &S, const Who &w, Me &me) {
     const Model &m = P.m;
     const int tid = threadIdx.x, L = m.n_layers, dim = m.dim;
     const int hd = m.head_dim, half = hd / 2, G = m.n_heads / m.n_kv_heads;
     const bool perm = m.weight_bf16;
     const uint32_t tag = P.tag;
-    Me me;
     unit_range(dim, C, w.rank, me.b0, me.b1);
     for (int k = 0; k < 4; k++) me.use[k] = 0;
     me.pj = -1;
@@ -894,7 +894,8 @@ __device__ __forceinline__ void compute_cta(const ClusterParams &P, CS &S, const
             {
                 uint64_t *dst = P.p_ffn + ((size_t)l * P.NF + w.c) * dim;
                 const bool res = w.c == 0;
-                for (int t = tid; t < p2.units; t += kComputeThreads) {
+                const bool lost = m.fault && l == 0 && w.c == 0 && w.rank == 0;  // test hook: a lost publish
+                for (int t = tid; t < p2.units && !lost; t += kComputeThreads) {
                     const int row = p2.u0 + t;
                     ll_store(dst + row, res ? S.xraw[row] + S.yv[t] : S.yv[t], tag);
                 }
@@ -952,13 +953,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cluster_kernel(const __gri
     if (tid >= kComputeThreads) {
         if (tid == kComputeThreads) c_producer(P, S, w);
     } else {
-        compute_cta<WBF16, C>(P, S, w);
+        Me me;
+        compute_cta<WBF16, C>(P, S, w, me);
         // An aborted step may leave this thread's cached-row copies in flight: they land
         // in this CTA's shared memory, so it may not exit before they complete.
         asm volatile("cp.async.wait_all;" ::: "memory");
+        if (tid == 0)
+            for (int k = 0; k < 4; k++) S.wbest_i[k] = (int)me.use[k];
     }
-    // No CTA leaves while a peer may still push into its shared memory.
+    // No CTA leaves while a peer may still push into its shared memory: first every CTA
+    // of the cluster has issued its last push; then, in a step that stopped early, each
+    // waits (briefly, bounded) for the pushes of exchanges it armed but did not await;
+    // then all leave together.
     __syncwarp();
+    cluster_sync_all();
+    if (tid == 0) {
+        for (int k = 0; k < 4; k++) {
+            const uint32_t u = (uint32_t)S.wbest_i[k];
+            if (u >= xb_uses(P, w, k)) continue;  // every armed use of this barrier was awaited
+            const unsigned long long t0 = global_ns();
+            while (!mbar_try_cl(&S.xb[k], u & 1))
+                if (global_ns() - t0 > 100000ull) break;  // bytes that were never sent
+        }
+    }
+    __syncthreads();
     cluster_sync_all();
 }
 

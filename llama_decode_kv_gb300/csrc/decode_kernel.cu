@@ -87,7 +87,7 @@ __device__ bool wait_slot(const StepParams &P, uint64_t *bar, uint32_t parity) {
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (ld_volatile_int(P.m.abort_flag)) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > P.m.wait_ns) {
             atomicOr(P.m.status, kStRingTimeout);
             atomicExch(P.m.abort_flag, 1);
             return false;
@@ -183,7 +183,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                 if (it == 0) t0 = global_ns();
                 if ((it & 15) == 15) {  // the abort flag and the clock, every 16 rounds
                     if (ld_volatile_int(P.m.abort_flag)) break;
-                    if (global_ns() - t0 > kWaitLimitNs) {
+                    if (global_ns() - t0 > P.m.wait_ns) {
                         atomicOr(P.m.status, kStExchangeTimeout);
                         atomicExch(P.m.abort_flag, 1);
                         break;
@@ -263,7 +263,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                 if (it == 0) t0 = global_ns();
                 if ((it & 15) == 15) {  // the abort flag and the clock, every 16 rounds
                     if (ld_volatile_int(P.m.abort_flag)) break;
-                    if (global_ns() - t0 > kWaitLimitNs) {
+                    if (global_ns() - t0 > P.m.wait_ns) {
                         atomicOr(P.m.status, kStExchangeTimeout);
                         atomicExch(P.m.abort_flag, 1);
                         break;
@@ -778,6 +778,7 @@ __device__ __forceinline__ Cand group_compute(const StepParams &P, const Mat &M,
         float *own = S.xown + c.b * P.own_ld + c.own;
         const float xn = *own + t;
         *own = xn;
+        if (m.fault && c.dst == m.ll_x + ll_layer(P, 1, m.dim)) return cd;  // test hook: a lost publish
         ll_store(c.dst, xn, tag);
         return cd;
     }
@@ -1236,9 +1237,10 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
                 if (P.next_ids) P.next_ids[b] = bi;
             }
         }
-        if (P.done_word) {  // host-memory ids: tell the host they are complete
+        if (P.done_word) {  // host-memory ids: tell the host they are complete, with the status
             compute_sync();
             if (tid == 0) {
+                ((volatile uint32_t *)P.done_word)[1] = (uint32_t)ld_volatile_int(m.status);
                 __threadfence_system();
                 *(volatile uint32_t *)P.done_word = P.tag;
             }

@@ -288,6 +288,8 @@ static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
     m.norm_eps = cfg->norm_eps;
     m.weight_bf16 = cfg->weight_dtype == SLM_BF16;
     m.kv_bf16 = cfg->kv_dtype == SLM_BF16;
+    m.wait_ns = kWaitLimitNs;
+    m.fault = 0;
 
     // Shared memory of the decode kernel: the activation tile / attention scratch region
     // takes what this shape needs, the weight ring (8 KB slots, a multiple of 8, at
@@ -687,8 +689,10 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         }
     }
     CK(c, cudaMallocHost((void **)&c->h_ids, (size_t)B * 4));
-    CK(c, cudaHostAlloc((void **)&c->h_step, (size_t)(2 * kMaxBatch + 1) * 4, cudaHostAllocMapped));
+    // mapped [host tokens; ids; done word; the device status at the done word]
+    CK(c, cudaHostAlloc((void **)&c->h_step, (size_t)(2 * kMaxBatch + 2) * 4, cudaHostAllocMapped));
     c->h_step[2 * kMaxBatch] = 0;
+    c->h_step[2 * kMaxBatch + 1] = 0;
     CK(c, cudaHostGetDevicePointer((void **)&c->d_step, c->h_step, 0));
     // tensor-core prefill buffers (blocks of up to 2048 prompt positions)
     if (prefill_supported(m)) {
@@ -878,6 +882,21 @@ static int launch(slm_ctx *c, StepParams &P, cudaStream_t s) {
     return SLM_OK;
 }
 
+// After a call with host buffers has waited for its step: a nonzero device status means
+// every result of the step is invalid (a bounded wait ran out, NaN logits or a bad token);
+// the status stays set until slm_sync reads and clears it.
+static int host_status(slm_ctx *c, uint32_t st) {
+    if (st == 0) return SLM_OK;
+    if (st & (kStExchangeTimeout | kStRingTimeout))
+        return fail(c, SLM_ETIMEOUT, "device wait timed out (status 0x%x); results invalid until slm_sync", st);
+    return fail(c, SLM_EDEVICE, "device status 0x%x (NaN logits or token out of range); results invalid until slm_sync", st);
+}
+
+static int read_status(slm_ctx *c, uint32_t *st) {
+    CK(c, cudaMemcpy(st, c->m.status, 4, cudaMemcpyDeviceToHost));
+    return SLM_OK;
+}
+
 extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids, const int32_t *tokens,
                                const int32_t *positions, float *logits, int32_t *next_ids, void *stream) {
     if (!c) return SLM_EINVAL;
@@ -936,11 +955,19 @@ extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids
             if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(3)) break;
         }
         std::atomic_thread_fence(std::memory_order_acquire);
-        if (!seen) CK(c, cudaStreamSynchronize(s));
+        uint32_t st = (uint32_t)c->h_step[2 * kMaxBatch + 1];
+        if (!seen) {
+            CK(c, cudaStreamSynchronize(s));
+            if ((rc = read_status(c, &st))) return rc;
+        }
         memcpy(next_ids, c->h_step + kMaxBatch, (size_t)batch * 4);
+        return host_status(c, st);
     } else if (!tok_dev || !log_dev || !ids_dev) {
         CK(c, cudaStreamSynchronize(s));
         if (!ids_dev) memcpy(next_ids, c->h_step + kMaxBatch, (size_t)batch * 4);
+        uint32_t st = 0;
+        if ((rc = read_status(c, &st))) return rc;
+        return host_status(c, st);
     }
     return SLM_OK;
 }
@@ -1018,6 +1045,9 @@ extern "C" int slm_prefill(slm_ctx *c, int32_t seq, const int32_t *tokens, int32
         if (!tok_dev || !log_dev || !ids_dev) {
             CK(c, cudaStreamSynchronize(s));
             if (!ids_dev) *next_id = c->h_ids[0];
+            uint32_t st = 0;
+            if (int rs = read_status(c, &st)) return rs;
+            return host_status(c, st);
         }
         return SLM_OK;
     }
@@ -1043,6 +1073,10 @@ extern "C" int slm_prefill(slm_ctx *c, int32_t seq, const int32_t *tokens, int32
     if (!tok_dev || !log_dev || !ids_dev) {
         CK(c, cudaStreamSynchronize(s));
         if (!ids_dev) *next_id = c->h_ids[0];
+        uint32_t st = 0;
+        int rc = read_status(c, &st);
+        if (rc) return rc;
+        return host_status(c, st);
     }
     return SLM_OK;
 }
@@ -1167,6 +1201,14 @@ extern "C" int slm_debug_trace(slm_ctx *c, int32_t enable, unsigned long long *o
         CK(c, cudaMemcpy(out_host, c->d_trace, n * 8, cudaMemcpyDeviceToHost));
     }
     return (int)c->grid;
+}
+
+extern "C" int slm_debug_faults(slm_ctx *c, unsigned long long wait_ns, int32_t lost_publish) {
+    if (!c) return SLM_EINVAL;
+    if (lost_publish != 0 && lost_publish != 1) return fail(c, SLM_EINVAL, "lost_publish must be 0 or 1");
+    c->m.wait_ns = wait_ns ? wait_ns : kWaitLimitNs;
+    c->m.fault = lost_publish;
+    return SLM_OK;
 }
 
 extern "C" int slm_debug_cluster(const slm_ctx *c, int32_t *out, int32_t out_len) {

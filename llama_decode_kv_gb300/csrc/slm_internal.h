@@ -84,6 +84,8 @@ struct Model {
     int *part_count;    // [n_layers][max_batch][KV] arrival counters (producer merge)
     int *status;        // device status word
     int *abort_flag;
+    unsigned long long wait_ns;  // limit of one bounded wait (kWaitLimitNs unless a test shortens it)
+    int fault;                   // test hook: 1 = one producer skips one publish (slm_debug_faults)
 };
 
 struct StepParams {
