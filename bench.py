@@ -1,6 +1,8 @@
 #!/usr/bin/env python
-"""Decode benchmark: greedy KV-cached decode on the SmolLM2-135M shape at batch 1 (headline)
-and batch 16 (the `batch16` object of the same line).
+"""Decode benchmark: greedy KV-cached decode on the SmolLM2-135M shape at batch 1 (headline),
+with the other workloads in objects of the same line: SmolLM2 at batch 16 (`batch16`),
+Llama-3.2-1B at batch 1 and 8 after 2048-token prompts and at batch 4 after 32768-token
+prompts (`llama1b_b1`, `llama1b_b8`, `llama1b_long`).
 
 ``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``
 
@@ -36,8 +38,8 @@ UNIT = "tokens/s"
 WORKLOAD = "smol_b1"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "llama_decode_kv_gb300", "csrc", "decode_kernel.cu")
-PROFILE = os.path.join(ROOT, "profiles", "decode_step_kernel.smol_b1.txt")
+KERNEL_SRC = os.path.join(ROOT, "llama_decode_kv_gb300", "csrc", "decode_cluster.cu")
+PROFILE = os.path.join(ROOT, "profiles", "decode_cluster_kernel.smol_b1.txt")
 
 
 def parse_args():
@@ -61,11 +63,52 @@ def peaks():
 
 
 def peaks_tensor():
+    """bf16 tensor peak for a kernel timed inside a long run of launches: the sustained
+    figure (the burst one, or the fallback, when it is missing)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["bf16_tflops"])
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured sustained"
+        return float(d["bf16_tflops"]), "measured burst"
     except Exception:
-        return 1900.0
+        return 1700.0, "fallback sustained"
+
+
+def host_cpu():
+    """CPU model of this host and its logical core count."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                model = line.split(":", 1)[1].strip()
+                break
+        if model is None:
+            r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+            for line in r.stdout.splitlines():
+                if line.startswith("Model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except Exception:
+        pass
+    return {"cpu_model": model or "unknown", "nproc": os.cpu_count()}
+
+
+class pinned_to_core0:
+    """Run the enclosed (single-threaded) oracle pinned to core 0, like taskset -c 0."""
+
+    def __enter__(self):
+        try:
+            self.old = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {0})
+            self.ok = True
+        except Exception:
+            self.ok = False
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            os.sched_setaffinity(0, self.old)
 
 
 def kv_bytes_read(shape, ctx: int) -> int:
@@ -283,22 +326,111 @@ def batch16_measure(slm, torch, W, local: int, warmup: int = 3):
 
 
 def cpu_baseline(shape, W, prompt, budget_s: float):
-    """The oracle, as it stands, on the host: greedy decode steps after the prompt."""
+    """The oracle, as it stands, on the host (pinned to core 0): greedy decode steps
+    after the prompt, the prefill timed per token."""
     import oracle
-    m = oracle.Model(shape, W)
-    _, nid = m.prefill(0, prompt)
-    steps, pos = 0, len(prompt)
-    t0 = time.perf_counter()
-    while True:
-        _, ids = m.decode_step([0], [nid], [pos])
-        nid, pos, steps = int(ids[0]), pos + 1, steps + 1
-        if time.perf_counter() - t0 >= budget_s or pos >= shape.max_seq:
-            break
-    dt = time.perf_counter() - t0
-    m.close()
+    with pinned_to_core0() as pin:
+        m = oracle.Model(shape, W)
+        t0 = time.perf_counter()
+        _, nid = m.prefill(0, prompt)
+        pf_s = time.perf_counter() - t0
+        steps, pos = 0, len(prompt)
+        t0 = time.perf_counter()
+        while True:
+            _, ids = m.decode_step([0], [nid], [pos])
+            nid, pos, steps = int(ids[0]), pos + 1, steps + 1
+            if time.perf_counter() - t0 >= budget_s or pos >= shape.max_seq:
+                break
+        dt = time.perf_counter() - t0
+        m.close()
     return {"value": steps / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "pinned": "core 0" if pin.ok else "not pinned", **host_cpu(),
+            "ms_per_step": dt / steps * 1e3, "ms_per_prefill_token": pf_s / len(prompt) * 1e3,
             "sample": f"{steps} single-threaded oracle decode steps (contexts {len(prompt) + 1}.."
                       f"{pos}) after a {len(prompt)}-token prompt, SmolLM2-135M shape, batch 1"}
+
+
+def oracle_llama_sample(shape, W, n_prompt: int = 3, n_steps: int = 2):
+    """The oracle on the Llama-3.2-1B shape, pinned to core 0: a short prompt and a few
+    decode steps (labelled sampled: the 2048- and 32768-token prefills are far beyond a
+    benchmark's time on one core; per step the weights dominate, about 1.24 GMAC)."""
+    import oracle
+    s = shape.replace(max_batch=1, max_seq=16)
+    with pinned_to_core0() as pin:
+        m = oracle.Model(s, W)
+        prompt = synth.make_prompt(s, 0, n_prompt)
+        t0 = time.perf_counter()
+        _, nid = m.prefill(0, prompt)
+        pf_s = time.perf_counter() - t0
+        pos = n_prompt
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            _, ids = m.decode_step([0], [nid], [pos])
+            nid, pos = int(ids[0]), pos + 1
+        dt = time.perf_counter() - t0
+        m.close()
+    return {"kind": "oracle", "cores": 1, "pinned": "core 0" if pin.ok else "not pinned",
+            "ms_per_step_per_row": dt / n_steps * 1e3, "ms_per_prefill_token": pf_s / n_prompt * 1e3,
+            "sample": f"sampled: {n_steps} decode steps at contexts {n_prompt + 1}..{pos} after a "
+                      f"{n_prompt}-token prompt (not at the workload's context)"}
+
+
+def llama_measure(slm, torch, W, local: int, name: str, steps: int, warmup: int = 3, peak: float = 0.0):
+    """A Llama-3.2-1B workload (bf16 weights and KV cache): every row prefilled with its
+    seeded prompt in one batched tensor-core prefill (timed separately), then `steps`
+    batched greedy decode steps timed with CUDA events.  HBM bytes per step = the
+    weights once + every row's K and V reads at that step's context."""
+    wl = synth.WORKLOADS[name]
+    s, B = wl.shape, wl.batch
+    dev = torch.device("cuda", local)
+    eng = slm.Engine(s, W)
+    rows = list(range(B))
+    prompts = torch.as_tensor(np.concatenate([synth.make_prompt(s, r, wl.prompt_len) for r in rows])).to(dev)
+    toks = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
+    pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    pa.record(torch.cuda.current_stream())
+    rc = eng.prefill_batch(rows, prompts, [wl.prompt_len] * B, None, toks[0])
+    pb.record(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    if rc != 0:
+        raise RuntimeError(f"{name} prefill: {eng.last_error()}")
+    pf_ms = pa.elapsed_time(pb)
+    state = {"pos": wl.prompt_len, "cur": 0, "ctx": []}
+
+    def step():
+        c = state["cur"]
+        if eng.decode_step(rows, toks[c], [state["pos"]] * B, None, toks[1 - c]) != 0:
+            raise RuntimeError(f"{name} decode: {eng.last_error()}")
+        state["ctx"].append(state["pos"] + 1)
+        state["pos"] += 1
+        state["cur"] = 1 - c
+
+    for _ in range(warmup):
+        step()
+    state["ctx"].clear()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if eng.sync() != 0:
+        raise RuntimeError(f"device status after {name}: {eng.last_error()}")
+    eng.close()
+    bytes_step = sum(synth.weight_bytes(s) + B * kv_bytes_read(s, c) for c in state["ctx"]) / steps
+    gbs = bytes_step / (ms / 1e3 / steps) / 1e9
+    pf_tokens = B * wl.prompt_len
+    return {"workload": f"{name}: Llama-3.2-1B shape (dim 2048, 16 layers, 32/8 heads, hidden 8192, vocab "
+                        f"128256), bf16 weights and KV cache, {B} x {wl.prompt_len}-token prompt, greedy decode",
+            "tokens_per_s": B * steps / (ms / 1e3), "ms_per_step": ms / steps, "steps": steps, "warmup": warmup,
+            "contexts": [min(state["ctx"]), max(state["ctx"])], "bytes_per_step": bytes_step,
+            "hbm_gbs": gbs, "roofline_frac": gbs / peak if peak else None, "peak_gbs": peak,
+            "prefill": {"call": f"slm_prefill_batch, {B} x {wl.prompt_len} tokens", "ms": pf_ms,
+                        "tokens_per_s": pf_tokens / (pf_ms / 1e3)}}
 
 
 def run_reference(args, world, rank):
@@ -431,10 +563,16 @@ def run_ours(args, world, rank, local):
     e2e_value = e2e_steps * wl.batch * world / e2e_s
 
     pf_t, pf_flops = prefill_measure(slm, torch, W, local)
-    tflops_peak = peaks_tensor()
+    tflops_peak, tflops_kind = peaks_tensor()
     b16 = batch16_measure(slm, torch, W, local)
     b16["roofline_frac"] = b16["hbm_gbs"] / peak
     b16["peak_gbs"] = peak
+    cluster = eng.cluster_plan()
+    eng.close()
+    del W
+    W_llama = synth.make_weights(synth.LLAMA1B)
+    llama = {n: llama_measure(slm, torch, W_llama, local, n, st, peak=peak)
+             for n, st in (("llama1b_b1", 64), ("llama1b_b8", 64), ("llama1b_long", 32))}
 
     if rank != 0:
         return
@@ -459,20 +597,26 @@ def run_ours(args, world, rank, local):
         "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_step_kernel", "peak_kind": peak_kind},
+                     "kernel": "decode_cluster_kernel" if cluster else "decode_step_kernel",
+                     "peak_kind": peak_kind},
+        "kernel_plan": cluster,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 4 * wl.batch,
                 "d2h_bytes_per_step": 4 * wl.batch},
         "gpu_launches": args.steps,
         "prefill": {"workload": "512-token prompt, same SmolLM2-135M-shaped weights, bf16 KV cache",
                     "tokens_per_s": 512 / pf_t, "ms": pf_t * 1e3,
-                    "tflops": pf_flops / pf_t / 1e12, "peak_tflops": tflops_peak,
+                    "tflops": pf_flops / pf_t / 1e12, "peak_tflops": tflops_peak, "peak_kind": tflops_kind,
                     "frac": pf_flops / pf_t / 1e12 / tflops_peak, "bound": "tensor",
                     "note": "activation operands split into bf16 hi + lo: the tensor cores execute 2x these FLOPs"},
         "batch16": b16,
+        **llama,
         "clocks": clk,
     }
     if world == 1:
-        line["cpu_baseline"] = cpu_baseline(s, W, prompt, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(s, synth.make_weights(s), prompt, args.cpu_budget)
+        lo = oracle_llama_sample(synth.LLAMA1B, W_llama)
+        for n in llama:
+            line[n]["cpu_baseline"] = lo
     print(json.dumps(line), flush=True)
 
 

@@ -1014,21 +1014,25 @@ cudaError_t cluster_capacity(int weight_bf16, size_t smem, int C, int *clusters)
     return cudaOccupancyMaxActiveClusters(clusters, cluster_fn(weight_bf16, C), &cfg);
 }
 
+// The CTAs wait on each other, so all of them must be resident at once: the grid is the
+// number of clusters the occupancy API reports resident together (one CTA per SM), on a
+// GPU this process has to itself.  Should some cluster not be scheduled, its peers'
+// bounded waits end the step with a timeout status instead of a hang.  (A cooperative
+// launch would state the guarantee, but Nsight Compute fails to launch cooperative
+// cluster kernels; the plain cluster launch profiles normally.)
 cudaError_t launch_decode_cluster(const ClusterParams &P, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[2];
+    cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)P.C;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
-    at[1].id = cudaLaunchAttributeCooperative;  // every CTA resident at once (they wait on each other)
-    at[1].val.cooperative = 1;
     cfg.gridDim = dim3((unsigned)P.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = at;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     void *args[] = {(void *)&P};
     return cudaLaunchKernelExC(&cfg, cluster_fn(P.m.weight_bf16, P.C), args);
 }
