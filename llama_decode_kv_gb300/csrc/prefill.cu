@@ -1,18 +1,24 @@
-// prefill.cu -- tensor-core prefill of one sequence's prompt.
+// prefill.cu -- tensor-core prefill of the prompts of one or several sequences.
 //
-// The prompt is processed in blocks of up to `rows` positions.  Per block and layer:
-//   xn  = rmsnorm(x) as bf16                       (one CTA per row)
-//   qkv = xn . Wqkv^T                              (tcgen05 GEMM, fp32 out)
-//   RoPE of q and k; k, v appended to the cache    (positions p0 .. p0 + T - 1)
-//   o   = causal GQA attention, as bf16            (flash-style, CUDA cores, fp32 math)
-//   x  += o . Wo^T                                 (GEMM, residual epilogue)
-//   xn  = rmsnorm(x) as bf16
-//   h   = silu(xn . W1^T) * (xn . W3^T) as bf16    (GEMM, SwiGLU epilogue on interleaved rows)
-//   x  += h . W2^T                                 (GEMM, residual epilogue)
-// and finally the logits of the last position (GEMM with the tied embedding) and its
-// argmax.  The block equations are those of the decode step (kasahare 0.4.0 /
-// simple-llm, "Architecture"); the GEMM operands are bf16 (weights as stored,
-// activations rounded), accumulation fp32, the residual stream fp32.
+// The prompt positions are processed in blocks of up to `rows` positions (a block may
+// hold the prompts of several sequences: a segment table maps rows to sequences).  Per
+// block and layer:
+//   xn  = rmsnorm(x), as two bf16 planes hi + lo (x ~ hi + lo to ~16 mantissa bits)
+//   qkv = xn . Wqkv^T                               (tcgen05 GEMM: bf16 weights x the hi
+//                                                    and the lo plane, fp32 accumulation)
+//   RoPE of q and k; k, v appended to the cache     (positions p0 .. p0 + T - 1)
+//   o   = causal GQA attention                      (flash-style on the tensor cores:
+//                                                    mma.sync bf16 QK^T and PV, fp32
+//                                                    online softmax), as hi + lo planes
+//   x  += o . Wo^T                                  (GEMM, residual epilogue)
+//   xn  = rmsnorm(x) as hi + lo planes
+//   h   = silu(xn . W1^T) * (xn . W3^T)             (GEMM, SwiGLU epilogue on interleaved
+//                                                    rows), as hi + lo planes
+//   x  += h . W2^T                                  (GEMM, residual epilogue)
+// and finally the logits of each sequence's last position (GEMM with the tied
+// embedding) and its argmax.  The block equations are those of the decode step
+// (kasahare 0.4.0 / simple-llm, "Architecture"); weights enter as stored (bf16), the
+// residual stream and every accumulation are fp32.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
