@@ -185,8 +185,8 @@ __device__ bool c_wait_xb(const Model &m, uint64_t *bar, uint32_t parity) {
 // Poll n tagged words (item e: src[(e / len) * src_ld + e % len]) into dst[e] until every
 // tag equals the launch's; each thread keeps up to kPollBatch loads in flight.  Returns
 // false if the wait ran out or another CTA aborted.  No barrier.
+template <int K = 8>
 __device__ bool poll_flat(const ClusterParams &P, const uint64_t *src, int n, int len, int src_ld, float *dst) {
-    constexpr int K = 8;
     const int tid = threadIdx.x;
     const uint32_t tag = P.tag;
     bool ok = true;
@@ -430,6 +430,20 @@ __device__ __forceinline__ float norm_stage(const ClusterParams &P, CS &S, int k
     return 1.0f / sqrtf(t / (float)m.dim + m.norm_eps);
 }
 
+// The residual x = the sum of nsrc partial vectors (tagged words src[s * dim + j]), summed
+// in source order into xraw.  Ends with a barrier; uniform result.
+__device__ __forceinline__ bool hop_full(const ClusterParams &P, CS &S, const uint64_t *src, int nsrc) {
+    const int dim = P.m.dim;
+    if (compute_any(!poll_flat(P, src, nsrc * dim, dim, dim, S.hop))) return false;
+    for (int j = threadIdx.x; j < dim; j += kComputeThreads) {
+        float v = 0.f;
+        for (int s = 0; s < nsrc; s++) v += S.hop[s * dim + j];  // source order: fixed
+        S.xraw[j] = v;
+    }
+    compute_sync();
+    return true;
+}
+
 // Column block [b0, b1) of the sum of nsrc partial vectors (tagged words src[s * dim + j])
 // pushed to every CTA of the cluster (xraw, barrier XB_X).
 template <int C>
@@ -656,8 +670,8 @@ __device__ __forceinline__ void better(float v, int i, float &bv, int &bi) {
     }
 }
 
-// The logits of this CTA's vocabulary rows (from S.yv), the per-CTA argmax candidate;
-// CTA 0 reduces the grid's candidates and writes the id.
+// The logits of this CTA's vocabulary rows (from S.yv) and the greedy argmax over the
+// grid (lowest index on ties).
 __device__ __forceinline__ void logits_tail(const ClusterParams &P, CS &S, const Phase &ph, float rs) {
     const Model &m = P.m;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -679,30 +693,30 @@ __device__ __forceinline__ void logits_tail(const ClusterParams &P, CS &S, const
         S.wbest_i[warp] = bi;
     }
     compute_sync();
-    if (tid == 0) {
-        float v = -INFINITY;
-        int i = 0x7fffffff;
-        for (int w = 0; w < kComputeWarps; w++) better(S.wbest_v[w], S.wbest_i[w], v, i);
-        ll_store(P.amax + (size_t)blockIdx.x * 2, v, P.tag);
-        ll_store(P.amax + (size_t)blockIdx.x * 2 + 1, __int_as_float(i), P.tag);
+    if (tid != 0) return;
+    float v = -INFINITY;
+    int i = 0x7fffffff;
+    for (int w = 0; w < kComputeWarps; w++) better(S.wbest_v[w], S.wbest_i[w], v, i);
+    // The grid's best: one 64-bit atomicMax of (order-preserving bits of the value, ~index)
+    // per CTA (larger value wins, then the lower index); the last CTA to arrive writes
+    // the id and resets the two words for the next step.
+    unsigned long long *best = (unsigned long long *)P.amax, *count = best + 1;
+    if (i != 0x7fffffff) {
+        const uint32_t b = __float_as_uint(v), ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+        atomicMax(best, ((unsigned long long)ord << 32) | (unsigned long long)(0xffffffffu - (uint32_t)i));
     }
-    if (blockIdx.x != 0) return;
-    const bool ok = !compute_any(!poll_flat(P, P.amax, P.grid * 2, P.grid * 2, 0, S.hop));
-    if (warp == 0) {
-        float v = -INFINITY;
-        int i = 0x7fffffff;
-        for (int c = lane; ok && c < P.grid; c += 32) better(S.hop[2 * c], __float_as_int(S.hop[2 * c + 1]), v, i);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) better(__shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o), v, i);
-        if (lane == 0) {
-            if (i == 0x7fffffff) i = 0;  // all NaN, or an aborted step: the status word records it
-            if (P.next_ids) P.next_ids[0] = i;
-            if (P.done_word) {  // host-memory ids: tell the host they are complete, with the status
-                ((volatile uint32_t *)P.done_word)[1] = (uint32_t)ld_volatile_int(m.status);
-                __threadfence_system();
-                *(volatile uint32_t *)P.done_word = P.tag;
-            }
-        }
+    __threadfence();
+    if (atomicAdd(count, 1ull) != (unsigned long long)(P.grid - 1)) return;
+    __threadfence();
+    const unsigned long long key = atomicAdd(best, 0ull);
+    const int id = key ? (int)(0xffffffffu - (uint32_t)(key & 0xffffffffu)) : 0;  // none: all NaN (status records it)
+    *(volatile unsigned long long *)best = 0ull;
+    *(volatile unsigned long long *)count = 0ull;
+    if (P.next_ids) P.next_ids[0] = id;
+    if (P.done_word) {  // host-memory ids: tell the host they are complete, with the status
+        ((volatile uint32_t *)P.done_word)[1] = (uint32_t)ld_volatile_int(m.status);
+        __threadfence_system();
+        *(volatile uint32_t *)P.done_word = P.tag;
     }
 }
 
@@ -856,16 +870,8 @@ __device__ __forceinline__ void compute_cta(const ClusterParams &P, CS &S, const
             Walk<WBF16> wk;
             walk_begin<WBF16>(P, S, p13, chunk, m.w13.KBp, wk);
             load_gain(P, S, m.norms + (size_t)l * 2 * dim + dim);
-            {  // x after the attention block: the sum of the NA partials, in cluster order
-                const uint64_t *src = P.p_att + (size_t)l * P.NA * dim;
-                if (compute_any(!poll_flat(P, src, P.NA * dim, dim, dim, S.hop))) return;
-                for (int j = tid; j < dim; j += kComputeThreads) {
-                    float v = 0.f;
-                    for (int s = 0; s < P.NA; s++) v += S.hop[s * dim + j];
-                    S.xraw[j] = v;
-                }
-                compute_sync();
-            }
+            // x after the attention block: the sum of the NA partials, in cluster order
+            if (!hop_full(P, S, P.p_att + (size_t)l * P.NA * dim, P.NA)) return;
             rs = norm_stage(P, S, m.w13.KBp);
             c_trace(P, l * kTracePerLayer + 3, 1);
             walk_run<WBF16>(P, S, p13, chunk, S.xs, m.w13.KBp, wk);

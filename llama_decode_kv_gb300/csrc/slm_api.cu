@@ -449,9 +449,8 @@ static void plan_cluster(slm_ctx *c, int clusters, int C, std::string &why) {
     P.off_p = take((size_t)G * tcap * 4);
     P.off_k = take((size_t)P.stage_rows * (hd * kvesz + 16));
     P.off_v = take((size_t)P.stage_rows * (hd * kvesz + 16));
-    const size_t blk = (size_t)(dim + C - 1) / C;
-    P.off_hop = take(std::max({(size_t)P.NF * blk, (size_t)P.NA * dim, (size_t)2 * P.grid,
-                               (size_t)m.emb.KBp * esz / 4}) * 4);  // also the staged embedding row
+    const size_t blk = (size_t)(dim + C - 1) / C;  // Wo / W2 rows per CTA
+    P.off_hop = take(std::max((size_t)P.NF * blk, (size_t)P.NA * dim) * 4);  // polled partials
     P.off_gain = take((size_t)dim * 4);
     // dot products of the largest slice (or the attention's weighted values)
     const size_t yv = std::max({(size_t)2 * (((G + 2) * hd / 2 + C - 1) / C), blk, (size_t)2 * ((P.hpc + C - 1) / C),
@@ -681,7 +680,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         } cb[] = {
             {(void **)&cp.p_att, Lz * cp.NA * dim * 8},
             {(void **)&cp.p_ffn, Lz * cp.NF * dim * 8},
-            {(void **)&cp.amax, (size_t)cp.grid * 2 * 8},
+            {(void **)&cp.amax, 2 * 8},  // argmax: best (value, index) word, arrival count
         };
         for (auto &b : cb) {
             if ((rc = dev_alloc(c, b.dst, b.bytes))) return rc;
@@ -1164,6 +1163,7 @@ extern "C" int slm_sync(slm_ctx *c, void *stream) {
     CK(c, cudaMemset(c->m.status, 0, 4));
     CK(c, cudaMemset(c->m.abort_flag, 0, 4));
     CK(c, cudaMemset(c->m.part_count, 0, (size_t)c->cfg.n_layers * c->cfg.max_batch * c->cfg.n_kv_heads * 4));
+    if (c->cl_on) CK(c, cudaMemset(c->cp.amax, 0, 2 * 8));  // an aborted step's argmax words
     CK(c, cudaDeviceSynchronize());
     if (st & (kStExchangeTimeout | kStRingTimeout))
         return fail(c, SLM_ETIMEOUT, "device wait timed out (status 0x%x)", st);

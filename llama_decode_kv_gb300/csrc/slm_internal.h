@@ -175,7 +175,7 @@ struct ClusterParams {
     int upc_qkv, upc_wo, upc_w13, upc_w2, upc_emb;  // work units per ring chunk, per phase
     uint64_t *p_att;             // [n_layers][NA][dim] tagged words: attention cluster partials
     uint64_t *p_ffn;             // [n_layers][NF][dim] tagged words: FFN cluster partials
-    uint64_t *amax;              // [grid][2] tagged words: per-CTA argmax candidates
+    uint64_t *amax;              // [2]: the grid's best (value, index) key and the CTAs' arrival count
     int ring_slots;
     int stage_rows;              // cached positions per CTA copied to shared memory
     int xs_floats;               // activation tile length
