@@ -14,20 +14,6 @@
 
 namespace slm {
 
-// Eight consecutive elements of a cached key or value row (global or shared memory).
-__device__ __forceinline__ void load8(const uint8_t *row, int d0, bool kvbf16, float (&v)[8]) {
-    if (kvbf16) {
-        uint4 u = *(const uint4 *)(row + d0 * 2);
-        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-        v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
-    } else {
-        float4 a = *(const float4 *)(row + d0 * 4);
-        float4 b = *(const float4 *)(row + d0 * 4 + 16);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-}
-
 __device__ __forceinline__ float kv_round(float v, bool bf16) {
     return bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
 }
@@ -58,6 +44,8 @@ struct AttnTask {
     const uint8_t *tail_k;       // position tail_t is read from these rows instead (the
     const uint8_t *tail_v;       //   step's own key and value); tail_t = -1: none
     int tail_t;
+    uint8_t *stream;             // if set: shared memory for the streamed read of a chunk
+    int stream_bytes;            //   in global memory (kAttnMaxSlots passes per warp at most)
     float *out;                  // final output rows: head j at out + j * hd
     float *part;                 // partials: head j, chunk c at (j * kMaxChunksPerSeq + c) * (hd + 2)
     int *counter;                // arrivals of this (row, kv head)'s chunks
@@ -69,15 +57,200 @@ struct AttnTask {
     int hd, G, t0, t1, nc, c;
 };
 
+// Eight consecutive elements of a cached key or value row (global or shared memory).
+template <bool BF16>
+__device__ __forceinline__ void load_row8(const uint8_t *row, int d0, float (&v)[8]) {
+    if (BF16) {
+        const uint4 u = *(const uint4 *)(row + d0 * 2);
+        v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+        v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+    } else {
+        const float4 a = *(const float4 *)(row + d0 * 4);
+        const float4 b = *(const float4 *)(row + d0 * 4 + 16);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// 2^x by the SFU instruction (PTX ex2.approx.ftz: relative error about 2^-22, inputs
+// below -126 give 0); softmax weights need no more.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// This warp's positions of one item: pass k takes positions t0 + (k * warps + warp) * PP
+// ..., one per lane group of LPP lanes (each lane 8 of the head_dim elements).  Every
+// pass scores the position against kMaxGroupPass query heads (heads past the group have
+// q = 0 and are ignored by the caller) and folds it into each head's online softmax:
+// the sums are rescaled only when the running max grows.
+//
+// SPLIT (LPP >= 4): the lane group's reduction of the four partial scores also hands
+// out the heads: after two exchange rounds each quarter of the group holds one head's
+// partial sums (head 2a + b for the lanes whose sub index has bits a = LPP/2, b = LPP/4),
+// the remaining rounds finish that head's score, and each lane runs the softmax update
+// of its one head; the weights (and, when a max grew, the rescale factors) are then
+// broadcast to the group for the weighted sum of V, which every lane keeps for all heads
+// on its 8 elements.  Otherwise every lane reduces and updates all four heads.
+//
+// Streamed (T.stream with room for at least two passes per warp): the warp's K and V
+// rows of pass k are copied into slot k % S of its own shared-memory ring S - 1 passes
+// ahead, so that each warp keeps S - 1 passes in flight (a long chunk read straight from
+// the cache is bound by load latency).  Only cached rows [t0, tail) are copied; the new
+// position is read from the tail rows.  Otherwise the rows are read where kbase / vbase
+// point (the cache, or a whole-chunk copy in shared memory).
+template <bool BF16, bool SPLIT>
+__device__ __forceinline__ void attn_scan(const AttnTask &T, const float (&qv)[kMaxGroupPass][8],
+                                          float (&mx)[kMaxGroupPass], float (&ls)[kMaxGroupPass],
+                                          float (&o)[kMaxGroupPass][8], int warp, int lane, int LPP, int PP,
+                                          int grp, bool lane_on, int d0) {
+    static_assert(kMaxGroupPass == 4, "the head split hands out four heads");
+    const int rowbytes = T.hd * (BF16 ? 2 : 4);
+    const int t0 = T.t0, t1 = T.t1;
+    const int stride = kComputeWarps * PP;     // positions of one pass of all warps
+    const int slotb = 2 * PP * rowbytes;       // one warp's K and V rows of one pass
+    const int per_warp = T.stream ? T.stream_bytes / kComputeWarps / 16 * 16 : 0;
+    const int S = min(kAttnMaxSlots, per_warp / slotb);
+    const bool streamed = S >= 2;
+    uint8_t *ring = T.stream + (size_t)warp * per_warp;
+    const int tc = T.tail_t >= 0 ? min(t1, T.tail_t) : t1;
+    const int npass = (t1 - t0 + stride - 1) / stride;
+    const int rows16 = rowbytes / 16;
+    // head split: this lane's head, and the lane of its group that owns head h
+    const int sub = lane & (LPP - 1), base = lane - sub;
+    const bool bitA = SPLIT && (sub & (LPP >> 1)), bitB = SPLIT && (sub & (LPP >> 2));
+    auto owner = [&](int h) { return base + (h >> 1) * (LPP >> 1) + (h & 1) * (LPP >> 2); };
+    float m_own = -INFINITY, l_own = 0.f;
+    int wr = 0, rd = 0;  // ring slots of the next copy and of the next pass
+    auto issue = [&](int k) {
+        if (k < npass) {
+            const int p0 = t0 + k * stride + warp * PP;
+            const int n = max(0, min(PP, tc - p0)) * rows16;  // 16-byte pieces
+            uint8_t *dst = ring + (size_t)wr * slotb;
+            const size_t src = (size_t)p0 * rowbytes;
+            for (int e = lane; e < n; e += 32) {
+                cp_async16(dst + e * 16, T.kbase + src + e * 16);
+                cp_async16(dst + PP * rowbytes + e * 16, T.vbase + src + e * 16);
+            }
+        }
+        cp_async_commit();  // empty groups too: every lane counts the same groups
+        wr = wr + 1 == S ? 0 : wr + 1;
+    };
+    if (streamed)
+        for (int k = 0; k < S - 1; k++) issue(k);
+    for (int k = 0; k < npass; k++) {
+        const int p0 = t0 + k * stride + warp * PP;
+        const uint8_t *kr, *vr;
+        if (streamed) {
+            issue(k + S - 1);
+            cp_async_wait_upto(S - 1);  // this lane's copies of pass k have landed
+            __syncwarp();               // ... and every lane's
+            kr = ring + (size_t)rd * slotb;
+            vr = kr + PP * rowbytes;
+            rd = rd + 1 == S ? 0 : rd + 1;
+        } else {
+            kr = T.kbase + (size_t)p0 * rowbytes;
+            vr = T.vbase + (size_t)p0 * rowbytes;
+        }
+        const int t = p0 + grp;
+        const bool valid = t < t1;
+        float kv8[8], vv8[8];
+        if (valid && lane_on) {
+            const bool tl = t == T.tail_t;
+            load_row8<BF16>(tl ? T.tail_k : kr + grp * rowbytes, d0, kv8);
+            load_row8<BF16>(tl ? T.tail_v : vr + grp * rowbytes, d0, vv8);
+        } else {
+#pragma unroll
+            for (int d = 0; d < 8; d++) kv8[d] = vv8[d] = 0.f;
+        }
+        float s[kMaxGroupPass];
+#pragma unroll
+        for (int j = 0; j < kMaxGroupPass; j++) {
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int d = 0; d < 8; d += 2) {
+                a = fmaf(qv[j][d], kv8[d], a);
+                b = fmaf(qv[j][d + 1], kv8[d + 1], b);
+            }
+            s[j] = a + b;
+        }
+        if (SPLIT) {
+            float k0 = bitA ? s[2] : s[0], k1 = bitA ? s[3] : s[1];
+            k0 += __shfl_xor_sync(0xffffffffu, bitA ? s[0] : s[2], LPP >> 1);
+            k1 += __shfl_xor_sync(0xffffffffu, bitA ? s[1] : s[3], LPP >> 1);
+            float sc = (bitB ? k1 : k0) + __shfl_xor_sync(0xffffffffu, bitB ? k0 : k1, LPP >> 2);
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1)
+                if (off < (LPP >> 2)) sc += __shfl_xor_sync(0xffffffffu, sc, off);  // uniform
+            float corr = 1.f, p = 0.f;
+            if (valid) {
+                if (sc > m_own) {  // a new running max (always at the first position)
+                    corr = fast_exp2(m_own - sc);
+                    l_own *= corr;
+                    m_own = sc;
+                }
+                p = fast_exp2(sc - m_own);
+                l_own += p;
+            }
+            if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < kMaxGroupPass; j++) {
+                    const float cj = __shfl_sync(0xffffffffu, corr, owner(j));
+#pragma unroll
+                    for (int d = 0; d < 8; d++) o[j][d] *= cj;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kMaxGroupPass; j++) {
+                const float pj = __shfl_sync(0xffffffffu, p, owner(j));
+#pragma unroll
+                for (int d = 0; d < 8; d++) o[j][d] = fmaf(pj, vv8[d], o[j][d]);
+            }
+        } else {
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                if (off < LPP) {  // uniform across the warp
+#pragma unroll
+                    for (int j = 0; j < kMaxGroupPass; j++) s[j] += __shfl_xor_sync(0xffffffffu, s[j], off);
+                }
+            }
+            if (valid) {
+#pragma unroll
+                for (int j = 0; j < kMaxGroupPass; j++) {
+                    if (s[j] > mx[j]) {  // a new running max (always at the first position)
+                        const float corr = fast_exp2(mx[j] - s[j]);
+                        ls[j] *= corr;
+#pragma unroll
+                        for (int d = 0; d < 8; d++) o[j][d] *= corr;
+                        mx[j] = s[j];
+                    }
+                    const float p = fast_exp2(s[j] - mx[j]);
+                    ls[j] += p;
+#pragma unroll
+                    for (int d = 0; d < 8; d++) o[j][d] = fmaf(p, vv8[d], o[j][d]);
+                }
+            }
+        }
+        if (streamed) __syncwarp();  // the slot just read is refilled by the next pass
+    }
+    if (streamed) cp_async_wait_upto(0);
+    if (SPLIT) {  // every lane of the group takes each head's (max, sum) from its owner
+#pragma unroll
+        for (int j = 0; j < kMaxGroupPass; j++) {
+            mx[j] = __shfl_sync(0xffffffffu, m_own, owner(j));
+            ls[j] = __shfl_sync(0xffffffffu, l_own, owner(j));
+        }
+    }
+}
+
 // All kComputeThreads threads of the CTA call this.  `scratch` holds
 // kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) floats; `flag` one int.
 __device__ __forceinline__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hd = T.hd, G = T.G;
-    const int t0 = T.t0, t1 = T.t1, nc = T.nc, c = T.c;
+    const int nc = T.nc, c = T.c;
     const bool kvbf16 = T.kv_bf16;
-    const size_t rowbytes = (size_t)hd * (kvbf16 ? 2 : 4);
-    const uint8_t *kbase = T.kbase, *vbase = T.vbase;
     const float qscale = rsqrtf((float)hd) * 1.4426950408889634f;  // scores in log2 units
     float *qs = scratch;
     float *ws = scratch + kMaxGroupPass * hd;
@@ -111,36 +284,12 @@ __device__ __forceinline__ void attn_core(const AttnTask &T, float *scratch, int
 #pragma unroll
             for (int d = 0; d < 8; d++) o[j][d] = 0.f;
         }
-        for (int tb = t0 + warp * PP; tb < t1; tb += kComputeWarps * PP) {
-            const int t = tb + grp;
-            const bool valid = t < t1;
-            float kv8[8], vv8[8];
-            if (valid && lane_on) {
-                const bool tl = t == T.tail_t;
-                load8(tl ? T.tail_k : kbase + (size_t)t * rowbytes, d0, kvbf16, kv8);
-                load8(tl ? T.tail_v : vbase + (size_t)t * rowbytes, d0, kvbf16, vv8);
-            } else {
-#pragma unroll
-                for (int d = 0; d < 8; d++) kv8[d] = vv8[d] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < kMaxGroupPass; j++) {
-                if (j >= Gp) break;
-                float s = 0.f;
-#pragma unroll
-                for (int d = 0; d < 8; d++) s = fmaf(qv[j][d], kv8[d], s);
-                for (int off = 1; off < LPP; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (valid) {
-                    float mn = fmaxf(mx[j], s);
-                    float corr = exp2f(mx[j] - mn);  // exp2(-inf) = 0 on the first position
-                    float p = exp2f(s - mn);
-                    ls[j] = ls[j] * corr + p;
-#pragma unroll
-                    for (int d = 0; d < 8; d++) o[j][d] = fmaf(p, vv8[d], o[j][d] * corr);
-                    mx[j] = mn;
-                }
-            }
-        }
+        if (kvbf16 && LPP >= 4)
+            attn_scan<true, true>(T, qv, mx, ls, o, warp, lane, LPP, PP, grp, lane_on, d0);
+        else if (kvbf16)
+            attn_scan<true, false>(T, qv, mx, ls, o, warp, lane, LPP, PP, grp, lane_on, d0);
+        else
+            attn_scan<false, false>(T, qv, mx, ls, o, warp, lane, LPP, PP, grp, lane_on, d0);
         // merge the position groups of this warp (lanes with the same `sub`)
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++) {

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kComputeThreads) attention_decode_kernel(const
     T.kv_bf16 = KVBF16;
     T.tail_k = T.tail_v = nullptr;
     T.tail_t = -1;
+    T.stream = nullptr;
+    T.stream_bytes = 0;
     T.kbase = P.k + ((size_t)b * P.KV + g) * P.cap * rowbytes;
     T.vbase = P.v + ((size_t)b * P.KV + g) * P.cap * rowbytes;
     T.out = P.out + ((size_t)b * P.H + (size_t)g * G) * hd;

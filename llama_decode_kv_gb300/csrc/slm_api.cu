@@ -38,7 +38,8 @@ struct slm_ctx {
     int device = 0;
     int grid = 0;
     size_t smem = 0;
-    int ring_slots = 0, xs_bytes = 0, attn_stage = 0;
+    int ring_slots = 0, xs_bytes = 0, xs_plan = 0, attn_stage = 0;
+    int attn_chunk_min = 0;      // SLM_ATTN_CHUNK: lower bound on the split-K chunk (tests)
     int own_ld = 0, acc_bytes = 0;  // decode kernel shared-memory layout (see ring_offset)
     Model m{};
     std::vector<void *> allocs;
@@ -355,8 +356,10 @@ static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
         for (const Mat *M : {&m.emb, &m.qkv, &m.w13}) need = std::max(need, tile(M) + (size_t)dim * 4);
         for (const Mat *M : {&m.wo, &m.w2}) need = std::max(need, tile(M));
         c->attn_stage = B <= 2 ? 16 * 1024 : 32 * 1024;
+        if (const char *e = getenv("SLM_ATTN_STAGE"))  // tests: a smaller whole-chunk copy budget
+            c->attn_stage = std::max(0, std::min(c->attn_stage, atoi(e)));
         need = std::max(need, (size_t)(kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) + (G + 2) * hd) * 4 +
-                                  c->attn_stage);
+                                  std::max(c->attn_stage, 2 * hd * 4));  // at least the new row
         need = std::max(need, (size_t)B * grid * 2 * 4);  // argmax candidates
         c->xs_bytes = (int)round_up(need, 128);
         const size_t base = decode_smem_bytes(B, c->own_ld, c->acc_bytes, c->xs_bytes, 0);
@@ -365,6 +368,14 @@ static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
         if (slots < kMinRingSlots)
             return fail(c, SLM_EUNSUPPORTED, "shared memory too small: %zu B of scratch leaves %d ring slots", need, slots);
         c->ring_slots = slots;
+        c->smem = decode_smem_bytes(B, c->own_ld, c->acc_bytes, c->xs_bytes, slots);
+        if (const char *e = getenv("SLM_ATTN_CHUNK")) c->attn_chunk_min = std::max(0, atoi(e));
+        // What the ring slots leave goes to the scratch region too: attention chunks too
+        // long to copy whole stream through it (deeper per-warp rings).  The step plans
+        // keep using the size the shape needs.
+        c->xs_plan = c->xs_bytes;
+        const size_t spare = kSmemLimit > c->smem ? (kSmemLimit - c->smem) / 128 * 128 : 0;
+        c->xs_bytes += (int)spare;
         c->smem = decode_smem_bytes(B, c->own_ld, c->acc_bytes, c->xs_bytes, slots);
     }
     return SLM_OK;
@@ -805,11 +816,28 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
     } else {
         ch = (work + 2LL * c->grid - 1) / (2LL * c->grid);
     }
-    ch = std::max<long long>(ch, kMinAttnChunk);
+    ch = std::max<long long>(ch, std::max(kMinAttnChunk, c->attn_chunk_min));
     ch = std::max<long long>(ch, (max_ctx + kMaxChunksPerSeq - 1) / kMaxChunksPerSeq);
     ch = (ch + 31) / 32 * 32;
+    if (!P.roles) {
+        // Item i runs on CTA i mod grid, so the phase lasts ceil(items / grid) chunks: of
+        // the chunk lengths up to twice this one, take the one whose busiest CTA reads
+        // the fewest positions (rounding each row up to whole chunks can leave a few CTAs
+        // with one item more than the rest).
+        long long best = ch, best_load = -1;
+        for (long long cand = ch; cand <= 2 * ch; cand += 32) {
+            long long items = 0;
+            for (int b = 0; b < P.batch; b++) items += (long long)KV * ((P.pos[b] + cand) / cand);
+            const long long load = (items + c->grid - 1) / c->grid * cand;
+            if (best_load < 0 || load < best_load) {
+                best = cand;
+                best_load = load;
+            }
+        }
+        ch = best;
+    }
     // consumer merge: batch * (KBp(Wo) + H * nc * (hd + 2)) floats must fit the tile
-    const long long tile = (long long)(c->xs_bytes / 4) / P.batch - m.wo.KBp;
+    const long long tile = (long long)(c->xs_plan / 4) / P.batch - m.wo.KBp;
     long long nc_fit = tile > 0 ? tile / ((long long)H * (hd + 2)) : 0;
     nc_fit = std::min<long long>(nc_fit, kMaxChunksA);
     // consumers poll batch * H * nc * (hd + 2) words: beyond ~8K words the polling rounds

@@ -18,6 +18,7 @@ constexpr int kMinRingSlots = 16;                     //   of 8: slot s is alway
 constexpr int kChunkBytes = 8192;                     // one ring slot = one warp's chunk
 constexpr int kMaxBatch = 16;
 constexpr int kMaxGroupPass = 4;                      // query heads per attention pass
+constexpr int kAttnMaxSlots = 8;                      // streamed attention: passes per warp ring
 constexpr int kMaxChunksPerSeq = 64;                  // split-K chunks per (row, kv head)
 constexpr int kMaxChunksA = 16;                       // chunks when consumers merge them
 constexpr int kMinAttnChunk = 32;                     // positions

@@ -115,6 +115,36 @@ def test_shape_variants_batched_ragged(slm, name):
     compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, [0, 1, 2], name)
 
 
+STREAM_VARIANTS = {k: VARIANTS[k] for k in ("mqa", "bf16_kv", "gqa8", "ragged_dims", "wide_head")}
+STREAM_VARIANTS.update({
+    # bf16 caches with head_dim >= 32 take the head-split reduction
+    "bf16kv_hd64_g4": dict(kv_dtype=synth.DTYPE_BF16, dim=256, n_heads=4, n_kv_heads=1, head_dim=64),
+    "bf16kv_hd128_g2": dict(kv_dtype=synth.DTYPE_BF16, dim=256, n_heads=4, n_kv_heads=2, head_dim=128),
+    "bf16kv_hd32_g8": dict(kv_dtype=synth.DTYPE_BF16, dim=256, n_heads=8, n_kv_heads=1, head_dim=32),
+    "bf16kv_hd48_g3": dict(kv_dtype=synth.DTYPE_BF16, dim=144, n_heads=3, n_kv_heads=1, head_dim=48),
+})
+
+
+@pytest.mark.parametrize("name", sorted(STREAM_VARIANTS))
+def test_streamed_attention_chunks(slm, name, monkeypatch):
+    """Attention chunks too long for one shared-memory copy stream through per-warp rings
+    (the long-context path).  Forcing 96-position chunks (SLM_ATTN_CHUNK) that are never
+    copied whole (SLM_ATTN_STAGE=0) at contexts of 70..210 gives several chunks per row,
+    chunks that end mid-pass and chunks that end at the new position, on every head
+    geometry; against the oracle."""
+    monkeypatch.setenv("SLM_ATTN_CHUNK", "96")
+    monkeypatch.setenv("SLM_ATTN_STAGE", "0")
+    s = synth.TINY.replace(max_batch=3, max_seq=256, **STREAM_VARIANTS[name])
+    W = synth.make_weights(s, seed=17)
+    lens = [70, 131, 203]
+    prompts = [synth.make_prompt(s, r, lens[r]) for r in range(3)]
+    steps = 4
+    ref_ids, ref_logits = oracle_reference(s, prompts, steps, [0, 1, 2], seed=17)
+    eng = _engine(slm, s, W)
+    g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, steps, 3, [0, 1, 2])
+    compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, [0, 1, 2], name + " streamed")
+
+
 def test_kv_slots_written_exactly(slm):
     s = synth.TINY.replace(max_batch=2)
     W = synth.make_weights(s, seed=5)
