@@ -75,6 +75,14 @@ typedef struct {
     int32_t dim, n_layers, n_heads, n_kv_heads, head_dim, hidden, vocab, max_seq, max_batch;
     float rope_theta, norm_eps;
     int32_t weight_dtype, kv_dtype;
+    /* KV cache layout.  kv_page_size = 0: every sequence slot owns max_seq positions of
+     * cache.  Otherwise (a power of two in [16, 2^20]) the cache is a pool of kv_pages
+     * pages of kv_page_size positions (kv_pages = 0: max_batch * ceil(max_seq /
+     * kv_page_size)); a sequence holds the pages its positions reach, slm_reset returns
+     * them, and slm_fork's clones share their source's pages until they write into one
+     * ("Inside nanochat Part 4: Understanding Inference", Continuous Batching: sequences
+     * join and leave the batch).  Results do not depend on the layout. */
+    int32_t kv_page_size, kv_pages;
 } slm_config;
 
 typedef struct slm_ctx slm_ctx;
@@ -171,8 +179,11 @@ int slm_reset(slm_ctx *ctx, int32_t seq);
  *     cache refuses to be filled when it is not empty).
  *   Every layer's cached keys and values of positions [0, length of src) are copied
  *   byte for byte into each destination, whose length becomes src's.  Nothing else
- *   changes.  Asynchronous on `stream` (one kernel launch): later calls on the same
- *   stream see the copies.  Errors: SLM_EINVAL, SLM_ESTATE, SLM_ECUDA.
+ *   changes.  With a paged cache nothing is copied here: the destinations' tables point
+ *   at src's pages, and a sequence that appends into a page it shares first gets a
+ *   private copy of that page's rows (so a fork costs one partial page per clone, at
+ *   its first step).  Asynchronous on `stream` (one kernel launch): later calls on the
+ *   same stream see the copies.  Errors: SLM_EINVAL, SLM_ESTATE, SLM_ECUDA.
  */
 int slm_fork(slm_ctx *ctx, int32_t src, int32_t n_dst, const int32_t *dst_seqs, void *stream);
 
@@ -204,6 +215,16 @@ int slm_sample(int32_t batch, int32_t vocab, const float *logits, int32_t ld, fl
 
 /* slm_seq_len -- current length of a sequence (>= 0), or a negative SLM_E* code. */
 int32_t slm_seq_len(const slm_ctx *ctx, int32_t seq);
+
+/*
+ * slm_kv_pages_free -- pages of a paged KV cache (kv_page_size > 0) that no sequence
+ * holds: what sequences can still grow into (admission for continuous batching).  0
+ * without paging; SLM_EINVAL for a NULL context.  With paging, slm_prefill,
+ * slm_prefill_batch and slm_decode_step return SLM_ECAPACITY, and change nothing, when
+ * the pages their rows need (a new page at every kv_page_size-th position, plus one when
+ * a row first writes into a page it shares after slm_fork) exceed this count.
+ */
+int32_t slm_kv_pages_free(const slm_ctx *ctx);
 
 /*
  * slm_sync -- wait for the work enqueued on `stream`, then read and clear the device
@@ -292,6 +313,13 @@ int slm_debug_gemm_bf16(int32_t M, int32_t N, int32_t K, const void *A, const vo
  * can check that a step writes exactly the slots it should.  Synchronous.
  */
 int slm_debug_fill_kv(slm_ctx *ctx, float value);
+
+/*
+ * slm_debug_page_table -- test hook: the page ids of sequence `seq` (ceil(max_seq /
+ * kv_page_size) entries; -1 = no page; without paging one entry, the slot itself),
+ * up to out_len of them into host `out`.  Returns the number of entries, or SLM_EINVAL.
+ */
+int32_t slm_debug_page_table(const slm_ctx *ctx, int32_t seq, int32_t *out, int32_t out_len);
 
 /*
  * slm_attention_workspace_bytes -- size in bytes of the device workspace that

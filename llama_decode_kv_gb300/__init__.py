@@ -38,7 +38,8 @@ class slm_config(ctypes.Structure):
                 ("dim", "n_layers", "n_heads", "n_kv_heads", "head_dim", "hidden", "vocab",
                  "max_seq", "max_batch")] + \
                [("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float),
-                ("weight_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+                ("weight_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("kv_page_size", ctypes.c_int32), ("kv_pages", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -49,6 +50,8 @@ _SIGS = {
     "slm_decode_step": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P]),
     "slm_reset": (ctypes.c_int, [_P, _I32]),
     "slm_seq_len": (_I32, [_P, _I32]),
+    "slm_kv_pages_free": (_I32, [_P]),
+    "slm_debug_page_table": (_I32, [_P, _I32, _P, _I32]),
     "slm_fork": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "slm_prefill_batch": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P]),
     "slm_sample": (ctypes.c_int, [_I32, _I32, _P, _I32, ctypes.c_float, _I32, ctypes.c_float, _P, _P, _P]),
@@ -89,11 +92,11 @@ class SlmError(RuntimeError):
         self.code = code
 
 
-def config_from_shape(shape) -> slm_config:
+def config_from_shape(shape, kv_page_size: int = 0, kv_pages: int = 0) -> slm_config:
     return slm_config(shape.dim, shape.n_layers, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                       shape.hidden, shape.vocab, shape.max_seq, shape.max_batch,
                       float(shape.rope_theta), float(shape.norm_eps), int(shape.weight_dtype),
-                      int(shape.kv_dtype))
+                      int(shape.kv_dtype), int(kv_page_size), int(kv_pages))
 
 
 def _ptr(x) -> Optional[int]:
@@ -159,11 +162,12 @@ def plan(shape, sms: int = 152) -> dict:
 class Engine:
     """One decode context: device weights, KV cache and per-sequence lengths."""
 
-    def __init__(self, shape, weights):
+    def __init__(self, shape, weights, kv_page_size: int = 0, kv_pages: int = 0):
+        """kv_page_size > 0: a paged KV cache of kv_pages pages (0: enough for every slot)."""
         import torch  # device memory and streams
         self.torch = torch
         self.shape = shape
-        self.cfg = config_from_shape(shape)
+        self.cfg = config_from_shape(shape, kv_page_size, kv_pages)
         buf = weights if not isinstance(weights, np.ndarray) else np.ascontiguousarray(weights)
         nbytes = buf.nbytes if isinstance(buf, np.ndarray) else buf.numel() * buf.element_size()
         h = ctypes.c_void_p()
@@ -221,6 +225,22 @@ class Engine:
 
     def seq_len(self, seq: int) -> int:
         return int(slm_seq_len(self.ctx, seq))
+
+    def pages_free(self) -> int:
+        """slm_kv_pages_free: pages of a paged cache that no sequence holds."""
+        n = int(slm_kv_pages_free(self.ctx))
+        if n < 0:
+            raise SlmError(n, "slm_kv_pages_free", self.last_error())
+        return n
+
+    def page_table(self, seq: int) -> np.ndarray:
+        """slm_debug_page_table: the page ids of sequence seq (-1: none)."""
+        n = int(slm_debug_page_table(self.ctx, seq, None, 0))
+        if n < 0:
+            raise SlmError(n, "slm_debug_page_table", self.last_error())
+        out = np.zeros(n, dtype=np.int32)
+        slm_debug_page_table(self.ctx, seq, out.ctypes.data, n)
+        return out
 
     def sync(self, stream=None) -> int:
         return slm_sync(self.ctx, _stream_ptr(stream))

@@ -40,7 +40,10 @@ struct AttnTask {
     bool kv_bf16;                // cache element type: bf16 or fp32
     const uint8_t *kbase;        // keys of the (row, kv head): position t at t * hd elements
     const uint8_t *vbase;        //   (global cache, or a shared-memory copy of the chunk
-                                 //   addressed as if it started at position 0)
+                                 //   addressed as if it started at position 0); with
+    const int *pages;            //   pages: position t at pages[t >> page_shift] * page_stride
+    size_t page_stride;          //   + (t & page_mask) * hd elements (a paged cache)
+    int page_shift, page_mask;
     const uint8_t *tail_k;       // position tail_t is read from these rows instead (the
     const uint8_t *tail_v;       //   step's own key and value); tail_t = -1: none
     int tail_t;
@@ -123,12 +126,19 @@ __device__ __forceinline__ void attn_scan(const AttnTask &T, const float (&qv)[k
     auto owner = [&](int h) { return base + (h >> 1) * (LPP >> 1) + (h & 1) * (LPP >> 2); };
     float m_own = -INFINITY, l_own = 0.f;
     int wr = 0, rd = 0;  // ring slots of the next copy and of the next pass
+    // byte offset of position t's row (a pass's PP rows never cross a page: pages hold a
+    // multiple of 16 rows and passes start at multiples of PP <= 16)
+    auto row_off = [&](int t) -> size_t {
+        return T.pages ? (size_t)__ldg(T.pages + (t >> T.page_shift)) * T.page_stride +
+                             (size_t)(t & T.page_mask) * rowbytes
+                       : (size_t)t * rowbytes;
+    };
     auto issue = [&](int k) {
         if (k < npass) {
             const int p0 = t0 + k * stride + warp * PP;
             const int n = max(0, min(PP, tc - p0)) * rows16;  // 16-byte pieces
             uint8_t *dst = ring + (size_t)wr * slotb;
-            const size_t src = (size_t)p0 * rowbytes;
+            const size_t src = n > 0 ? row_off(p0) : 0;
             for (int e = lane; e < n; e += 32) {
                 cp_async16(dst + e * 16, T.kbase + src + e * 16);
                 cp_async16(dst + PP * rowbytes + e * 16, T.vbase + src + e * 16);
@@ -150,8 +160,9 @@ __device__ __forceinline__ void attn_scan(const AttnTask &T, const float (&qv)[k
             vr = kr + PP * rowbytes;
             rd = rd + 1 == S ? 0 : rd + 1;
         } else {
-            kr = T.kbase + (size_t)p0 * rowbytes;
-            vr = T.vbase + (size_t)p0 * rowbytes;
+            const size_t off = p0 < t1 ? row_off(p0) : 0;
+            kr = T.kbase + off;
+            vr = T.vbase + off;
         }
         const int t = p0 + grp;
         const bool valid = t < t1;

@@ -45,6 +45,10 @@ __global__ void __launch_bounds__(kComputeThreads) attention_decode_kernel(const
     T.kv_bf16 = KVBF16;
     T.tail_k = T.tail_v = nullptr;
     T.tail_t = -1;
+    T.pages = nullptr;
+    T.page_stride = 0;
+    T.page_shift = 0;
+    T.page_mask = 0;
     T.stream = nullptr;
     T.stream_bytes = 0;
     T.kbase = P.k + ((size_t)b * P.KV + g) * P.cap * rowbytes;

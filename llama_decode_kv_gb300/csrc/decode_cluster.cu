@@ -519,10 +519,9 @@ __device__ __forceinline__ void stage_kv(const ClusterParams &P, CS &S, const Me
     const Model &m = P.m;
     const int esz = m.kv_bf16 ? 2 : 4;
     const int rb = m.head_dim * esz, srb = rb + 16, per = rb / 16;
-    const size_t head = ((((size_t)layer * m.max_batch + P.seq) * m.n_kv_heads + g) * m.max_seq + me.t0) * rb;
     for (int e = threadIdx.x; e < me.ns * per; e += kComputeThreads) {
         const int t = e / per, q = e - t * per;
-        const size_t src = head + (size_t)t * rb + (size_t)q * 16;
+        const size_t src = kv_row(m, layer, P.seq, g, me.t0 + t) * rb + (size_t)q * 16;
         cp_async16(S.kst + (size_t)t * srb + q * 16, m.kc + src);
         cp_async16(S.vst + (size_t)t * srb + q * 16, m.vc + src);
     }
@@ -544,8 +543,9 @@ __device__ __forceinline__ void attention_cta(const ClusterParams &P, CS &S, con
     const int esz = bf ? 2 : 4, rb = hd * esz, srb = rb + 16;
     const int pos = P.pos, T = me.T, t0 = me.t0, ns = me.ns;
     const int tcap = (m.max_seq + C - 1) / C;
-    const size_t head = ((((size_t)layer * m.max_batch + P.seq) * m.n_kv_heads + w.g) * m.max_seq) * rb;
-    const uint8_t *kg = m.kc + head, *vg = m.vc + head;
+    // positions this CTA did not stage are read from the cache
+    auto kg = [&](int t) { return m.kc + kv_row(m, layer, P.seq, w.g, t) * rb; };
+    auto vg = [&](int t) { return m.vc + kv_row(m, layer, P.seq, w.g, t) * rb; };
     // scores s[j][t] = q_j . k_t (q carries log2(e) / sqrt(hd)); this thread's items
     for (int it = 0; it < me.nsc; it++) {
         const int j = me.sj[it], tt = me.st[it], t = t0 + tt;
@@ -559,7 +559,7 @@ __device__ __forceinline__ void attention_cta(const ClusterParams &P, CS &S, con
                 s1 = fmaf(a.z, b.z, fmaf(a.w, b.w, s1));
             }
         } else {
-            const uint8_t *k = tt < ns ? S.kst + (size_t)tt * srb : kg + (size_t)t * rb;
+            const uint8_t *k = tt < ns ? S.kst + (size_t)tt * srb : kg(t);
             if (bf) {
                 for (int d = 0; d < hd / 8; d++) {
                     const uint4 u = *(const uint4 *)(k + d * 16);
@@ -607,15 +607,15 @@ __device__ __forceinline__ void attention_cta(const ClusterParams &P, CS &S, con
         int tt = 0;
         for (; tt + 1 < T; tt += 2) {
             const int t = t0 + tt;
-            const float v0 = t == pos ? S.qkv[(G + 1) * hd + d] : kv_elem(tt < ns ? S.vst + (size_t)tt * srb : vg + (size_t)t * rb, d, bf);
+            const float v0 = t == pos ? S.qkv[(G + 1) * hd + d] : kv_elem(tt < ns ? S.vst + (size_t)tt * srb : vg(t), d, bf);
             const float v1 = t + 1 == pos ? S.qkv[(G + 1) * hd + d]
-                                          : kv_elem(tt + 1 < ns ? S.vst + (size_t)(tt + 1) * srb : vg + (size_t)(t + 1) * rb, d, bf);
+                                          : kv_elem(tt + 1 < ns ? S.vst + (size_t)(tt + 1) * srb : vg(t + 1), d, bf);
             o0 = fmaf(p[tt], v0, o0);
             o1 = fmaf(p[tt + 1], v1, o1);
         }
         if (tt < T) {
             const int t = t0 + tt;
-            const float v0 = t == pos ? S.qkv[(G + 1) * hd + d] : kv_elem(tt < ns ? S.vst + (size_t)tt * srb : vg + (size_t)t * rb, d, bf);
+            const float v0 = t == pos ? S.qkv[(G + 1) * hd + d] : kv_elem(tt < ns ? S.vst + (size_t)tt * srb : vg(t), d, bf);
             o0 = fmaf(p[tt], v0, o0);
         }
         const uint32_t sbar = smem_addr(&S.xb[XB_ST]);
@@ -821,13 +821,12 @@ __device__ __forceinline__ void compute_cta(const ClusterParams &P, CS &S, const
                         o1 = __bfloat162float(h1v);
                         if (peer == 0) {
                             __nv_bfloat16 *row = (__nv_bfloat16 *)(sub == G ? m.kc : m.vc) +
-                                                 ((((size_t)l * m.max_batch + P.seq) * m.n_kv_heads + w.g) * m.max_seq + P.pos) * hd;
+                                                 kv_row(m, l, P.seq, w.g, P.pos) * hd;
                             row[i] = h0v;
                             row[i + half] = h1v;
                         }
                     } else if (peer == 0) {
-                        float *row = (float *)(sub == G ? m.kc : m.vc) +
-                                     ((((size_t)l * m.max_batch + P.seq) * m.n_kv_heads + w.g) * m.max_seq + P.pos) * hd;
+                        float *row = (float *)(sub == G ? m.kc : m.vc) + kv_row(m, l, P.seq, w.g, P.pos) * hd;
                         row[i] = o0;
                         row[i + half] = o1;
                     }

@@ -150,7 +150,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
         const int n = rows * len;
         for (int base = 0; base < n; base += kComputeThreads * kPollBatch) {
             int so[kPollBatch], dof[kPollBatch];
-            float g[kPollBatch];
+            float g[kPollBatch], xv[kPollBatch];  // xv: the words' values, squared in k order
             bool need[kPollBatch];
 #pragma unroll
             for (int k = 0; k < kPollBatch; k++) {
@@ -160,6 +160,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                 so[k] = r * src_ld + j;
                 dof[k] = r * dst_ld + (perm_ld ? xpos(j, perm_ld, true) : j);
                 g[k] = (gain && need[k]) ? __ldg(gain + j) : 1.f;
+                xv[k] = 0.f;
             }
             unsigned long long t0 = 0;
             for (int it = 0;; it++) {
@@ -172,7 +173,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                     if (!need[k]) continue;
                     if ((uint32_t)(w[k] >> 32) == tag) {
                         const float x = __uint_as_float((uint32_t)w[k]);
-                        ss = fmaf(x, x, ss);
+                        xv[k] = x;
                         dst[dof[k]] = x * g[k];
                         need[k] = false;
                     } else {
@@ -190,6 +191,9 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                     }
                 }
             }
+            // the sum of squares in a fixed order, whatever order the words arrived in
+#pragma unroll
+            for (int k = 0; k < kPollBatch; k++) ss = fmaf(xv[k], xv[k], ss);
         }
         if (ssp) {
             ss = warp_sum(ss);
@@ -210,6 +214,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
         for (int base = 0; base < nl; base += tpr * kPollBatchW) {
             int wj[kPollBatchW];  // first word (column) of load k
             float g0[kPollBatchW], g1[kPollBatchW];
+            float xv[kPollBatchW][2];  // the words' values, squared in (k, h) order
             uint32_t pend = 0;   // bit 2k + h: word h of load k still missing
 #pragma unroll
             for (int k = 0; k < kPollBatchW; k++) {
@@ -220,6 +225,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                 g0[k] = (gain && l < nl) ? __ldg(gain + wj[k]) : 1.f;
                 g1[k] = (gain && l < nl && wpl == 2) ? __ldg(gain + wj[k] + 1) : 1.f;
                 if (l < nl) pend |= (wpl == 2 ? 3u : 1u) << (2 * k);
+                xv[k][0] = xv[k][1] = 0.f;
             }
             unsigned long long t0 = 0;
             for (int it = 0;; it++) {
@@ -240,7 +246,8 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                         (uint32_t)(w[k][1] >> 32) == tag) {  // both words: one 32-bit store per plane
                         pend &= ~(3u << (2 * k));
                         const float x0 = __uint_as_float((uint32_t)w[k][0]), x1 = __uint_as_float((uint32_t)w[k][1]);
-                        ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+                        xv[k][0] = x0;
+                        xv[k][1] = x1;
                         plane_store2((uint16_t *)dst, dst_ld, b, wj[k], x0 * g0[k], x1 * g1[k]);
                         continue;
                     }
@@ -251,7 +258,7 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                         pend &= ~bit;
                         const int j = wj[k] + h;
                         const float x = __uint_as_float((uint32_t)w[k][h]);
-                        ss = fmaf(x, x, ss);
+                        xv[k][h] = x;
                         const float y = x * (h ? g1[k] : g0[k]);
                         if (planes)  // dst_ld is the plane row length
                             plane_store((uint16_t *)dst, dst_ld, b, j, y);
@@ -270,6 +277,8 @@ __device__ __forceinline__ void poll_words(const StepParams &P, const uint64_t *
                     }
                 }
             }
+#pragma unroll
+            for (int k = 0; k < kPollBatchW; k++) ss = fmaf(xv[k][1], xv[k][1], fmaf(xv[k][0], xv[k][0], ss));
         }
     }
     if (ssp) {  // per warp and row: lanes of one row are min(tpr, 32) consecutive lanes
@@ -678,8 +687,7 @@ __device__ __forceinline__ EpiCtx prepare_ctx(const StepParams &P, int epi, int 
         }
         if (s >= G) {
             const int esz = m.kv_bf16 ? 2 : 4;
-            c.cache = (s == G ? m.kc : m.vc) +
-                      (((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + pos) * hd + i) * esz;
+            c.cache = (s == G ? m.kc : m.vc) + (kv_row(m, layer, P.seq[b], g, pos) * hd + i) * esz;
         }
         c.dst = m.ll_qkv + ll_layer(P, layer, m.qkv.rows) + (size_t)b * m.qkv.rows + ((size_t)g * (G + 2) + s) * hd + i;
         return c;
@@ -975,8 +983,7 @@ __device__ __forceinline__ Cand mma_epilogue(const StepParams &P, int epi, int l
             o1 *= qscale;
         } else {
             const bool bf = m.kv_bf16;
-            uint8_t *row = (sub == G ? m.kc : m.vc) +
-                           ((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + pos) * hd * (bf ? 2 : 4);
+            uint8_t *row = (sub == G ? m.kc : m.vc) + kv_row(m, layer, P.seq[b], g, pos) * hd * (bf ? 2 : 4);
             if (bf) {
                 const __nv_bfloat16 h0 = __float2bfloat16_rn(o0), h1 = __float2bfloat16_rn(o1);
                 ((__nv_bfloat16 *)row)[d] = h0;
@@ -1265,7 +1272,10 @@ __device__ __forceinline__ void attn_item(const StepParams &P, int layer, int b,
     const int CH = P.attn_chunk, nc = P.nchunk[b];
     const int t0 = c * CH, t1 = min(ctx, t0 + CH);
     const size_t rowbytes = (size_t)hd * (kvbf16 ? 2 : 4);
-    const size_t head_off = ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq) * rowbytes;
+    // rows of page 0 of this layer and kv head; the sequence's pages from its table row
+    const size_t head_off = (((size_t)layer * m.kv_npages) * KV + g) * m.kv_rows * rowbytes;
+    const size_t page_stride = (size_t)KV * m.kv_rows * rowbytes;
+    const int *pages = m.kv_table + (size_t)seq * m.kv_pps;
     const uint8_t *kbase = m.kc + head_off;
     const uint8_t *vbase = m.vc + head_off;
     const uint64_t *qkv = m.ll_qkv + ll_layer(P, layer, qrows) + (size_t)b * qrows + (size_t)g * (G + 2) * hd;
@@ -1283,9 +1293,12 @@ __device__ __forceinline__ void attn_item(const StepParams &P, int layer, int b,
     if (stage) {
         const int per_row = (int)(rowbytes / 16), n16 = (tc - t0) * per_row;
         for (int e = tid; e < n16; e += kComputeThreads) {
-            const size_t off = (size_t)(e / per_row) * rowbytes + (size_t)(e % per_row) * 16;
-            cp_async16(kst + off, kbase + (size_t)t0 * rowbytes + off);
-            cp_async16(vst + off, vbase + (size_t)t0 * rowbytes + off);
+            const int r = e / per_row, t = t0 + r;
+            const size_t piece = (size_t)(e - r * per_row) * 16;
+            const size_t src = (size_t)__ldg(pages + (t >> m.kv_shift)) * page_stride +
+                               (size_t)(t & m.kv_mask) * rowbytes + piece;
+            cp_async16(kst + (size_t)r * rowbytes + piece, kbase + src);
+            cp_async16(vst + (size_t)r * rowbytes + piece, vbase + src);
         }
     }
     poll_words(P, qkv, hd, appends ? G + 2 : G, hd, raw, hd, 0, nullptr, nullptr);
@@ -1312,6 +1325,10 @@ __device__ __forceinline__ void attn_item(const StepParams &P, int layer, int b,
     T.kv_bf16 = kvbf16;
     T.kbase = stage ? kst - (size_t)t0 * rowbytes : kbase;
     T.vbase = stage ? vst - (size_t)t0 * rowbytes : vbase;
+    T.pages = stage ? nullptr : pages;
+    T.page_stride = page_stride;
+    T.page_shift = m.kv_shift;
+    T.page_mask = m.kv_mask;
     T.tail_k = kst;
     T.tail_v = vst;
     T.tail_t = (appends && !stage) ? pos : -1;
@@ -1358,14 +1375,13 @@ __device__ __forceinline__ void prefetch_attention_kv(const StepParams &P, int l
         const int g = local / nc, c = local - g * nc;
         const int t0 = c * P.attn_chunk, tc = min(P.pos[b], t0 + P.attn_chunk);  // cached rows
         if (g >= m.n_kv_heads || tc <= t0) continue;
-        const size_t off = ((((size_t)layer * m.max_batch + P.seq[b]) * m.n_kv_heads + g) * m.max_seq + t0) * rowbytes;
-        size_t bytes = min((size_t)(tc - t0) * rowbytes, kPrefetchKvBytes);
-        const uint8_t *src = (threadIdx.x == 0 ? m.kc : m.vc) + off;
-        while (bytes) {  // one bulk prefetch moves less than 4 GB; stay well below
-            const uint32_t n = (uint32_t)min(bytes, (size_t)(1u << 20));
-            bulk_prefetch_l2(src, n);
-            src += n;
-            bytes -= n;
+        const int tend = t0 + (int)min((size_t)(tc - t0), kPrefetchKvBytes / rowbytes);
+        for (int t = t0; t < tend;) {  // one bulk prefetch per page (each below 1 MB)
+            const long long page_end = ((long long)(t >> m.kv_shift) + 1) << m.kv_shift;
+            const int n = (int)min((long long)tend, min(page_end, (long long)t + (1 << 20) / (long long)rowbytes)) - t;
+            bulk_prefetch_l2((threadIdx.x == 0 ? m.kc : m.vc) + kv_row(m, layer, P.seq[b], g, t) * rowbytes,
+                             (uint32_t)(n * rowbytes));
+            t += n;
         }
     }
 }

@@ -92,6 +92,13 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Row index (in head_dim elements) of position `pos` of sequence `seq`, kv head g, in
+// layer `layer` of the KV cache (see Model: a page-table lookup, then the row).
+__device__ __forceinline__ size_t kv_row(const Model &m, int layer, int seq, int g, int pos) {
+    const int page = __ldg(m.kv_table + (size_t)seq * m.kv_pps + (pos >> m.kv_shift));
+    return (((size_t)layer * m.kv_npages + page) * m.n_kv_heads + g) * m.kv_rows + (pos & m.kv_mask);
+}
+
 // 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all).
 __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");

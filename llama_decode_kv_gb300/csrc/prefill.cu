@@ -116,7 +116,7 @@ __global__ void rope_append_kernel(const Model m, float *qkv, int layer, const P
                 h[i + half] = b2;
                 continue;
             }
-            uint8_t *kd = m.kc + ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq + pos) * rowbytes;
+            uint8_t *kd = m.kc + kv_row(m, layer, seq, g, pos) * rowbytes;
             if (KVBF16) {
                 ((uint16_t *)kd)[i] = f32_to_bf16_bits(a2);
                 ((uint16_t *)kd)[i + half] = f32_to_bf16_bits(b2);
@@ -125,7 +125,7 @@ __global__ void rope_append_kernel(const Model m, float *qkv, int layer, const P
                 ((float *)kd)[i + half] = b2;
             }
         } else {
-            uint8_t *vd = m.vc + ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq + pos) * rowbytes;
+            uint8_t *vd = m.vc + kv_row(m, layer, seq, g, pos) * rowbytes;
             if (KVBF16) {
                 ((uint16_t *)vd)[i] = f32_to_bf16_bits(a);
                 ((uint16_t *)vd)[i + half] = f32_to_bf16_bits(b);
@@ -209,16 +209,16 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};  // rows g4, g4 + 8
     const int pos0 = p0 + q0 + warp * 16 + g4, pos1 = pos0 + 8;    // this lane's two rows
     const size_t rowbytes = (size_t)HD * 2;
-    const uint8_t *kbase = m.kc + ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq) * rowbytes;
-    const uint8_t *vbase = m.vc + ((((size_t)layer * m.max_batch + seq) * KV + g) * m.max_seq) * rowbytes;
+
     for (int k0 = 0; k0 <= last; k0 += KB) {
         __syncthreads();  // previous block's readers are done
         for (int e = tid; e < KB * (HD / 8); e += blockDim.x) {  // 16-byte pieces
             const int j = e / (HD / 8), c = (e - j * (HD / 8)) * 8, kp = k0 + j;
             uint16_t *kd = ks + j * LD + c, *vd = vs + j * LD + c;
             if (kp <= last) {
-                cp_async16(kd, kbase + (size_t)kp * rowbytes + c * 2);
-                cp_async16(vd, vbase + (size_t)kp * rowbytes + c * 2);
+                const size_t src = kv_row(m, layer, seq, g, kp) * rowbytes + c * 2;
+                cp_async16(kd, m.kc + src);
+                cp_async16(vd, m.vc + src);
             } else {
                 *(uint4 *)kd = make_uint4(0, 0, 0, 0);
                 *(uint4 *)vd = make_uint4(0, 0, 0, 0);

@@ -19,6 +19,7 @@
 #include <string>
 #include <vector>
 
+#include "kv_pages.h"
 #include "prefill.cuh"
 #include "slm_internal.h"
 
@@ -44,6 +45,8 @@ struct slm_ctx {
     Model m{};
     std::vector<void *> allocs;
     std::vector<int> len;
+    KvPages pages;               // the KV cache's page table (host copy) and pool
+    int *d_table = nullptr;      //   device copy of the table
     uint32_t launch_seq = 0;     // exchange tag of the last launch
     unsigned long long *d_trace = nullptr;  // phase timeline, when tracing is on
     bool prefill_tc = false;     // long prompts go through the tensor-core prefill
@@ -208,6 +211,21 @@ static bool config_ok(const slm_config *c, std::string &why) {
     }
     if (c->head_dim % 8 || c->head_dim > 256) {
         snprintf(buf, sizeof buf, "head_dim %d must be a multiple of 8 and at most 256", c->head_dim);
+        why = buf;
+        return false;
+    }
+    if (c->kv_page_size != 0 &&
+        (c->kv_page_size < 16 || c->kv_page_size > (1 << 20) || (c->kv_page_size & (c->kv_page_size - 1)))) {
+        snprintf(buf, sizeof buf, "kv_page_size %d must be 0 or a power of two in [16, 2^20]", c->kv_page_size);
+        why = buf;
+        return false;
+    }
+    if (c->kv_pages < 0 || (c->kv_pages > 0 && c->kv_page_size == 0)) {
+        why = "kv_pages must be >= 0, and 0 without paging";
+        return false;
+    }
+    if (c->kv_page_size != 0 && c->kv_pages != 0 && c->kv_pages < (c->max_seq + c->kv_page_size - 1) / c->kv_page_size) {
+        snprintf(buf, sizeof buf, "kv_pages %d cannot hold one sequence of max_seq %d", c->kv_pages, c->max_seq);
         why = buf;
         return false;
     }
@@ -652,7 +670,14 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
 
     // ---- KV cache and scratch
     const size_t kvesz = m.kv_bf16 ? 2 : 4;
-    const size_t kv_bytes = (size_t)L * B * KV * cfg->max_seq * hd * kvesz;
+    KvPages &kp = c->pages;
+    if (cfg->kv_page_size == 0) {
+        kp.init_contiguous(B, cfg->max_seq);
+    } else {
+        const int pps = (cfg->max_seq + cfg->kv_page_size - 1) / cfg->kv_page_size;
+        kp.init_paged(B, cfg->max_seq, cfg->kv_page_size, cfg->kv_pages ? cfg->kv_pages : B * pps);
+    }
+    const size_t kv_bytes = (size_t)L * kp.npages * KV * kp.rows * hd * kvesz;
     void *p;
     if ((rc = dev_alloc(c, &p, kv_bytes))) return rc;
     m.kc = (uint8_t *)p;
@@ -660,6 +685,16 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     m.vc = (uint8_t *)p;
     CK(c, cudaMemset(m.kc, 0, kv_bytes));
     CK(c, cudaMemset(m.vc, 0, kv_bytes));
+    if ((rc = dev_alloc(c, &p, kp.table.size() * 4))) return rc;
+    c->d_table = (int *)p;
+    CK(c, cudaMemcpy(c->d_table, kp.table.data(), kp.table.size() * 4, cudaMemcpyHostToDevice));
+    kp.clear_queue();
+    m.kv_table = c->d_table;
+    m.kv_pps = kp.pps;
+    m.kv_shift = kp.shift;
+    m.kv_mask = kp.contiguous ? 0x7fffffff : kp.rows - 1;
+    m.kv_rows = kp.rows;
+    m.kv_npages = kp.npages;
     const size_t Lz = L;
     struct {
         void **dst;
@@ -924,6 +959,46 @@ static int read_status(slm_ctx *c, uint32_t *st) {
     return SLM_OK;
 }
 
+// Launch the page-table writes and page copies queued on the host, in stream order
+// before the kernels that read the cache.
+static int flush_pages(slm_ctx *c, cudaStream_t s) {
+    KvPages &kp = c->pages;
+    for (size_t i = 0; i < kp.copies.size(); i += kMaxBatch) {
+        PageCopies a{};
+        for (size_t j = i; j < kp.copies.size() && a.n < kMaxBatch; j++, a.n++) {
+            a.src[a.n] = kp.copies[j].src;
+            a.dst[a.n] = kp.copies[j].dst;
+            a.rows[a.n] = kp.copies[j].rows;
+        }
+        CK(c, copy_kv_pages(c->m, a, s));
+    }
+    for (size_t i = 0; i < kp.upd_idx.size(); i += kTableWritesMax) {
+        TableWrites w{};
+        for (size_t j = i; j < kp.upd_idx.size() && w.n < kTableWritesMax; j++, w.n++) {
+            w.idx[w.n] = kp.upd_idx[j];
+            w.val[w.n] = kp.upd_val[j];
+        }
+        CK(c, write_kv_table(c->d_table, w, s));
+    }
+    kp.clear_queue();
+    return SLM_OK;
+}
+
+// Pages for `n` sequences to grow from lens[i] to tos[i] positions: all of them, or
+// SLM_ECAPACITY and nothing taken.  Then the table and copies reach the device.
+static int reserve_pages(slm_ctx *c, int n, const int *seqs, const int *lens, const int *tos, cudaStream_t s) {
+    KvPages &kp = c->pages;
+    if (!kp.contiguous) {
+        int need = 0;
+        for (int i = 0; i < n; i++) need += kp.pages_needed(seqs[i], lens[i], tos[i]);
+        if (need > kp.pages_free())
+            return fail(c, SLM_ECAPACITY, "KV page pool exhausted: %d pages needed, %d free of %d", need,
+                        kp.pages_free(), kp.npages);
+        for (int i = 0; i < n; i++) kp.prepare(seqs[i], lens[i], tos[i]);
+    }
+    return flush_pages(c, s);
+}
+
 extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids, const int32_t *tokens,
                                const int32_t *positions, float *logits, int32_t *next_ids, void *stream) {
     if (!c) return SLM_EINVAL;
@@ -970,6 +1045,11 @@ extern "C" int slm_decode_step(slm_ctx *c, int32_t batch, const int32_t *seq_ids
     const bool spin = !ids_dev && log_dev;
     P.done_word = spin ? (uint32_t *)(c->d_step + 2 * kMaxBatch) : nullptr;
     P.do_logits = 1;
+    {
+        int tos[kMaxBatch];
+        for (int i = 0; i < batch; i++) tos[i] = P.pos[i] + 1;
+        if (int rp = reserve_pages(c, batch, P.seq, P.pos, tos, s)) return rp;
+    }
     int rc = launch(c, P, s);
     if (rc) return rc;
     for (int i = 0; i < batch; i++) c->len[P.seq[i]] = P.pos[i] + 1;
@@ -1019,6 +1099,10 @@ extern "C" int slm_prefill_batch(slm_ctx *c, int32_t nseq, const int32_t *seqs, 
         if (lens[i] < kTensorPrefillMin) tc = false;
     }
     cudaStream_t s = (cudaStream_t)stream;
+    {
+        int zeros[kMaxBatch] = {0};
+        if (int rp = reserve_pages(c, nseq, seqs, zeros, lens, s)) return rp;
+    }
     if (tc) {
         cudaError_t e = prefill_run_batch(c->m, c->plan, nseq, seqs, lens, tokens, last_logits, next_ids, s);
         if (e != cudaSuccess) {
@@ -1051,6 +1135,10 @@ extern "C" int slm_prefill(slm_ctx *c, int32_t seq, const int32_t *tokens, int32
     const bool log_dev = !last_logits || is_device_ptr(last_logits);
     const bool ids_dev = is_device_ptr(next_id);
     const int32_t *dtok = tokens;
+    {
+        const int zero = 0;
+        if (int rp = reserve_pages(c, 1, &seq, &zero, &n, s)) return rp;
+    }
     if (!tok_dev) {
         for (int i = 0; i < n; i++)
             if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab)
@@ -1112,10 +1200,12 @@ extern "C" int slm_reset(slm_ctx *c, int32_t seq) {
     if (!c) return SLM_EINVAL;
     if (seq == -1) {
         std::fill(c->len.begin(), c->len.end(), 0);
+        for (int q = 0; q < c->cfg.max_batch; q++) c->pages.release(q);
         return SLM_OK;
     }
     if (seq < 0 || seq >= c->cfg.max_batch) return fail(c, SLM_EINVAL, "seq %d out of range", seq);
     c->len[seq] = 0;
+    c->pages.release(seq);
     return SLM_OK;
 }
 
@@ -1158,9 +1248,6 @@ extern "C" int slm_fork(slm_ctx *c, int32_t src, int32_t n_dst, const int32_t *d
     if (n_dst < 1 || n_dst > B - 1 || n_dst > kMaxBatch)
         return fail(c, SLM_EINVAL, "n_dst %d out of range [1, %d]", n_dst, B - 1);
     if (c->len[src] < 1) return fail(c, SLM_ESTATE, "source sequence %d is empty", src);
-    ForkArgs a{};
-    a.src = src;
-    a.len = c->len[src];
     for (int i = 0; i < n_dst; i++) {
         const int d = dst_seqs[i];
         if (d < 0 || d >= B) return fail(c, SLM_EINVAL, "destination sequence %d out of range", d);
@@ -1169,11 +1256,26 @@ extern "C" int slm_fork(slm_ctx *c, int32_t src, int32_t n_dst, const int32_t *d
             if (dst_seqs[j] == d) return fail(c, SLM_EINVAL, "destination %d repeated", d);
         if (c->len[d] != 0)
             return fail(c, SLM_ESTATE, "destination sequence %d is not empty (%d positions)", d, c->len[d]);
-        a.dst[i] = d;
     }
-    CK(c, fork_kv(c->m, a, n_dst, (cudaStream_t)stream));
-    for (int i = 0; i < n_dst; i++) c->len[a.dst[i]] = a.len;
+    // paged: the clones share the source's pages (copied on their first write);
+    // otherwise the rows are copied into each clone's own page
+    for (int i = 0; i < n_dst; i++) c->pages.fork(src, dst_seqs[i], c->len[src]);
+    if (int rc = flush_pages(c, (cudaStream_t)stream)) return rc;
+    for (int i = 0; i < n_dst; i++) c->len[dst_seqs[i]] = c->len[src];
     return SLM_OK;
+}
+
+extern "C" int32_t slm_kv_pages_free(const slm_ctx *c) {
+    if (!c) return SLM_EINVAL;
+    return c->pages.contiguous ? 0 : c->pages.pages_free();
+}
+
+extern "C" int32_t slm_debug_page_table(const slm_ctx *c, int32_t seq, int32_t *out, int32_t out_len) {
+    if (!c || seq < 0 || seq >= c->cfg.max_batch || (!out && out_len > 0) || out_len < 0) return SLM_EINVAL;
+    const KvPages &kp = c->pages;
+    const int n = std::min(out_len, kp.pps);
+    for (int i = 0; i < n; i++) out[i] = kp.table[(size_t)seq * kp.pps + i];
+    return kp.pps;
 }
 
 extern "C" int32_t slm_seq_len(const slm_ctx *c, int32_t seq) {
@@ -1254,7 +1356,7 @@ extern "C" int slm_debug_cluster(const slm_ctx *c, int32_t *out, int32_t out_len
 extern "C" int slm_debug_fill_kv(slm_ctx *c, float value) {
     if (!c) return SLM_EINVAL;
     const slm_config &g = c->cfg;
-    size_t n = (size_t)g.n_layers * g.max_batch * g.n_kv_heads * g.max_seq * g.head_dim;
+    size_t n = (size_t)g.n_layers * c->pages.npages * g.n_kv_heads * c->pages.rows * g.head_dim;
     fill_kv_kernel<<<1024, 256>>>(c->m.kc, n, value, c->m.kv_bf16);
     fill_kv_kernel<<<1024, 256>>>(c->m.vc, n, value, c->m.kv_bf16);
     CK(c, cudaGetLastError());
@@ -1277,9 +1379,18 @@ extern "C" int slm_debug_copy_kv(slm_ctx *c, int32_t layer, int32_t seq, int32_t
         float *dst = which ? v_host : k_host;
         if (!dst) continue;
         const uint8_t *base = which ? c->m.vc : c->m.kc;
+        const KvPages &kp = c->pages;
         for (int kvh = 0; kvh < g.n_kv_heads; kvh++) {
-            size_t off = ((((size_t)layer * g.max_batch + seq) * g.n_kv_heads + kvh) * g.max_seq) * hd * esz;
-            CK(c, cudaMemcpy(tmp.data(), base + off, (size_t)n * hd * esz, cudaMemcpyDeviceToHost));
+            for (int t = 0; t < n;) {  // one run per page
+                const int pg = kp.table[(size_t)seq * kp.pps + (t >> kp.shift)];
+                const int r0 = kp.contiguous ? t : (t & (kp.rows - 1));
+                const int cnt = std::min(n - t, kp.rows - r0);
+                if (pg < 0) return fail(c, SLM_ESTATE, "position %d of sequence %d has no page", t, seq);
+                const size_t off = ((((size_t)layer * kp.npages + pg) * g.n_kv_heads + kvh) * kp.rows + r0) * hd * esz;
+                CK(c, cudaMemcpy(tmp.data() + (size_t)t * hd * esz, base + off, (size_t)cnt * hd * esz,
+                                 cudaMemcpyDeviceToHost));
+                t += cnt;
+            }
             float *o = dst + (size_t)kvh * n * hd;
             for (size_t i = 0; i < (size_t)n * hd; i++) o[i] = widen(tmp.data(), (int)esz, i);
         }

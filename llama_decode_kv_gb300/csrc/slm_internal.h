@@ -70,7 +70,14 @@ struct Model {
     Mat w2;            // [dim][hidden]
     const float *norms;      // [n_layers][2][dim] (attn, ffn) then [dim] output norm
     const float *rope;       // [max_seq][head_dim/2][2] = (cos, sin)
-    uint8_t *kc, *vc;        // [n_layers][max_batch][KV][max_seq][hd]
+    // KV cache in pages: position p of sequence s is row (p & kv_mask) of page
+    // kv_table[s * kv_pps + (p >> kv_shift)]; a page holds kv_rows rows per (layer, kv
+    // head): kc / vc [n_layers][kv_npages][KV][kv_rows][hd].  Without paging every
+    // sequence owns one page of max_seq rows (page s, kv_shift 31), which is the plain
+    // [n_layers][max_batch][KV][max_seq][hd] layout.
+    uint8_t *kc, *vc;
+    const int *kv_table;     // device [max_batch][kv_pps]
+    int kv_pps, kv_shift, kv_mask, kv_rows, kv_npages;
     // Exchange buffers.  Every element is a tagged 8-byte word (value in the low half,
     // the launch's tag in the high half) so that consumers poll the data itself.  They
     // are per layer: nothing is rewritten within one launch.
@@ -194,12 +201,20 @@ struct ClusterParams {
 };
 
 // Cache replication (cache_ops.cu): positions [0, len) of sequence src into dst[0..n).
-struct ForkArgs {
-    int dst[kMaxBatch];
-    int src;
-    int len;
+// KV cache pages (cache_ops.cu): rows [0, rows[i]) of page src[i] copied into page dst[i],
+// every layer and kv head, keys and values (a fork without paging, or a copy on write).
+struct PageCopies {
+    int n;
+    int src[kMaxBatch], dst[kMaxBatch], rows[kMaxBatch];
 };
-cudaError_t fork_kv(const Model &m, const ForkArgs &a, int n_dst, cudaStream_t stream);
+cudaError_t copy_kv_pages(const Model &m, const PageCopies &a, cudaStream_t stream);
+// Page-table entries written on the device: table[idx[i]] = val[i].
+constexpr int kTableWritesMax = 256;
+struct TableWrites {
+    int n;
+    int idx[kTableWritesMax], val[kTableWritesMax];
+};
+cudaError_t write_kv_table(int *table, const TableWrites &w, cudaStream_t stream);
 
 // Next-token sampling (sampling.cu), one CTA per row.
 constexpr int kMaxTopK = 1024;

@@ -199,7 +199,8 @@ def test_llama1b_long_context_workload(slm):
 
 
 @pytest.mark.slow
-def test_long_context_2layer_against_oracle(slm):
+@pytest.mark.parametrize("page", [0, 256])
+def test_long_context_2layer_against_oracle(slm, page):
     """4 rows x (32768-token prompt + 8 greedy decode steps) with the Llama-3.2-1B attention
     geometry (32 query heads, 8 kv heads, head_dim 64, bf16 KV, theta 500000) in a 2-layer
     model small enough for the oracle to prefill offline (tests/golden/long2l_row*.npz).
@@ -207,7 +208,8 @@ def test_long_context_2layer_against_oracle(slm):
     kernel's split-K attention over 32k cached positions (long chunks per work item);
     every logit of every row and step is compared with the oracle's (teacher forcing),
     ids under the gap rule.  The invariant behind it: cached generation equals the plain
-    recomputation (GOTOken, "About one token per second")."""
+    recomputation (GOTOken, "About one token per second").  page = 256: the same on a
+    paged cache of 256-position pages."""
     wl = synth.WORKLOADS["llama1b_long_2l"]
     s = wl.shape
     W = synth.make_weights(s)
@@ -218,7 +220,7 @@ def test_long_context_2layer_against_oracle(slm):
     prompts = [synth.make_prompt(s, r, wl.prompt_len) for r in range(wl.batch)]
     for r, g in gold.items():
         assert np.array_equal(g["prompt"], prompts[r])
-    eng = slm.Engine(s, W)
+    eng = slm.Engine(s, W, kv_page_size=page)
     dev = torch.device("cuda")
     toks = torch.as_tensor(np.concatenate(prompts).astype(np.int32), device=dev)
     last = torch.empty((wl.batch, s.vocab), dtype=torch.float32, device=dev)
