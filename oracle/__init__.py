@@ -24,7 +24,8 @@ _SO = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1
+F32, BF16, Q8 = 0, 1, 2
+Q8_BLOCK = 32
 OK, EINVAL, ENOMEM, ECAPACITY, EPOS, ESTATE = 0, -1, -2, -3, -4, -5
 
 
@@ -82,6 +83,7 @@ def lib():
                 "orc_attend": (None, [_P, _P, _P, _P, _I, _I, _P]),
                 "orc_silu_mul": (None, [_P, _P, _P, _I]),
                 "orc_argmax": (_I32, [_P, _I]),
+                "orc_quantize_q8_row": (None, [_P, _I, _P, _P]),
                 "orc_weight_count": (ctypes.c_size_t, [ctypes.POINTER(Config)]),
                 "orc_create": (_I, [ctypes.POINTER(Config), _P, ctypes.c_size_t, ctypes.POINTER(_P)]),
                 "orc_destroy": (None, [_P]),
@@ -172,6 +174,16 @@ def silu_mul(a, b) -> np.ndarray:
 def argmax(x) -> int:
     x = _f32(x)
     return int(lib().orc_argmax(_ptr(x), x.size))
+
+
+def quantize_q8_row(w) -> Tuple[np.ndarray, np.ndarray]:
+    """One weight row to int8 blocks of Q8_BLOCK: (q int8[n], d float32[ceil(n / 32)])."""
+    w = _f32(w).ravel()
+    n = w.size
+    q = np.zeros(n, dtype=np.int8)
+    d = np.zeros((n + Q8_BLOCK - 1) // Q8_BLOCK, dtype=np.float32)
+    lib().orc_quantize_q8_row(_ptr(w), n, _ptr(q), _ptr(d))
+    return q, d
 
 
 # ------------------------------------------------------------------ the model

@@ -37,6 +37,14 @@
  * rounded to fp32; query head h reads kv head h / (H/KV); softmax subtracts the max,
  * exponentiates with expf, divides by the ascending sum, then weights V; argmax takes
  * the lowest index on a tie; a bf16 KV cache rounds k and v to nearest-even on append.
+ *
+ * Block-quantised int8 weights (kasahare 0.4.0, "Where to go from here": INT8 weight
+ * loading, block-quantised like GGUF; the pages give no format, so this is the plainest
+ * one): every row of every projection matrix and of the tied embedding is cut into
+ * blocks of ORC_Q8_BLOCK consecutive elements (the last block of a row may be shorter);
+ * a block keeps d = max|w| / 127 and q_i = w_i / d rounded to the nearest integer, halves
+ * away from zero (an all-zero block: d = 0, q = 0).  The weight the model then uses is
+ * the fp32 product d * q_i; nothing else changes.  The norm gains stay fp32.
  */
 #include "oracle.h"
 
@@ -132,6 +140,45 @@ void orc_silu_mul(float *h, const float *a, const float *b, int n) {
     for (int i = 0; i < n; i++) h[i] = (a[i] / (1.0f + expf(-a[i]))) * b[i];
 }
 
+/* one row of n weights to int8 blocks of ORC_Q8_BLOCK: q[n], d[ceil(n / ORC_Q8_BLOCK)] */
+void orc_quantize_q8_row(const float *w, int n, int8_t *q, float *d) {
+    for (int b0 = 0, blk = 0; b0 < n; b0 += ORC_Q8_BLOCK, blk++) {
+        int b1 = b0 + ORC_Q8_BLOCK < n ? b0 + ORC_Q8_BLOCK : n;
+        float amax = 0.0f;
+        for (int i = b0; i < b1; i++) {
+            float a = fabsf(w[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / 127.0f;
+        d[blk] = s;
+        for (int i = b0; i < b1; i++) {
+            float v = s > 0.0f ? roundf(w[i] / s) : 0.0f;
+            if (v > 127.0f) v = 127.0f;
+            if (v < -127.0f) v = -127.0f;
+            q[i] = (int8_t)v;
+        }
+    }
+}
+
+/* replace each of `rows` rows of n weights by its block-quantised value d * q */
+static int q8_dequantize_rows(float *w, size_t rows, int n) {
+    int8_t *q = malloc((size_t)n);
+    float *d = malloc(((size_t)n / ORC_Q8_BLOCK + 1) * sizeof(float));
+    if (!q || !d) {
+        free(q);
+        free(d);
+        return ORC_ENOMEM;
+    }
+    for (size_t r = 0; r < rows; r++) {
+        float *row = w + r * (size_t)n;
+        orc_quantize_q8_row(row, n, q, d);
+        for (int i = 0; i < n; i++) row[i] = d[i / ORC_Q8_BLOCK] * (float)q[i];
+    }
+    free(q);
+    free(d);
+    return ORC_OK;
+}
+
 int32_t orc_argmax(const float *x, int n) {
     int32_t best = 0;
     for (int i = 0; i < n; i++)
@@ -165,7 +212,7 @@ static int cfg_ok(const orc_config *c) {
         return 0;
     if (c->n_heads % c->n_kv_heads) return 0;
     if (c->head_dim % 2) return 0;
-    if (c->weight_dtype != ORC_F32 && c->weight_dtype != ORC_BF16) return 0;
+    if (c->weight_dtype != ORC_F32 && c->weight_dtype != ORC_BF16 && c->weight_dtype != ORC_Q8) return 0;
     if (c->kv_dtype != ORC_F32 && c->kv_dtype != ORC_BF16) return 0;
     if (!(c->norm_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return 0;
     return 1;
@@ -265,6 +312,23 @@ int orc_create(const orc_config *cfg, const void *weights, size_t nbytes, orc_mo
         L->w2 = p; p += dim * hid;
     }
     m->out_norm = p;
+    if (c->weight_dtype == ORC_Q8) { /* fp32 input weights, quantised matrix by matrix */
+        int rc = q8_dequantize_rows((float *)m->emb, (size_t)c->vocab, (int)dim);
+        for (int l = 0; l < c->n_layers && rc == ORC_OK; l++) {
+            orc_layer *L = &m->layers[l];
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->wq, qd, (int)dim);
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->wk, kvd, (int)dim);
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->wv, kvd, (int)dim);
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->wo, dim, (int)qd);
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->w1, hid, (int)dim);
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->w3, hid, (int)dim);
+            if (rc == ORC_OK) rc = q8_dequantize_rows((float *)L->w2, dim, (int)hid);
+        }
+        if (rc != ORC_OK) {
+            orc_destroy(m);
+            return rc;
+        }
+    }
     *out = m;
     return ORC_OK;
 }

@@ -13,7 +13,8 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_Q8 = 2 };
+enum { ORC_Q8_BLOCK = 32 };
 enum {
     ORC_OK = 0,
     ORC_EINVAL = -1,
@@ -41,6 +42,7 @@ void orc_attend(float *out, const float *q, const float *kc, const float *vc, in
                 int head_dim, float *scores);
 void orc_silu_mul(float *h, const float *a, const float *b, int n);
 int32_t orc_argmax(const float *x, int n);
+void orc_quantize_q8_row(const float *w, int n, int8_t *q, float *d);
 
 /* the model */
 size_t orc_weight_count(const orc_config *c);

@@ -33,6 +33,7 @@ import numpy as np
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DTYPE_Q8 = 2  # block-quantised int8 weights: the input buffer is fp32, quantised by the consumer
 
 WEIGHT_SEED = 1234
 PROMPT_SEED = 5678

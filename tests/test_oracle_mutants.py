@@ -37,6 +37,21 @@ MUTANTS = {
 }
 
 
+# block-quantised int8 weights: caught by tests/test_oracle_q8.py
+Q8_MUTANTS = {
+    "q8 halves to even": ("float v = s > 0.0f ? roundf(w[i] / s) : 0.0f;", "float v = s > 0.0f ? rintf(w[i] / s) : 0.0f;"),
+    "q8 scale over 128": ("float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    "q8 blocks of 16": ("b1 = b0 + ORC_Q8_BLOCK < n ? b0 + ORC_Q8_BLOCK : n;", "b1 = b0 + 16 < n ? b0 + 16 : n;"),
+    "q8 embedding left unquantised": ("int rc = q8_dequantize_rows((float *)m->emb, (size_t)c->vocab, (int)dim);",
+                                      "int rc = ORC_OK;"),
+    "q8 w2 blocks along the output axis": ("rc = q8_dequantize_rows((float *)L->w2, dim, (int)hid);",
+                                           "rc = q8_dequantize_rows((float *)L->w2, hid, (int)dim);"),
+}
+PIN_FILE = {name: "test_oracle_pins.py" for name in MUTANTS}
+PIN_FILE.update({name: "test_oracle_q8.py" for name in Q8_MUTANTS})
+MUTANTS.update(Q8_MUTANTS)
+
+
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, tmp_path):
     old, new = MUTANTS[name]
@@ -50,6 +65,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                     "-o", str(so), str(mut), "-lm"], check=True)
     env = dict(os.environ, ORACLE_SO=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", PIN_FILE[name])],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
