@@ -243,6 +243,37 @@ def prefill_measure(slm, torch, W, local: int, reps: int = 3):
     return t, flops
 
 
+def paged_measure(slm, torch, W, local: int, steps: int, warmup: int, page: int = 64):
+    """The headline workload on a paged KV cache (`page`-position pages): the same prompt,
+    warm-up and number of steps as the main timed region, so the same contexts; device
+    ids fed back.  Returns ms per step (the overhead of the page table is the ratio to
+    the contiguous cache's)."""
+    wl = synth.WORKLOADS[WORKLOAD]
+    s = wl.shape
+    dev = torch.device("cuda", local)
+    eng = slm.Engine(s, W, kv_page_size=page)
+    toks = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(2)]
+    prompt = synth.make_prompt(s, 0, wl.prompt_len)
+    _, nid = eng.prefill_checked(0, prompt, want_logits=False)
+    toks[0].copy_(nid)
+    pos, cur = len(prompt), 0
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warmup + steps):
+        if i == warmup:
+            torch.cuda.synchronize()
+            a.record(stream)
+        if eng.decode_step([0], toks[cur], [pos], None, toks[1 - cur]) != 0:
+            raise RuntimeError(f"paged decode: {eng.last_error()}")
+        pos, cur = pos + 1, 1 - cur
+    b.record(stream)
+    torch.cuda.synchronize()
+    if eng.sync() != 0:
+        raise RuntimeError(f"device status after the paged run: {eng.last_error()}")
+    eng.close()
+    return a.elapsed_time(b) / steps
+
+
 def batch16_measure(slm, torch, W, local: int, warmup: int = 3):
     """The SmolLM2 batch-16 workload: 16 independent rows with a bf16 KV cache, each
     prefilled with a seeded 512-token prompt (tensor-core prefill, untimed), then batched
@@ -562,6 +593,8 @@ def run_ours(args, world, rank, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = e2e_steps * wl.batch * world / e2e_s
 
+    eng.reset(0)
+    paged_ms = paged_measure(slm, torch, W, local, args.steps, max(args.warmup, 3))
     pf_t, pf_flops = prefill_measure(slm, torch, W, local)
     tflops_peak, tflops_kind = peaks_tensor()
     b16 = batch16_measure(slm, torch, W, local)
@@ -608,6 +641,10 @@ def run_ours(args, world, rank, local):
                     "tflops": pf_flops / pf_t / 1e12, "peak_tflops": tflops_peak, "peak_kind": tflops_kind,
                     "frac": pf_flops / pf_t / 1e12 / tflops_peak, "bound": "tensor",
                     "note": "activation operands split into bf16 hi + lo: the tensor cores execute 2x these FLOPs"},
+        "paged": {"what": "the same workload, steps and contexts on a paged KV cache (64-position pages, "
+                          "slm_config.kv_page_size = 64)",
+                  "ms_per_step": paged_ms, "tokens_per_s": wl.batch * 1e3 / paged_ms,
+                  "overhead_vs_contiguous": paged_ms / (total_ms / args.steps) - 1.0},
         "batch16": b16,
         **llama,
         "clocks": clk,

@@ -41,7 +41,7 @@ extern "C" {
 #endif
 
 /* element types */
-enum { SLM_F32 = 0, SLM_BF16 = 1 };
+enum { SLM_F32 = 0, SLM_BF16 = 1, SLM_Q8 = 2 };
 
 /* status codes */
 enum {
@@ -63,9 +63,14 @@ enum {
  * MHA, 1 for MQA: kasahare "Architecture"), head_dim, hidden (SwiGLU width), vocab.
  * max_seq is the per-sequence cache capacity (GOTOken keeps a fixed context constant;
  * kasahare preallocates its KvSlots), max_batch the number of sequence slots.
- * Embeddings are always tied (kasahare "Optimisations").  weight_dtype: SLM_F32 or
- * SLM_BF16.  kv_dtype: the cache element type, SLM_F32 or SLM_BF16 (rounded to
- * nearest-even on append).
+ * Embeddings are always tied (kasahare "Optimisations").  weight_dtype: SLM_F32,
+ * SLM_BF16, or SLM_Q8: block-quantised int8 (kasahare 0.4.0, "Where to go from here":
+ * INT8 weights, block-quantised like GGUF), given as fp32 weights and quantised by
+ * slm_create with slm_quantize_q8: every row of the embedding and of each projection
+ * matrix in blocks of 32, about 1.125 bytes per weight on the device; the norm gains
+ * stay fp32.  Single-row steps of int8 engines run on the persistent kernel and their
+ * prompts are prefilled one position at a time.  kv_dtype: the cache element type,
+ * SLM_F32 or SLM_BF16 (rounded to nearest-even on append).
  * Requirements: all counts > 0, dim a multiple of 4, n_heads % n_kv_heads == 0, head_dim a multiple of 8
  * and <= 256, max_batch <= 16, norm_eps >= 0, rope_theta > 0.  Shapes whose fp32
  * activation tile (max_batch x input width) cannot fit in shared memory give
@@ -212,6 +217,18 @@ int slm_fork(slm_ctx *ctx, int32_t src, int32_t n_dst, const int32_t *dst_seqs, 
  */
 int slm_sample(int32_t batch, int32_t vocab, const float *logits, int32_t ld, float temperature, int32_t top_k,
                float top_p, const float *uniforms, int32_t *next_ids, void *stream);
+
+/*
+ * slm_quantize_q8 -- block-quantised int8 weights (the SLM_Q8 format).  Needs no context
+ * or device: a host function.  For each of `rows` rows of `cols` fp32 weights (w[rows][cols],
+ * row-major) and each block of 32 consecutive weights of the row (the last block of a
+ * row holds cols % 32 of them when cols is not a multiple of 32): d = max|w| / 127 (fp32)
+ * and q = w / d rounded to the nearest integer, halves away from zero, in [-127, 127]; an
+ * all-zero block has d = 0 and q = 0.  The weight this represents is d * q.
+ *   q: host int8[rows][cols]; d: host float[rows][ceil(cols / 32)].
+ *   Returns SLM_OK, or SLM_EINVAL for NULL pointers, rows < 0 or cols < 1.
+ */
+int slm_quantize_q8(const float *w, int32_t rows, int32_t cols, int8_t *q, float *d);
 
 /* slm_seq_len -- current length of a sequence (>= 0), or a negative SLM_E* code. */
 int32_t slm_seq_len(const slm_ctx *ctx, int32_t seq);

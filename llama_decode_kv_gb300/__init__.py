@@ -51,6 +51,7 @@ _SIGS = {
     "slm_reset": (ctypes.c_int, [_P, _I32]),
     "slm_seq_len": (_I32, [_P, _I32]),
     "slm_kv_pages_free": (_I32, [_P]),
+    "slm_quantize_q8": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "slm_debug_page_table": (_I32, [_P, _I32, _P, _I32]),
     "slm_fork": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
     "slm_prefill_batch": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P]),
@@ -141,6 +142,20 @@ def sample(logits, temperature: float, top_k: int, top_p: float, uniforms, next_
     batch, ld = int(logits.shape[0]), int(logits.shape[1])
     return slm_sample(batch, ld, _ptr(logits), ld, float(temperature), int(top_k), float(top_p), _ptr(uniforms),
                       _ptr(next_ids), _stream_ptr(stream))
+
+
+def quantize_q8(w: np.ndarray):
+    """slm_quantize_q8 on a [rows][cols] fp32 array: (q int8[rows][cols], d float32[rows][ceil(cols/32)])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    if w.ndim == 1:
+        w = w[None, :]
+    rows, cols = w.shape
+    q = np.zeros((rows, cols), dtype=np.int8)
+    d = np.zeros((rows, (cols + 31) // 32), dtype=np.float32)
+    rc = slm_quantize_q8(w.ctypes.data, rows, cols, q.ctypes.data, d.ctypes.data)
+    if rc != 0:
+        raise SlmError(rc, "slm_quantize_q8")
+    return q, d
 
 
 def plan(shape, sms: int = 152) -> dict:

@@ -482,7 +482,7 @@ __device__ __forceinline__ void walk_load(const ClusterParams &P, CS &S, const P
     c_wait_slot(P.m, &S.full[ci % slots], (ci / slots) & 1);
     wk.buf = S.ring + (size_t)(ci % slots) * kChunkBytes;
     wk.nr = min(ph.upc, ph.units - wk.j * ph.upc) * ph.rpu;
-    load_pieces<1, kRG, WBF16>(wk.gw.w, wk.buf, ph.rowbytes, wk.nr, threadIdx.x & 31, kbp / (WBF16 ? 8 : 4));
+    load_pieces<1, kRG, WBF16>(wk.gw, wk.buf, ph.rowbytes, wk.nr, threadIdx.x & 31, kbp / (WBF16 ? 8 : 4), kbp);
 }
 
 template <bool WBF16>

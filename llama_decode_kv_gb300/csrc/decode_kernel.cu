@@ -331,12 +331,11 @@ __device__ void cursor_enter(const StepParams &P, Cursor &c) {
 // Next chunk of the sequence; false at the end.
 __device__ bool cursor_next(const StepParams &P, Cursor &c, Chunk &out) {
     const Model &m = P.m;
-    const int esz = m.weight_bf16 ? 2 : 4;
     while (!c.done) {
         const Mat &M = phase_mat(m, c.phase);
         if (c.u < c.u1) {
             const int cu = M.rows_per_chunk / M.rows_per_unit;
-            const long long rowbytes = (long long)M.KBp * esz;
+            const long long rowbytes = tile_rowbytes(m.weight_type, M.KBp);
             const int nunits = min(cu, c.u1 - c.u);
             out.src = M.base + (long long)(c.phase == 4 ? 0 : c.layer) * M.layer_stride +
                       ((long long)c.kt * M.rows + (long long)c.u * M.rows_per_unit) * rowbytes;
@@ -413,7 +412,9 @@ __device__ __forceinline__ void producer(const StepParams &P, Shared &S) {
 enum Epi { EPI_QKV = 0, EPI_WO = 1, EPI_W13 = 2, EPI_W2 = 3, EPI_LOGITS = 4 };
 
 __device__ __forceinline__ float emb_elem(const Model &m, int tok, int k) {
-    const uint8_t *row = m.emb.base + (long long)tok * m.emb.KBp * (m.weight_bf16 ? 2 : 4);
+    const uint8_t *row = m.emb.base + (long long)tok * tile_rowbytes(m.weight_type, m.emb.KBp);
+    if (m.weight_type == kWQ8)  // scale of k's block times its int8 value
+        return ((const float *)(row + m.emb.KBp))[k / kQ8Block] * (float)((const int8_t *)row)[k];
     if (m.weight_bf16) {
         uint16_t b = ((const uint16_t *)row)[k];
         return __uint_as_float((uint32_t)b << 16);
@@ -519,7 +520,7 @@ __device__ void zero_pad(const StepParams &P, float *xs, int ld, int from, bool 
 // the Wo input tile: o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 __device__ __forceinline__ void merge_chunk_states(const StepParams &P, int layer, const Mat &M, Shared &S, int pld) {
     const Model &m = P.m;
-    const bool perm = m.weight_bf16;
+    const bool perm = m.x_perm;
     const int H = m.n_heads, hd = m.head_dim, st = hd + 2;
     int ncmax = 1;
     for (int b = 0; b < P.batch; b++) ncmax = max(ncmax, P.nchunk[b]);
@@ -563,9 +564,9 @@ template <int NB>
 __device__ __forceinline__ void stage_input(const StepParams &P, int epi, int layer, const Mat &M, int kt, Shared &S) {
     const Model &m = P.m;
     const int tid = threadIdx.x;
-    const bool perm = m.weight_bf16;
+    const bool perm = m.x_perm;
     const int pl = perm ? M.KBp : 0;
-    const int pld = (NB == kMaxBatch && perm) ? M.KBp + 8 : 0;  // activation planes (tensor-core phases)
+    const int pld = (NB == kMaxBatch && m.weight_bf16) ? M.KBp + 8 : 0;  // activation planes (tensor-core phases)
     float *dst = S.xs;
     const int dld = pld ? pld : M.KBp;
     compute_sync();  // everyone is done with the previous tile
@@ -715,18 +716,18 @@ struct Cand {
 
 // The dots of a prepared group, the warp reduction and the epilogue.  rs1: 1/rms of the
 // single batch row when NB = 1 (RMSNorm inputs).
-template <int NB, int RG, int RPU, bool WBF16>
+template <int NB, int RG, int RPU, int WT>
 __device__ __forceinline__ Cand group_compute(const StepParams &P, const Mat &M, Shared &S,
-                                              const GroupW<NB, RG, WBF16> &G, const EpiCtx &c, const uint8_t *base,
+                                              const GroupW<NB, RG, WT> &G, const EpiCtx &c, const uint8_t *base,
                                               int nr, int kt, float rs1) {
     constexpr int V = RG * NB;
     constexpr int SHIFT = 5 - Log2<V>::value;
     const Model &m = P.m;
     const int lane = threadIdx.x & 31;
-    const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
+    const size_t rowbytes = (size_t)tile_rowbytes(WT, M.KBp);
     Cand cd{-INFINITY, 0, 0};
     float acc[V];
-    rows_dot<NB, RG, WBF16>(G, base, rowbytes, nr, S.xs, M.KBp, P.batch, acc);
+    rows_dot<NB, RG, WT>(G, base, rowbytes, nr, S.xs, M.KBp, P.batch, acc);
     const float val = reduce_scatter<V>(acc);
     float second = 0.f;
     if constexpr (RPU == 2) second = __shfl_sync(0xffffffffu, val, ((((lane >> SHIFT) + NB) << SHIFT) & 31));
@@ -814,7 +815,7 @@ __device__ __forceinline__ bool is_norm_input(int epi) { return epi == EPI_QKV |
 // waits for its first chunk's weights, loads its first group's pieces into registers
 // and prepares that group's epilogue; after the poll only the arithmetic and the
 // stores remain.  Returns the updated chunk counter.
-template <int NB, bool WBF16, int RG>
+template <int NB, int WT, int RG>
 __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                                uint32_t chunk_i, int tslot) {
     // RG: rows of a group (8 at batch 1 when chunks hold at least 4 rows, else 2)
@@ -827,14 +828,14 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
     const int cpk = (u1 - u0 + cu - 1) / cu;            // chunks per K tile
     const int nch = M.nkt * cpk;
     const uint32_t slots = (uint32_t)P.ring_slots;
-    const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
-    const int pieces = M.KBp / (WBF16 ? 8 : 4);
+    const size_t rowbytes = (size_t)tile_rowbytes(WT, M.KBp);
+    const int pieces = M.KBp / Piece<WT>::elems;
     const bool pairs = M.rows_per_unit == 2;
     // the warp's chunks of the phase: j, j + 8, ...; the current group: units [g, g + ng)
     // of chunk j
     int j = (warp - (int)(chunk_i & 7)) & 7;
     int g = 0, ng = 0;
-    GroupW<NB, RG, WBF16> wp;
+    GroupW<NB, RG, WT> wp;
     EpiCtx ctx;
     const uint8_t *buf = nullptr;
     // Prepare the group at unit g of chunk j: weights of its first pieces into registers,
@@ -846,7 +847,7 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
         ng = min(nunits - g, RG / M.rows_per_unit);  // batches: 2 rows share each activation load
         if (g == 0) wait_slot(P, &S.full[ci % slots], (ci / slots) & 1);
         buf = S.ring + (size_t)(ci % slots) * kChunkBytes + (size_t)g * M.rows_per_unit * rowbytes;
-        load_pieces<NB, RG, WBF16>(wp.w, buf, rowbytes, ng * M.rows_per_unit, lane, pieces);
+        load_pieces<NB, RG, WT>(wp, buf, rowbytes, ng * M.rows_per_unit, lane, pieces, M.KBp);
         ctx = pairs ? prepare_ctx<NB, RG, 2>(P, epi, layer, u0, unit0, g, ng)
                     : prepare_ctx<NB, RG, 1>(P, epi, layer, u0, unit0, g, ng);
     };
@@ -860,9 +861,9 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
         while (j < nch && j < (kt + 1) * cpk) {
             const int unit0 = (j - kt * cpk) * cu, nunits = min(cu, u1 - u0 - unit0);
             if (pairs)
-                group_compute<NB, RG, 2, WBF16>(P, M, S, wp, ctx, buf, ng * 2, kt, rs1);
+                group_compute<NB, RG, 2, WT>(P, M, S, wp, ctx, buf, ng * 2, kt, rs1);
             else
-                group_compute<NB, RG, 1, WBF16>(P, M, S, wp, ctx, buf, ng, kt, rs1);
+                group_compute<NB, RG, 1, WT>(P, M, S, wp, ctx, buf, ng, kt, rs1);
             g += ng;
             if (g >= nunits) {  // chunk done: release its slot, move to the warp's next one
                 __syncwarp();
@@ -880,7 +881,7 @@ __device__ __forceinline__ uint32_t layer_walk(const StepParams &P, int epi, int
 
 // The logits: chunks of up to R rows per group (8 at batch 1), each lane keeping the
 // best (value, index) per batch row.
-template <int NB, bool WBF16, bool G8>
+template <int NB, int WT, bool G8>
 __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &M, Shared &S, uint32_t chunk_i, int tslot,
                                                 float (&best_v)[NB], int (&best_i)[NB]) {
     constexpr int R = NB == 1 ? (G8 ? 8 : 2) : GemvShape<NB>::R;
@@ -892,8 +893,8 @@ __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &
     const int cu = M.rows_per_chunk;
     const int nch = (u1 - u0 + cu - 1) / cu;
     const uint32_t slots = (uint32_t)P.ring_slots;
-    const size_t rowbytes = (size_t)M.KBp * (WBF16 ? 2 : 4);
-    const int pieces = M.KBp / (WBF16 ? 8 : 4);
+    const size_t rowbytes = (size_t)tile_rowbytes(WT, M.KBp);
+    const int pieces = M.KBp / Piece<WT>::elems;
     int j = (warp - (int)(chunk_i & 7)) & 7;
     if (j < nch) wait_slot(P, &S.full[(chunk_i + (uint32_t)j) % slots], ((chunk_i + (uint32_t)j) / slots) & 1);
     stage_input<NB>(P, EPI_LOGITS, 0, M, 0, S);
@@ -909,16 +910,16 @@ __device__ __forceinline__ uint32_t logits_walk(const StepParams &P, const Mat &
         for (int g = 0; g < nunits; g += R) {
             const int ng = min(R, nunits - g);
             if (R > 1 && ng == 1) {
-                GroupW<NB, 1, WBF16> w;
-                load_pieces<NB, 1, WBF16>(w.w, buf + (size_t)g * rowbytes, rowbytes, 1, lane, pieces);
+                GroupW<NB, 1, WT> w;
+                load_pieces<NB, 1, WT>(w, buf + (size_t)g * rowbytes, rowbytes, 1, lane, pieces, M.KBp);
                 const EpiCtx c = prepare_ctx<NB, 1, 1>(P, EPI_LOGITS, 0, u0, unit0, g, 1);
-                keep_best<NB>(group_compute<NB, 1, 1, WBF16>(P, M, S, w, c, buf + (size_t)g * rowbytes, 1, 0, rs1),
+                keep_best<NB>(group_compute<NB, 1, 1, WT>(P, M, S, w, c, buf + (size_t)g * rowbytes, 1, 0, rs1),
                               best_v, best_i);
             } else {
-                GroupW<NB, R, WBF16> w;
-                load_pieces<NB, R, WBF16>(w.w, buf + (size_t)g * rowbytes, rowbytes, ng, lane, pieces);
+                GroupW<NB, R, WT> w;
+                load_pieces<NB, R, WT>(w, buf + (size_t)g * rowbytes, rowbytes, ng, lane, pieces, M.KBp);
                 const EpiCtx c = prepare_ctx<NB, R, 1>(P, EPI_LOGITS, 0, u0, unit0, g, ng);
-                keep_best<NB>(group_compute<NB, R, 1, WBF16>(P, M, S, w, c, buf + (size_t)g * rowbytes, ng, 0, rs1),
+                keep_best<NB>(group_compute<NB, R, 1, WT>(P, M, S, w, c, buf + (size_t)g * rowbytes, ng, 0, rs1),
                               best_v, best_i);
             }
         }
@@ -1124,26 +1125,26 @@ __device__ __forceinline__ uint32_t mma_walk(const StepParams &P, int epi, int l
     return chunk_i + (uint32_t)nch;
 }
 
-template <int NB, bool WBF16, bool G8>
+template <int NB, int WT, bool G8>
 __device__ __forceinline__ uint32_t gemv_phase(const StepParams &P, int epi, int layer, const Mat &M, Shared &S,
                                             uint32_t chunk_i, int tslot) {
-    if constexpr (NB == kMaxBatch && WBF16) {  // batch 16: tensor cores
+    if constexpr (NB == kMaxBatch && WT == kWBF16) {  // batch 16: tensor cores
         float bv[2];
         int bi[2];
         return mma_walk<false>(P, epi, layer, M, S, chunk_i, tslot, bv, bi);
     } else {
-        return layer_walk<NB, WBF16, (NB == 1 && G8) ? 8 : 2>(P, epi, layer, M, S, chunk_i, tslot);
+        return layer_walk<NB, WT, (NB == 1 && G8) ? 8 : 2>(P, epi, layer, M, S, chunk_i, tslot);
     }
 }
 
 // The logits and the greedy argmax: per lane, per warp, per CTA best candidates (lowest
 // index on ties); CTA 0 collects every CTA's candidate.
-template <int NB, bool WBF16, bool G8>
+template <int NB, int WT, bool G8>
 __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uint32_t chunk_i, int tslot) {
     const Model &m = P.m;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int batch = P.batch;
-    if constexpr (NB == kMaxBatch && WBF16) {
+    if constexpr (NB == kMaxBatch && WT == kWBF16) {
         // lane (g4, t4) holds candidates of batch rows g4 and g4 + 8: reduce over t4
         float bv[2] = {-INFINITY, -INFINITY};
         int bi[2] = {0x7fffffff, 0x7fffffff};
@@ -1177,7 +1178,7 @@ __device__ __forceinline__ void logits_phase(const StepParams &P, Shared &S, uin
         best_v[b] = -INFINITY;
         best_i[b] = 0x7fffffff;
     }
-    logits_walk<NB, WBF16, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
+    logits_walk<NB, WT, G8>(P, m.emb, S, chunk_i, tslot, best_v, best_i);
     trace_mark(P, tslot + 1, 0);
     compute_sync();  // the logits phase is done with S.xs
 #pragma unroll
@@ -1410,7 +1411,7 @@ __device__ __forceinline__ void attention_phase(const StepParams &P, int layer, 
 
 // G8: batch-1 row groups of up to 8 rows (models whose chunks hold several rows);
 // otherwise groups of 2 rows or one pair.
-template <int NB, bool WBF16, bool G8>
+template <int NB, int WT, bool G8>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ StepParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Shared S = carve(smem_raw, P);
@@ -1424,7 +1425,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     }
     __syncthreads();
     if (tid >= kComputeThreads) {
-        if (tid == kComputeThreads) producer<NB == kMaxBatch && WBF16>(P, S);
+        if (tid == kComputeThreads) producer<NB == kMaxBatch && WT == kWBF16>(P, S);
         return;
     }
     const Model &m = P.m;
@@ -1443,10 +1444,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
             }
             const int epi = ph == 0 ? EPI_QKV : ph == 2 ? EPI_WO : ph == 3 ? EPI_W13 : EPI_W2;
             const Mat M = ph == 0 ? m.qkv : ph == 2 ? m.wo : ph == 3 ? m.w13 : m.w2;
-            chunk_i = gemv_phase<NB, WBF16, G8>(P, epi, l, M, S, chunk_i, t);
+            chunk_i = gemv_phase<NB, WT, G8>(P, epi, l, M, S, chunk_i, t);
         }
     }
-    if (P.do_logits) logits_phase<NB, WBF16, G8>(P, S, chunk_i, m.n_layers * kTracePerLayer);
+    if (P.do_logits) logits_phase<NB, WT, G8>(P, S, chunk_i, m.n_layers * kTracePerLayer);
 }
 
 // ------------------------------------------------------------------ host-side launch
@@ -1455,9 +1456,9 @@ size_t decode_smem_bytes(int max_batch, int own_ld, int acc_bytes, int xs_bytes,
     return ring_offset(max_batch, own_ld, acc_bytes, xs_bytes) + (size_t)ring_slots * kChunkBytes;
 }
 
-template <int NB, bool WBF16, bool G8>
+template <int NB, int WT, bool G8>
 static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
-    auto fn = decode_step_kernel<NB, WBF16, G8>;
+    auto fn = decode_step_kernel<NB, WT, G8>;
     const size_t smem = decode_smem_bytes(P.m.max_batch, P.own_ld, P.acc_bytes, P.xs_bytes, P.ring_slots);
     static size_t smem_set = 0;  // the attribute only grows; set it once per size (host latency per step)
     if (smem > smem_set) {
@@ -1469,20 +1470,26 @@ static cudaError_t launch_nb(const StepParams &P, cudaStream_t stream) {
     return cudaLaunchCooperativeKernel((const void *)fn, dim3(P.grid), dim3(kThreads), args, smem, stream);
 }
 
-template <bool WBF16>
+template <int WT>
 static cudaError_t launch_w(const StepParams &P, cudaStream_t stream) {
-    if (P.batch <= 1) return P.wide_groups ? launch_nb<1, WBF16, true>(P, stream) : launch_nb<1, WBF16, false>(P, stream);
-    if (P.batch <= 4) return launch_nb<4, WBF16, false>(P, stream);
-    if (P.batch <= 8) return launch_nb<8, WBF16, false>(P, stream);
-    return launch_nb<16, WBF16, false>(P, stream);
+    if (P.batch <= 1) return P.wide_groups ? launch_nb<1, WT, true>(P, stream) : launch_nb<1, WT, false>(P, stream);
+    if (P.batch <= 4) return launch_nb<4, WT, false>(P, stream);
+    if (P.batch <= 8) return launch_nb<8, WT, false>(P, stream);
+    return launch_nb<16, WT, false>(P, stream);
 }
 
 cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream) {
-    return P.m.weight_bf16 ? launch_w<true>(P, stream) : launch_w<false>(P, stream);
+    switch (P.m.weight_type) {
+    case kWQ8: return launch_w<kWQ8>(P, stream);
+    case kWBF16: return launch_w<kWBF16>(P, stream);
+    default: return launch_w<kWF32>(P, stream);
+    }
 }
 
-cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm) {
-    auto fn = weight_bf16 ? decode_step_kernel<1, true, true> : decode_step_kernel<1, false, true>;
+cudaError_t decode_occupancy(int weight_type, size_t smem, int *blocks_per_sm) {
+    auto fn = weight_type == kWQ8     ? decode_step_kernel<1, kWQ8, true>
+              : weight_type == kWBF16 ? decode_step_kernel<1, kWBF16, true>
+                                      : decode_step_kernel<1, kWF32, true>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, kThreads, smem);

@@ -1,7 +1,11 @@
-// gemv.cuh -- the CUDA-core GEMV building blocks of the decode kernels: bf16 (or fp32)
-// weight rows from shared memory times fp32 activation rows, fp32 accumulation, and a
-// transposing warp reduction.  Used by the persistent decode kernel and by the cluster
-// decode kernel.
+// gemv.cuh -- the CUDA-core GEMV building blocks of the decode kernels: weight rows
+// from shared memory (fp32, bf16, or block-quantised int8) times fp32 activation rows,
+// fp32 accumulation, and a transposing warp reduction.  Used by the persistent decode
+// kernel and by the cluster decode kernel.
+//
+// Weight types WT: kWF32 (pieces of 4 elements, 16 bytes), kWBF16 (8 elements, 16
+// bytes), kWQ8 (8 int8 elements, 8 bytes; a stored row is its KBp int8 values followed by
+// one fp32 scale per block of 32, and an element is scale * value).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -50,35 +54,67 @@ template <int NB, int RG> struct Unroll {
     static constexpr int value = RG * NB >= 8 ? 1 : RG * NB >= 4 ? 2 : 3;
 };
 
+template <int WT> struct Piece {
+    static constexpr int elems = WT == kWF32 ? 4 : 8;  // elements per piece
+    static constexpr int bytes = WT == kWQ8 ? 8 : 16;
+};
+
+// 8 int8 weights (two words) to floats: each byte, sign bit flipped, becomes the low
+// mantissa byte of 1.5 * 2^23 (exact for 0..255), and subtracting 1.5 * 2^23 + 128
+// leaves the signed value.
+__device__ __forceinline__ void q8_unpack(uint32_t lo, uint32_t hi, float (&v)[8]) {
+    const uint32_t a = lo ^ 0x80808080u, b = hi ^ 0x80808080u;
+    const float off = 12583040.0f;  // 1.5 * 2^23 + 128
+    v[0] = __uint_as_float(__byte_perm(a, 0x4B400000u, 0x7650)) - off;
+    v[1] = __uint_as_float(__byte_perm(a, 0x4B400000u, 0x7651)) - off;
+    v[2] = __uint_as_float(__byte_perm(a, 0x4B400000u, 0x7652)) - off;
+    v[3] = __uint_as_float(__byte_perm(a, 0x4B400000u, 0x7653)) - off;
+    v[4] = __uint_as_float(__byte_perm(b, 0x4B400000u, 0x7650)) - off;
+    v[5] = __uint_as_float(__byte_perm(b, 0x4B400000u, 0x7651)) - off;
+    v[6] = __uint_as_float(__byte_perm(b, 0x4B400000u, 0x7652)) - off;
+    v[7] = __uint_as_float(__byte_perm(b, 0x4B400000u, 0x7653)) - off;
+}
+
 // A lane's first U pieces of each of a group's RG weight rows, held in registers: for
-// the layer phases they are loaded before the input vector is polled.
-template <int NB, int RG, bool WBF16>
+// the layer phases they are loaded before the input vector is polled.  (int8 weights:
+// with each piece's block scale.)
+template <int NB, int RG, int WT>
 struct GroupW {
     static constexpr int U = Unroll<NB, RG>::value;
     uint4 w[U][RG];
+    float sc[WT == kWQ8 ? U : 1][WT == kWQ8 ? RG : 1];
 };
 
-// Row r of the group at base + r * rowbytes; rows >= nr read as zero.
-template <int NB, int RG, bool WBF16>
-__device__ __forceinline__ void load_pieces(uint4 (&w)[Unroll<NB, RG>::value][RG], const uint8_t *base, size_t rowbytes,
-                                            int nr, int p0, int pieces) {
+// Row r of the group at base + r * rowbytes; rows >= nr read as zero.  kbp: elements
+// per stored row (where an int8 row's scales start).
+template <int NB, int RG, int WT>
+__device__ __forceinline__ void load_pieces(GroupW<NB, RG, WT> &G, const uint8_t *base, size_t rowbytes, int nr, int p0,
+                                            int pieces, int kbp) {
 #pragma unroll
     for (int u = 0; u < Unroll<NB, RG>::value; u++)
 #pragma unroll
         for (int r = 0; r < RG; r++) {
             const int p = p0 + 32 * u;
-            w[u][r] = (p < pieces && r < nr) ? ((const uint4 *)(base + (size_t)r * rowbytes))[p] : make_uint4(0, 0, 0, 0);
+            const bool on = p < pieces && r < nr;
+            const uint8_t *row = base + (size_t)r * rowbytes;
+            if constexpr (WT == kWQ8) {
+                const uint2 q = on ? ((const uint2 *)row)[p] : make_uint2(0, 0);
+                G.w[u][r] = make_uint4(q.x, q.y, 0, 0);
+                G.sc[u][r] = on ? ((const float *)(row + kbp))[p >> 2] : 0.f;
+            } else {
+                G.w[u][r] = on ? ((const uint4 *)row)[p] : make_uint4(0, 0, 0, 0);
+            }
         }
 }
 
 // acc[u][r * NB + b] += piece (p0 + 32 u) of row r . the same piece of staged row b.
-template <int NB, int RG, bool WBF16>
-__device__ __forceinline__ void fma_pieces(const uint4 (&w)[Unroll<NB, RG>::value][RG], int p0, int pieces,
-                                           const float *xs, int KBp, int batch,
-                                           float (&acc)[Unroll<NB, RG>::value][RG * NB]) {
+template <int NB, int RG, int WT>
+__device__ __forceinline__ void fma_pieces(const GroupW<NB, RG, WT> &G, int p0, int pieces, const float *xs, int KBp,
+                                           int batch, float (&acc)[Unroll<NB, RG>::value][RG * NB]) {
     constexpr int U = Unroll<NB, RG>::value;
-    constexpr int EPP = WBF16 ? 8 : 4;
-    (void)EPP;
+    constexpr bool WBF16 = WT != kWF32;  // 8-element pieces, activations in xpos() planes
+    constexpr int EPP = Piece<WT>::elems;
+    const auto &w = G.w;
 #pragma unroll
     for (int u = 0; u < U; u++) {
         const int p = p0 + 32 * u;
@@ -100,7 +136,14 @@ __device__ __forceinline__ void fma_pieces(const uint4 (&w)[Unroll<NB, RG>::valu
             for (int r = 0; r < RG; r++) {
                 const uint4 q = w[u][r];
                 float &a = acc[u][r * NB + b];
-                if constexpr (WBF16) {
+                if constexpr (WT == kWQ8) {
+                    float v[8];
+                    q8_unpack(q.x, q.y, v);
+                    float t = v[0] * x[0];
+#pragma unroll
+                    for (int e = 1; e < 8; e++) t = fmaf(v[e], x[e], t);
+                    a = fmaf(G.sc[u][r], t, a);
+                } else if constexpr (WBF16) {
                     a = fmaf(bf16_lo(q.x), x[0], a);
                     a = fmaf(bf16_hi(q.x), x[1], a);
                     a = fmaf(bf16_lo(q.y), x[2], a);
@@ -122,23 +165,23 @@ __device__ __forceinline__ void fma_pieces(const uint4 (&w)[Unroll<NB, RG>::valu
 
 // Dots of RG weight rows with every staged batch row: the lane's first U pieces per row
 // come from G, the rest from shared memory.  Value index r * NB + b.
-template <int NB, int RG, bool WBF16>
-__device__ __forceinline__ void rows_dot(const GroupW<NB, RG, WBF16> &G, const uint8_t *base, size_t rowbytes, int nr,
+template <int NB, int RG, int WT>
+__device__ __forceinline__ void rows_dot(const GroupW<NB, RG, WT> &G, const uint8_t *base, size_t rowbytes, int nr,
                                          const float *xs, int KBp, int batch, float (&out)[RG * NB]) {
     constexpr int U = Unroll<NB, RG>::value;
     const int lane = threadIdx.x & 31;
-    const int pieces = KBp / (WBF16 ? 8 : 4);
+    const int pieces = KBp / Piece<WT>::elems;
     float acc[U][RG * NB];
 #pragma unroll
     for (int u = 0; u < U; u++)
 #pragma unroll
         for (int v = 0; v < RG * NB; v++) acc[u][v] = 0.f;
-    fma_pieces<NB, RG, WBF16>(G.w, lane, pieces, xs, KBp, batch, acc);
+    fma_pieces<NB, RG, WT>(G, lane, pieces, xs, KBp, batch, acc);
 #pragma unroll 1
     for (int p0 = lane + 32 * U; p0 < pieces; p0 += 32 * U) {
-        uint4 w[U][RG];
-        load_pieces<NB, RG, WBF16>(w, base, rowbytes, nr, p0, pieces);
-        fma_pieces<NB, RG, WBF16>(w, p0, pieces, xs, KBp, batch, acc);
+        GroupW<NB, RG, WT> w;
+        load_pieces<NB, RG, WT>(w, base, rowbytes, nr, p0, pieces, KBp);
+        fma_pieces<NB, RG, WT>(w, p0, pieces, xs, KBp, batch, acc);
     }
 #pragma unroll
     for (int v = 0; v < RG * NB; v++) {

@@ -25,7 +25,7 @@
 
 namespace slm {
 cudaError_t launch_decode_step(const StepParams &P, cudaStream_t stream);
-cudaError_t decode_occupancy(int weight_bf16, size_t smem, int *blocks_per_sm);
+cudaError_t decode_occupancy(int weight_type, size_t smem, int *blocks_per_sm);
 size_t decode_smem_bytes(int max_batch, int own_ld, int acc_bytes, int xs_bytes, int ring_slots);
 cudaError_t cluster_capacity(int weight_bf16, size_t smem, int C, int *clusters);
 cudaError_t cluster_kernel_attrs(int weight_bf16, size_t smem, int C);
@@ -129,17 +129,20 @@ static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // accumulated).  A chunk (one warp's piece of work) holds whole units: enough that a
 // CTA's share (of `ctas` CTAs) splits into about one chunk per warp or more, at most one
 // slot and at most 8 rows (one row group of the batch-1 kernel).
-static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int max_batch,
+static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int wt, int max_batch,
                      bool allow_split, int ctas, size_t budget) {
+    // int8 rows (KB bytes + KB / 8 bytes of scales) are whole 16-byte units, as the bulk
+    // copies into the ring need, when KB is a multiple of 128
+    const size_t pad = wt == kWQ8 ? 128 : kPadElems;
     for (int nkt = 1; nkt <= 64; nkt++) {
-        int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), kPadElems);
+        int KB = (int)round_up((size_t)((K + nkt - 1) / nkt), pad);
         int real_nkt = (K + KB - 1) / KB;
         // batches of more than 8 rows run the tensor-core kernel: 16 rows of bf16 hi + lo
         // planes, padded by 8 elements
         size_t xs = max_batch > 8 ? (size_t)kMaxBatch * (KB + 8) * 4 : (size_t)max_batch * KB * 4;
-        size_t unit_bytes = (size_t)KB * esz * rows_per_unit;
+        size_t unit_bytes = (size_t)tile_rowbytes(wt, KB) * rows_per_unit;
         // (the batch-16 tensor-core kernel pads every bf16 row in the ring by kRowPad)
-        const size_t slot_unit = unit_bytes + (max_batch > 8 && esz == 2 ? (size_t)kRowPad * rows_per_unit : 0);
+        const size_t slot_unit = unit_bytes + (max_batch > 8 && wt == kWBF16 ? (size_t)kRowPad * rows_per_unit : 0);
         if (xs <= budget && slot_unit <= (size_t)kChunkBytes) {
             if (real_nkt > 1 && !allow_split) return false;
             M.rows = rows;
@@ -157,7 +160,7 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
             const int want = (per_cta + kComputeWarps - 1) / kComputeWarps;
             const int upc = std::max(1, std::min(fit, max_batch > 1 && rows_per_unit == 1 ? std::max(2, want) : want));
             M.rows_per_chunk = upc * rows_per_unit;
-            M.layer_stride = (long long)real_nkt * rows * KB * esz;
+            M.layer_stride = (long long)real_nkt * rows * tile_rowbytes(wt, KB);
             return true;
         }
         if (!allow_split) return false;
@@ -167,14 +170,56 @@ static bool plan_mat(Mat &M, int rows, int K, int rows_per_unit, int esz, int ma
 
 // Copy rows [r0, r0 + n) of a row-major [*, K] source into the tiled layout at row
 // offset dst_row0 of a matrix with `rows` rows.
-static void pack_rows(uint8_t *dst, const Mat &M, int dst_row0, const uint8_t *src, int n, int esz) {
-    for (int kt = 0; kt < M.nkt; kt++) {
-        int k0 = kt * M.KB;
-        int kn = std::min(M.KB, M.K - k0);
-        for (int r = 0; r < n; r++) {
-            uint8_t *d = dst + ((size_t)kt * M.rows + dst_row0 + r) * M.KBp * esz;
-            memcpy(d, src + ((size_t)r * M.K + k0) * esz, (size_t)kn * esz);
-            if (kn < M.KBp) memset(d + (size_t)kn * esz, 0, (size_t)(M.KBp - kn) * esz);
+// Block-quantised int8: for each block of kQ8Block consecutive weights of a row (the
+// last block of a row may be shorter), d = max|w| / 127 and q = w / d rounded to the
+// nearest integer, halves away from zero (an all-zero block: d = 0, q = 0).
+extern "C" int slm_quantize_q8(const float *w, int32_t rows, int32_t cols, int8_t *q, float *d) {
+    if (!w || !q || !d || rows < 0 || cols < 1) return SLM_EINVAL;
+    const int nb = (cols + kQ8Block - 1) / kQ8Block;
+    for (int32_t r = 0; r < rows; r++) {
+        const float *wr = w + (size_t)r * cols;
+        for (int b = 0; b < nb; b++) {
+            const int j0 = b * kQ8Block, j1 = std::min(cols, j0 + kQ8Block);
+            float amax = 0.0f;
+            for (int j = j0; j < j1; j++) amax = std::max(amax, std::fabs(wr[j]));
+            const float scale = amax / 127.0f;
+            d[(size_t)r * nb + b] = scale;
+            for (int j = j0; j < j1; j++) {
+                float v = scale > 0.0f ? std::round(wr[j] / scale) : 0.0f;
+                v = std::min(127.0f, std::max(-127.0f, v));
+                q[(size_t)r * cols + j] = (int8_t)v;
+            }
+        }
+    }
+    return SLM_OK;
+}
+
+// Copy rows [r0, r0 + n) of a row-major [*, K] source (elements of `src_esz` bytes) into
+// the tiled layout of weight type wt at row offset dst_row0 of a matrix with `rows`
+// rows.  int8 rows (fp32 source) are quantised here, blocks counted from column 0.
+static void pack_rows(uint8_t *dst, const Mat &M, int dst_row0, const uint8_t *src, int n, int src_esz, int wt = -1) {
+    if (wt < 0) wt = src_esz == 2 ? kWBF16 : kWF32;
+    const size_t rb = (size_t)tile_rowbytes(wt, M.KBp);
+    std::vector<int8_t> q;
+    std::vector<float> d;
+    if (wt == kWQ8) {
+        q.resize(M.K);
+        d.resize((M.K + kQ8Block - 1) / kQ8Block);
+    }
+    for (int r = 0; r < n; r++) {
+        const uint8_t *s = src + (size_t)r * M.K * src_esz;
+        if (wt == kWQ8) slm_quantize_q8((const float *)s, 1, M.K, q.data(), d.data());
+        for (int kt = 0; kt < M.nkt; kt++) {
+            const int k0 = kt * M.KB, kn = std::min(M.KB, M.K - k0);
+            uint8_t *o = dst + ((size_t)kt * M.rows + dst_row0 + r) * rb;
+            memset(o, 0, rb);
+            if (wt == kWQ8) {  // KB is a multiple of kQ8Block: tiles hold whole blocks
+                memcpy(o, q.data() + k0, (size_t)kn);
+                const int b0 = k0 / kQ8Block, nb = (kn + kQ8Block - 1) / kQ8Block;
+                memcpy(o + M.KBp, d.data() + b0, (size_t)nb * 4);
+            } else {
+                memcpy(o, s + (size_t)k0 * src_esz, (size_t)kn * src_esz);
+            }
         }
     }
 }
@@ -234,8 +279,8 @@ static bool config_ok(const slm_config *c, std::string &why) {
         why = buf;
         return false;
     }
-    if (c->weight_dtype != SLM_F32 && c->weight_dtype != SLM_BF16) {
-        why = "weight_dtype must be SLM_F32 or SLM_BF16";
+    if (c->weight_dtype != SLM_F32 && c->weight_dtype != SLM_BF16 && c->weight_dtype != SLM_Q8) {
+        why = "weight_dtype must be SLM_F32, SLM_BF16 or SLM_Q8";
         return false;
     }
     if (c->kv_dtype != SLM_F32 && c->kv_dtype != SLM_BF16) {
@@ -290,7 +335,8 @@ extern "C" void slm_destroy(slm_ctx *ctx) {
 // The engine's work split and shared-memory layout for `sms` CTAs (one per SM): pure
 // arithmetic on the config, no device calls (slm_debug_plan runs it on the host).
 static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
-    const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4;
+    const int wt = cfg->weight_dtype == SLM_Q8 ? kWQ8 : cfg->weight_dtype == SLM_BF16 ? kWBF16 : kWF32;
+    const double esz = wt == kWQ8 ? 1.125 : wt == kWBF16 ? 2.0 : 4.0;  // stored bytes per weight
     const int dim = cfg->dim, H = cfg->n_heads, KV = cfg->n_kv_heads, hd = cfg->head_dim;
     const int hid = cfg->hidden, V = cfg->vocab, L = cfg->n_layers, B = cfg->max_batch;
     const int qd = H * hd, kvd = KV * hd, qkv_rows = qd + 2 * kvd;
@@ -305,7 +351,9 @@ static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
     m.max_seq = cfg->max_seq;
     m.max_batch = B;
     m.norm_eps = cfg->norm_eps;
-    m.weight_bf16 = cfg->weight_dtype == SLM_BF16;
+    m.weight_bf16 = wt == kWBF16;
+    m.weight_type = wt;
+    m.x_perm = wt != kWF32;
     m.kv_bf16 = cfg->kv_dtype == SLM_BF16;
     m.wait_ns = kWaitLimitNs;
     m.fault = 0;
@@ -351,17 +399,17 @@ static int plan_engine(slm_ctx *c, const slm_config *cfg, int sms) {
         return kSmemLimit - (size_t)kMinRingSlots * kChunkBytes - layout_overhead(B, c->own_ld, (int)acc);
     };
     c->acc_bytes = 0;
-    bool planned = plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res, budget(0)) &&
-                   plan_mat(m.w2, dim, hid, 1, esz, B, true, ctas_res, budget(0));
+    bool planned = plan_mat(m.wo, dim, qd, 1, wt, B, true, ctas_res, budget(0)) &&
+                   plan_mat(m.w2, dim, hid, 1, wt, B, true, ctas_res, budget(0));
     if (planned && (m.wo.nkt > 1 || m.w2.nkt > 1)) {
         c->acc_bytes = (int)acc_bytes_for(c->own_ld);
-        planned = plan_mat(m.wo, dim, qd, 1, esz, B, true, ctas_res, budget(c->acc_bytes)) &&
-                  plan_mat(m.w2, dim, hid, 1, esz, B, true, ctas_res, budget(c->acc_bytes));
+        planned = plan_mat(m.wo, dim, qd, 1, wt, B, true, ctas_res, budget(c->acc_bytes)) &&
+                  plan_mat(m.w2, dim, hid, 1, wt, B, true, ctas_res, budget(c->acc_bytes));
     }
     const size_t bn = budget(c->acc_bytes) - (size_t)dim * 4;
-    planned = planned && plan_mat(m.emb, V, dim, 1, esz, B, false, grid, bn) &&
-              plan_mat(m.qkv, qkv_rows, dim, 2, esz, B, false, ctas_qkv, bn) &&
-              plan_mat(m.w13, 2 * hid, dim, 2, esz, B, false, ctas_w13, bn);
+    planned = planned && plan_mat(m.emb, V, dim, 1, wt, B, false, grid, bn) &&
+              plan_mat(m.qkv, qkv_rows, dim, 2, wt, B, false, ctas_qkv, bn) &&
+              plan_mat(m.w13, 2 * hid, dim, 2, wt, B, false, ctas_w13, bn);
     if (!planned)
         return fail(c, SLM_EUNSUPPORTED,
                     "activation tile of max_batch=%d rows does not fit in shared memory for this shape", B);
@@ -411,6 +459,10 @@ static void plan_cluster(slm_ctx *c, int clusters, int C, std::string &why) {
             why = "disabled by SLM_NO_CLUSTER";
             return;
         }
+    if (m.weight_type == kWQ8) {
+        why = "int8 weights run on the persistent kernel";
+        return;
+    }
     const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4, kvesz = cfg->kv_dtype == SLM_BF16 ? 2 : 4;
     const int dim = cfg->dim, H = cfg->n_heads, KV = cfg->n_kv_heads, hd = cfg->head_dim, hid = cfg->hidden;
     const int G = H / KV, qd = H * hd, kvd = KV * hd;
@@ -502,7 +554,7 @@ static void plan_cluster(slm_ctx *c, int clusters, int C, std::string &why) {
 static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, size_t nbytes) {
     std::string why;
     if (!config_ok(cfg, why)) return fail(c, SLM_EINVAL, "bad config: %s", why.c_str());
-    const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4;
+    const int esz = cfg->weight_dtype == SLM_BF16 ? 2 : 4;  // of the caller's weights (int8: fp32 in)
     const size_t n_w = weight_count(cfg);
     if (nbytes != n_w * esz)
         return fail(c, SLM_EINVAL, "weights are %zu bytes, the config needs %zu", nbytes, n_w * esz);
@@ -523,7 +575,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     (void)qkv_rows;
     (void)grid;
     int per_sm = 0;
-    CK(c, decode_occupancy(m.weight_bf16, c->smem, &per_sm));
+    CK(c, decode_occupancy(m.weight_type, c->smem, &per_sm));
     if (per_sm < 1) return fail(c, SLM_EUNSUPPORTED, "decode kernel does not fit on an SM (%zu B smem)", c->smem);
     {
         // clusters of 16 CTAs (measured faster at the SmolLM2 shape: less work per CTA
@@ -559,7 +611,8 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
     }
     const size_t al = 256;
     size_t off_emb = 0;
-    size_t off_qkv = round_up(off_emb + (size_t)m.emb.nkt * V * m.emb.KBp * esz, al);
+    const int wt = m.weight_type;
+    size_t off_qkv = round_up(off_emb + (size_t)m.emb.nkt * V * tile_rowbytes(wt, m.emb.KBp), al);
     size_t off_wo = round_up(off_qkv + (size_t)L * m.qkv.layer_stride, al);
     size_t off_w13 = round_up(off_wo + (size_t)L * m.wo.layer_stride, al);
     size_t off_w2 = round_up(off_w13 + (size_t)L * m.w13.layer_stride, al);
@@ -586,7 +639,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         cur += count;
         return p;
     };
-    pack_rows(h.data() + off_emb, m.emb, 0, take((size_t)V * dim), V, esz);
+    pack_rows(h.data() + off_emb, m.emb, 0, take((size_t)V * dim), V, esz, wt);
     float *norms = (float *)(h.data() + off_norm);
     for (int l = 0; l < L; l++) {
         const uint8_t *an = take(dim);
@@ -598,8 +651,8 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         const int G = H / KV, half = hd / 2;
         auto pack_head = [&](int dst0, const uint8_t *src) {
             for (int i = 0; i < half; i++) {
-                pack_rows(qkv, m.qkv, dst0 + 2 * i, src + (size_t)i * dim * esz, 1, esz);
-                pack_rows(qkv, m.qkv, dst0 + 2 * i + 1, src + (size_t)(i + half) * dim * esz, 1, esz);
+                pack_rows(qkv, m.qkv, dst0 + 2 * i, src + (size_t)i * dim * esz, 1, esz, wt);
+                pack_rows(qkv, m.qkv, dst0 + 2 * i + 1, src + (size_t)(i + half) * dim * esz, 1, esz, wt);
             }
         };
         for (int g = 0; g < KV; g++) {
@@ -609,7 +662,7 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
             pack_head(r0 + (G + 1) * hd, wv + (size_t)g * hd * dim * esz);
         }
         const uint8_t *wo_src = take((size_t)dim * qd);
-        pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, wo_src, dim, esz);
+        pack_rows(h.data() + off_wo + (size_t)l * m.wo.layer_stride, m.wo, 0, wo_src, dim, esz, wt);
         if (c->cl_on) {  // [kv head g][dim][wo_kbp]: columns g G hd .. (g + 1) G hd - 1 of Wo
             uint8_t *dst = h.data() + off_wog + (size_t)l * wo_g_stride;
             const size_t gw = (size_t)Gq * hd;
@@ -623,11 +676,11 @@ static int create_impl(slm_ctx *c, const slm_config *cfg, const void *weights, s
         const uint8_t *w3 = take((size_t)hid * dim);
         uint8_t *w13 = h.data() + off_w13 + (size_t)l * m.w13.layer_stride;
         for (int j = 0; j < hid; j++) {  // interleave gate and up rows
-            pack_rows(w13, m.w13, 2 * j, w1 + (size_t)j * dim * esz, 1, esz);
-            pack_rows(w13, m.w13, 2 * j + 1, w3 + (size_t)j * dim * esz, 1, esz);
+            pack_rows(w13, m.w13, 2 * j, w1 + (size_t)j * dim * esz, 1, esz, wt);
+            pack_rows(w13, m.w13, 2 * j + 1, w3 + (size_t)j * dim * esz, 1, esz, wt);
         }
         const uint8_t *w2_src = take((size_t)dim * hid);
-        pack_rows(h.data() + off_w2 + (size_t)l * m.w2.layer_stride, m.w2, 0, w2_src, dim, esz);
+        pack_rows(h.data() + off_w2 + (size_t)l * m.w2.layer_stride, m.w2, 0, w2_src, dim, esz, wt);
         if (c->cl_on) {  // [FFN cluster f][dim][w2_kbp]: columns f hpc .. (f + 1) hpc - 1 of W2
             uint8_t *dst = h.data() + off_w2c + (size_t)l * w2_c_stride;
             for (int f = 0; f < cp.NF; f++) {

@@ -58,10 +58,20 @@ struct Mat {
     int rows_per_chunk;  // multiple of rows_per_unit
 };
 
+// Weight storage types: fp32, bf16, block-quantised int8 (a stored row of a K tile is
+// its KBp int8 values, then one fp32 scale per block of kQ8Block elements).
+constexpr int kWF32 = 0, kWBF16 = 1, kWQ8 = 2;
+constexpr int kQ8Block = 32;
+__host__ __device__ inline long long tile_rowbytes(int wt, int KBp) {
+    return wt == kWQ8 ? (long long)KBp + (long long)(KBp / kQ8Block) * 4 : (long long)KBp * (wt == kWBF16 ? 2 : 4);
+}
+
 struct Model {
     int dim, n_layers, n_heads, n_kv_heads, head_dim, hidden, vocab, max_seq, max_batch;
     float norm_eps;
-    int weight_bf16;   // 1 = bf16 weights, 0 = fp32
+    int weight_bf16;   // 1 = bf16 weights, 0 = fp32 or int8
+    int weight_type;   // kWF32, kWBF16 or kWQ8
+    int x_perm;        // activation tiles in the xpos() order (8-element weight pieces)
     int kv_bf16;       // 1 = bf16 cache, 0 = fp32
     Mat emb;           // [vocab][dim], also the tied output projection
     Mat qkv;           // [(H + 2 KV) hd][dim]: per kv group g, its G q heads, k, v rows

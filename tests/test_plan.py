@@ -19,7 +19,21 @@ def _shapes():
                for n, wl in synth.WORKLOADS.items())
     out["smol_b8_f32"] = synth.SMOL.replace(max_batch=8, weight_dtype=synth.DTYPE_F32)
     out["llama_b4"] = synth.LLAMA1B.replace(max_batch=4)
+    # block-quantised int8 weights
+    out["smol_b1_q8"] = synth.SMOL.replace(weight_dtype=synth.DTYPE_Q8)
+    out["smol_b16_q8"] = synth.SMOL.replace(max_batch=16, weight_dtype=synth.DTYPE_Q8, kv_dtype=synth.DTYPE_BF16)
+    out["llama_b1_q8"] = synth.LLAMA1B.replace(max_batch=1, weight_dtype=synth.DTYPE_Q8)
+    out["llama_b8_q8"] = synth.LLAMA1B.replace(weight_dtype=synth.DTYPE_Q8)
+    out["tiny_ragged_q8"] = synth.TINY.replace(max_batch=3, weight_dtype=synth.DTYPE_Q8, dim=72, n_heads=3,
+                                               n_kv_heads=1, head_dim=24, hidden=100, vocab=333)
     return out
+
+
+def _rowbytes(s, KBp):
+    """Stored bytes of one row of one K tile: int8 rows carry one fp32 scale per 32."""
+    if s.weight_dtype == synth.DTYPE_Q8:
+        return KBp + KBp // 32 * 4
+    return KBp * (2 if s.weight_dtype == synth.DTYPE_BF16 else 4)
 
 
 @pytest.mark.parametrize("name", sorted(_shapes()))
@@ -38,7 +52,9 @@ def test_plan_invariants(name, sms):
         assert M["nkt"] * M["KB"] >= M["K"] > (M["nkt"] - 1) * M["KB"], mname
         assert M["KBp"] % 64 == 0 and M["KBp"] >= M["KB"], mname
         assert M["rows_per_chunk"] % M["rows_per_unit"] == 0 and M["rows_per_chunk"] <= 8, mname
-        assert M["rows_per_chunk"] * (M["KBp"] * esz + pad) <= CHUNK, mname
+        assert M["rows_per_chunk"] * (_rowbytes(s, M["KBp"]) + pad) <= CHUNK, mname
+        # every row starts on a 16-byte boundary (the ring's bulk copies need it)
+        assert _rowbytes(s, M["KBp"]) % 16 == 0, mname
         tile = 16 * (M["KBp"] + 8) * 4 if B > 8 else B * M["KBp"] * 4
         extra = s.dim * 4 if mname in ("emb", "qkv", "w13") else 0
         assert tile + extra <= p["xs_bytes"], mname
