@@ -464,6 +464,56 @@ def llama_measure(slm, torch, W, local: int, name: str, steps: int, warmup: int 
                         "tokens_per_s": pf_tokens / (pf_ms / 1e3)}}
 
 
+def q8_weight_bytes(s) -> int:
+    """Device bytes of block-quantised int8 weights: every matrix row stores one byte per
+    weight plus a 4-byte scale per block of 32; the norm gains stay fp32."""
+    total = 0
+    for name, _layer, _off, count in synth.layout(s):
+        if name.endswith("norm"):
+            total += 4 * count
+            continue
+        k = s.hidden if name == "w2" else (s.n_heads * s.head_dim if name == "wo" else s.dim)
+        total += (count // k) * (k + 4 * ((k + 31) // 32))
+    return total
+
+
+def q8_measure(slm, torch, local: int, base, prompt_len: int, steps: int, peak: float, warmup: int = 3):
+    """Batch-1 greedy decode with block-quantised int8 weights (slm_config.weight_dtype =
+    SLM_Q8): the prompt is prefilled one position at a time (untimed), then `steps` steps
+    timed with CUDA events, ids fed back on the device.  Bytes per step = the int8 weights
+    and scales once + the K and V rows read."""
+    s = base.replace(weight_dtype=synth.DTYPE_Q8, max_batch=1)
+    W = synth.make_weights(s)  # fp32, quantised by slm_create
+    dev = torch.device("cuda", local)
+    eng = slm.Engine(s, W)
+    del W
+    toks = [torch.zeros(1, dtype=torch.int32, device=dev) for _ in range(2)]
+    _, nid = eng.prefill_checked(0, synth.make_prompt(s, 0, prompt_len), want_logits=False)
+    toks[0].copy_(nid)
+    pos, cur, ctx = prompt_len, 0, []
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warmup + steps):
+        if i == warmup:
+            torch.cuda.synchronize()
+            a.record(stream)
+        if eng.decode_step([0], toks[cur], [pos], None, toks[1 - cur]) != 0:
+            raise RuntimeError(f"int8 decode: {eng.last_error()}")
+        if i >= warmup:
+            ctx.append(pos + 1)
+        pos, cur = pos + 1, 1 - cur
+    b.record(stream)
+    torch.cuda.synchronize()
+    if eng.sync() != 0:
+        raise RuntimeError(f"device status after the int8 run: {eng.last_error()}")
+    eng.close()
+    ms = a.elapsed_time(b) / steps
+    bytes_step = q8_weight_bytes(s) + sum(kv_bytes_read(s, c) for c in ctx) / steps
+    gbs = bytes_step / (ms / 1e3) / 1e9
+    return {"ms_per_step": ms, "tokens_per_s": 1e3 / ms, "steps": steps, "contexts": [min(ctx), max(ctx)],
+            "bytes_per_step": bytes_step, "hbm_gbs": gbs, "roofline_frac": gbs / peak, "peak_gbs": peak}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -606,6 +656,10 @@ def run_ours(args, world, rank, local):
     W_llama = synth.make_weights(synth.LLAMA1B)
     llama = {n: llama_measure(slm, torch, W_llama, local, n, st, peak=peak)
              for n, st in (("llama1b_b1", 64), ("llama1b_b8", 64), ("llama1b_long", 32))}
+    q8 = {"what": "block-quantised int8 weights (SLM_Q8: blocks of 32 per row, fp32 scales), batch 1, "
+                  "fp32 activations and accumulation, persistent kernel",
+          "smol_b1_q8": q8_measure(slm, torch, local, synth.SMOL, wl.prompt_len, args.steps, peak),
+          "llama1b_b1_q8": q8_measure(slm, torch, local, synth.LLAMA1B, 128, 64, peak)}
 
     if rank != 0:
         return
@@ -646,6 +700,7 @@ def run_ours(args, world, rank, local):
                   "ms_per_step": paged_ms, "tokens_per_s": wl.batch * 1e3 / paged_ms,
                   "overhead_vs_contiguous": paged_ms / (total_ms / args.steps) - 1.0},
         "batch16": b16,
+        "int8_weights": q8,
         **llama,
         "clocks": clk,
     }
