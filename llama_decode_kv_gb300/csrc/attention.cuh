@@ -255,6 +255,141 @@ __device__ __forceinline__ void attn_scan(const AttnTask &T, const float (&qv)[k
     }
 }
 
+// The scan of a long chunk on the tensor cores (bf16 cache, head_dim HD = 64, streamed).
+// The chunk is a small dense contraction: the G query heads against the positions' keys,
+// then the weights against the values; as CUDA-core code its per-position instructions
+// (shuffles, the online update) bounded the phase, not HBM.  Here each warp takes
+// passes of 8 positions: S = Q K^T (16 x 8, rows = heads, q as bf16 A fragments,
+// mma.sync m16n8k16), the online softmax on the accumulator rows (quad shuffles), and
+// O += P V (P as bf16 A fragments, mma.sync m16n8k8 over HD / 8 dim tiles) -- the
+// prefill's precision (q and p enter as bf16, fp32 accumulation).  The rows of pass k
+// reach its ring slot S - 1 passes ahead by cp.async, 16 bytes further apart than in
+// the cache so that ldmatrix reads them without bank conflicts.  The warp's state
+// (max, sum, weighted V) of each head j < Gp goes to ws like the CUDA-core scan's.
+template <int HD>
+__device__ __forceinline__ void attn_scan_mma(const AttnTask &T, const float *qs, int Gp, float *ws, int warp,
+                                              int lane) {
+    constexpr int RB = HD * 2, RS = RB + 16, NP = 8;  // row bytes, slot row stride, positions
+    const int t0 = T.t0, t1 = T.t1;
+    const int stride = kComputeWarps * NP;
+    const int slotb = 2 * NP * RS;
+    const int per_warp = T.stream_bytes / kComputeWarps / 16 * 16;
+    const int S = min(kAttnMaxSlots, per_warp / slotb);  // >= 2: the caller checks
+    uint8_t *ring = T.stream + (size_t)warp * per_warp;
+    const int tc = T.tail_t >= 0 ? min(t1, T.tail_t) : t1;
+    const int npass = (t1 - t0 + stride - 1) / stride;
+    const int g4 = lane >> 2, t4 = lane & 3;
+    auto row_off = [&](int t) -> size_t {
+        return T.pages ? (size_t)__ldg(T.pages + (t >> T.page_shift)) * T.page_stride + (size_t)(t & T.page_mask) * RB
+                       : (size_t)t * RB;
+    };
+    // q (already scaled to log2 units) as A fragments: rows = heads, zero past Gp
+    uint32_t qa[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; kk++) {
+        const int c = kk * 16 + 2 * t4;
+        const bool on = g4 < Gp;
+        qa[kk][0] = on ? pack_bf16x2(qs[g4 * HD + c], qs[g4 * HD + c + 1]) : 0u;
+        qa[kk][1] = 0u;
+        qa[kk][2] = on ? pack_bf16x2(qs[g4 * HD + c + 8], qs[g4 * HD + c + 9]) : 0u;
+        qa[kk][3] = 0u;
+    }
+    float o[HD / 8][4];
+#pragma unroll
+    for (int n = 0; n < HD / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // row g4 (this lane's two positions of each pass)
+    int wr = 0, rd = 0;
+    auto issue = [&](int k) {
+        if (k < npass) {
+            const int p0 = t0 + k * stride + warp * NP;
+            const int n = max(0, min(NP, tc - p0)) * (RB / 16);  // 16-byte pieces of K (and of V)
+            uint8_t *dst = ring + (size_t)wr * slotb;
+            const size_t src = n > 0 ? row_off(p0) : 0;  // a pass never crosses a page
+            for (int e = lane; e < n; e += 32) {
+                const int r = e / (RB / 16), pc = e - r * (RB / 16);
+                cp_async16(dst + r * RS + pc * 16, T.kbase + src + (size_t)r * RB + pc * 16);
+                cp_async16(dst + (NP + r) * RS + pc * 16, T.vbase + src + (size_t)r * RB + pc * 16);
+            }
+        }
+        cp_async_commit();
+        wr = wr + 1 == S ? 0 : wr + 1;
+    };
+    for (int k = 0; k < S - 1; k++) issue(k);
+    for (int k = 0; k < npass; k++) {
+        const int p0 = t0 + k * stride + warp * NP;
+        issue(k + S - 1);
+        cp_async_wait_upto(S - 1);
+        __syncwarp();
+        uint8_t *ks = ring + (size_t)rd * slotb, *vs = ks + NP * RS;
+        rd = rd + 1 == S ? 0 : rd + 1;
+        if (p0 + NP > t1) {  // rows past the chunk: zero V (their weights are 0, and 0 * NaN is not)
+            const int r0 = max(0, t1 - p0);
+            for (int e = lane; e < (NP - r0) * (RB / 16); e += 32)
+                *(uint4 *)(vs + (r0 + e / (RB / 16)) * RS + (e % (RB / 16)) * 16) = make_uint4(0, 0, 0, 0);
+            __syncwarp();
+        }
+        if (T.tail_t >= p0 && T.tail_t < p0 + NP) {  // the new position's row from the exchange
+            const int r = T.tail_t - p0;
+            if (lane < RB / 16)
+                *(uint4 *)(ks + r * RS + lane * 16) = *(const uint4 *)(T.tail_k + lane * 16);
+            else if (lane < 2 * (RB / 16))
+                *(uint4 *)(vs + r * RS + (lane - RB / 16) * 16) = *(const uint4 *)(T.tail_v + (lane - RB / 16) * 16);
+            __syncwarp();
+        }
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; kk += 2) {  // two k steps per x4 load
+            uint32_t b[4];
+            ldsm_x4(b, ks + (lane & 7) * RS + (kk * 16 + (lane >> 3) * 8) * 2);
+            mma_bf16_16816(sc, qa[kk], b[0], b[1]);
+            mma_bf16_16816(sc, qa[kk + 1], b[2], b[3]);
+        }
+        const int pa = p0 + 2 * t4;
+        const float s0 = pa < t1 ? sc[0] : -INFINITY, s1 = pa + 1 < t1 ? sc[1] : -INFINITY;
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        if (m_new > m_run) {  // the running max grew (always at the first position)
+            const float corr = fast_exp2(m_run - m_new);  // 0 when m_run = -inf
+            l_run *= corr;
+#pragma unroll
+            for (int n = 0; n < HD / 8; n++) {
+                o[n][0] *= corr;
+                o[n][1] *= corr;
+            }
+            m_run = m_new;
+        }
+        const float p0v = m_run == -INFINITY ? 0.f : fast_exp2(s0 - m_run);
+        const float p1v = m_run == -INFINITY ? 0.f : fast_exp2(s1 - m_run);
+        l_run += p0v + p1v;
+        const uint32_t pa0 = pack_bf16x2(p0v, p1v);
+#pragma unroll
+        for (int nb = 0; nb < HD / 32; nb++) {  // four dim tiles per x4 load
+            uint32_t b[4];
+            ldsm_x4_t(b, vs + (lane & 7) * RS + (nb * 32 + (lane >> 3) * 8) * 2);
+#pragma unroll
+            for (int i = 0; i < 4; i++) mma_bf16_1688(o[nb * 4 + i], pa0, 0u, b[i]);
+        }
+        __syncwarp();  // the slot just read is refilled by the next pass
+    }
+    cp_async_wait_upto(0);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (g4 < Gp) {
+        float *w = ws + ((size_t)warp * kMaxGroupPass + g4) * (HD + 2);
+#pragma unroll
+        for (int n = 0; n < HD / 8; n++) {
+            w[2 + n * 8 + 2 * t4] = o[n][0];
+            w[3 + n * 8 + 2 * t4] = o[n][1];
+        }
+        if (t4 == 0) {
+            w[0] = m_run;
+            w[1] = l_run;
+        }
+    }
+}
+
 // All kComputeThreads threads of the CTA call this.  `scratch` holds
 // kMaxGroupPass * hd + kComputeWarps * kMaxGroupPass * (hd + 2) floats; `flag` one int.
 __device__ __forceinline__ void attn_core(const AttnTask &T, float *scratch, int *flag) {
@@ -282,6 +417,10 @@ __device__ __forceinline__ void attn_core(const AttnTask &T, float *scratch, int
             compute_sync();
             qsrc = qs;
         }
+        if (kvbf16 && hd == 64 && T.stream &&
+            T.stream_bytes / kComputeWarps / 16 * 16 >= 2 * (2 * 8 * (64 * 2 + 16))) {
+            attn_scan_mma<64>(T, qsrc, Gp, ws, warp, lane);  // long chunk: tensor cores
+        } else {
         float qv[kMaxGroupPass][8];
 #pragma unroll
         for (int j = 0; j < kMaxGroupPass; j++)
@@ -322,6 +461,7 @@ __device__ __forceinline__ void attn_core(const AttnTask &T, float *scratch, int
                     w[1] = ls[j];
                 }
             }
+        }
         }
         compute_sync();
         // merge the warps: thread e handles (head j, dim d)
