@@ -911,13 +911,14 @@ static void plan_attention(const slm_ctx *c, StepParams &P) {
         // Item i runs on CTA i mod grid, so the phase lasts ceil(items / grid) chunks: of
         // the chunk lengths up to twice this one, take the one whose busiest CTA reads
         // the fewest positions (rounding each row up to whole chunks can leave a few CTAs
-        // with one item more than the rest).
+        // with one item more than the rest), and of equal ones the longest (fewer items:
+        // each has its own poll, setup and partial state to merge).
         long long best = ch, best_load = -1;
         for (long long cand = ch; cand <= 2 * ch; cand += 32) {
             long long items = 0;
             for (int b = 0; b < P.batch; b++) items += (long long)KV * ((P.pos[b] + cand) / cand);
             const long long load = (items + c->grid - 1) / c->grid * cand;
-            if (best_load < 0 || load < best_load) {
+            if (best_load < 0 || load <= best_load) {
                 best = cand;
                 best_load = load;
             }
