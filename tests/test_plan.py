@@ -93,3 +93,34 @@ def test_shapes_that_do_not_fit_are_refused():
         slm.plan(synth.LLAMA1B.replace(dim=32768, n_heads=256, n_kv_heads=64, hidden=65536))
     with pytest.raises(slm.SlmError):
         slm.plan(synth.TINY.replace(n_kv_heads=3))  # heads not a multiple of kv heads
+
+
+@pytest.mark.parametrize("bad", [
+    dict(kv_page_size=8),            # below 16 positions
+    dict(kv_page_size=48),           # not a power of two
+    dict(kv_page_size=0, kv_pages=4),  # a pool without pages
+    dict(kv_page_size=16, kv_pages=3),  # cannot hold one max_seq sequence (64 / 16 = 4 pages)
+    dict(kv_page_size=16, kv_pages=-1),
+    dict(weight_dtype=3),            # no such weight type
+])
+def test_bad_cache_and_weight_configs_are_refused(bad):
+    cfg = slm.config_from_shape(synth.TINY)
+    for k, v in bad.items():
+        setattr(cfg, k, v)
+    import ctypes
+    import numpy as np
+    out = np.zeros(64, dtype=np.int32)
+    rc = slm.slm_debug_plan(ctypes.byref(cfg), 152, out.ctypes.data, out.size)
+    assert rc == slm.SLM_EINVAL, (bad, rc)
+
+
+@pytest.mark.parametrize("good", [dict(kv_page_size=16), dict(kv_page_size=16, kv_pages=4),
+                                  dict(kv_page_size=1 << 20), dict(weight_dtype=2)])
+def test_paged_and_int8_configs_plan(good):
+    cfg = slm.config_from_shape(synth.TINY)
+    for k, v in good.items():
+        setattr(cfg, k, v)
+    import ctypes
+    import numpy as np
+    out = np.zeros(64, dtype=np.int32)
+    assert slm.slm_debug_plan(ctypes.byref(cfg), 152, out.ctypes.data, out.size) == 0
