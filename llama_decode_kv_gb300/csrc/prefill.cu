@@ -303,7 +303,10 @@ template <int HD>
 static size_t attn_tc_smem() { return (size_t)3 * 64 * (HD + 8) * 2; }
 
 // argmax of one row (lowest index on ties); a NaN sets the status word.
+// Row blockIdx.x of v [rows][n]: its argmax (lowest index on ties) into out[blockIdx.x].
 __global__ void argmax_kernel(const float *v, int n, int *out, int *status) {
+    v += (size_t)blockIdx.x * n;
+    out += blockIdx.x;
     __shared__ float bv[32];
     __shared__ int bi[32];
     float best = -INFINITY;
@@ -541,8 +544,7 @@ cudaError_t prefill_run_batch(const Model &m, const PrefillPlan &p, int nseq, co
             float *lg = (last_logits ? last_logits : p.logits) + (last_logits ? (size_t)first * m.vocab : 0);
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * m.n_layers)], m.emb, k, GEMM_STORE_F32, lg, nullptr,
                        nullptr, m.vocab, m.status, s));
-            for (int j = 0; j < k; j++)
-                argmax_kernel<<<1, 1024, 0, s>>>(lg + (size_t)j * m.vocab, m.vocab, next_ids + first + j, m.status);
+            argmax_kernel<<<k, 1024, 0, s>>>(lg, m.vocab, next_ids + first, m.status);  // one CTA per row
             PF_CK(cudaGetLastError());
         }
         r0 += T;
