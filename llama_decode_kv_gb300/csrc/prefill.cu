@@ -182,8 +182,9 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
     uint16_t *out = out_blk + (size_t)sg.row[sgi] * m.n_heads * HD;
     extern __shared__ __align__(16) uint16_t sm[];
     uint16_t *qs = sm;                  // [QB][LD]
-    uint16_t *ks = qs + QB * LD;        // [KB][LD]
-    uint16_t *vs = ks + KB * LD;        // [KB][LD]
+    // double-buffered keys / values: buffer b = [KB][LD] keys, then [KB][LD] values
+    auto kbuf = [&](int b) { return qs + QB * LD + b * 2 * KB * LD; };
+    auto vbuf = [&](int b) { return qs + QB * LD + b * 2 * KB * LD + KB * LD; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g4 = lane >> 2, t4 = lane & 3;
     const int h = blockIdx.y, KV = m.n_kv_heads, G = m.n_heads / KV, g = h / G;
@@ -211,11 +212,11 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
     const int pos0 = p0 + q0 + warp * 16 + g4, pos1 = pos0 + 8;    // this lane's two rows
     const size_t rowbytes = (size_t)HD * 2;
 
-    for (int k0 = 0; k0 <= last; k0 += KB) {
-        __syncthreads();  // previous block's readers are done
+    // key / value block k0 into buffer b: cp.async pieces, zeros past `last`
+    auto load = [&](int k0, int b) {
         for (int e = tid; e < KB * (HD / 8); e += blockDim.x) {  // 16-byte pieces
             const int j = e / (HD / 8), c = (e - j * (HD / 8)) * 8, kp = k0 + j;
-            uint16_t *kd = ks + j * LD + c, *vd = vs + j * LD + c;
+            uint16_t *kd = kbuf(b) + j * LD + c, *vd = vbuf(b) + j * LD + c;
             if (kp <= last) {
                 const size_t src = kv_row(m, layer, seq, g, kp) * rowbytes + c * 2;
                 cp_async16(kd, m.kc + src);
@@ -225,8 +226,16 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
                 *(uint4 *)vd = make_uint4(0, 0, 0, 0);
             }
         }
-        cp_async_wait_all();
-        __syncthreads();
+        cp_async_commit();
+    };
+    load(0, 0);
+    for (int k0 = 0, kb = 0; k0 <= last; k0 += KB, kb++) {
+        // the next block loads while this one is computed
+        const bool more = k0 + KB <= last;
+        if (more) load(k0 + KB, (kb + 1) & 1);
+        cp_async_wait_upto(more ? 1 : 0);
+        __syncthreads();  // block kb (and its zero fill) is visible to every warp
+        const uint16_t *ks = kbuf(kb & 1), *vs = vbuf(kb & 1);
         // S = Q K^T for 64 keys: 8 tiles of 8 keys
         float sc[KB / 8][4];
 #pragma unroll
@@ -300,6 +309,7 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
                 mma_bf16_16816(o[n + 1], pa, b[2], b[3]);
             }
         }
+        __syncthreads();  // every warp is done with this buffer before the next prefetch fills it
     }
     // row sums over the quad, normalise, store (bf16 hi + lo planes)
     float l0 = lrow[0], l1 = lrow[1];
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
 }
 
 template <int HD>
-static size_t attn_tc_smem() { return (size_t)3 * 64 * (HD + 8) * 2; }
+static size_t attn_tc_smem() { return (size_t)5 * 64 * (HD + 8) * 2; }  // Q + two K / V buffers
 
 // argmax of one row (lowest index on ties); a NaN sets the status word.
 // Row blockIdx.x of v [rows][n]: its argmax (lowest index on ties) into out[blockIdx.x].
