@@ -75,14 +75,6 @@ __device__ __forceinline__ void load_row8(const uint8_t *row, int d0, float (&v)
     }
 }
 
-// 2^x by the SFU instruction (PTX ex2.approx.ftz: relative error about 2^-22, inputs
-// below -126 give 0); softmax weights need no more.
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // This warp's positions of one item: pass k takes positions t0 + (k * warps + warp) * PP
 // ..., one per lane group of LPP lanes (each lane 8 of the head_dim elements).  Every
 // pass scores the position against kMaxGroupPass query heads (heads past the group have

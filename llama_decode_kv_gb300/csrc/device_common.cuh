@@ -99,6 +99,14 @@ __device__ __forceinline__ size_t kv_row(const Model &m, int layer, int seq, int
     return (((size_t)layer * m.kv_npages + page) * m.n_kv_heads + g) * m.kv_rows + (pos & m.kv_mask);
 }
 
+// 2^x by the SFU instruction (PTX ex2.approx.ftz: relative error about 2^-22, inputs
+// below -126 give 0); softmax weights need no more.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- warp-level tensor-core pieces (mma.sync, ldmatrix): bf16 x bf16 -> fp32
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {

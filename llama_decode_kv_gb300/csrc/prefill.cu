@@ -167,36 +167,85 @@ __global__ void rope_append_kernel(const Model m, float *qkv, int layer, const P
 
 // Causal attention of query rows p0 .. p0 + T - 1 of one query head on the tensor cores:
 // a CTA takes 64 rows (4 warps x 16), walks the cached keys / values 64 positions at a
-// time (bf16, copied to padded shared memory with cp.async), S = Q K^T and O += P V by
-// mma.sync m16n8k16 with fp32 accumulation, online softmax in the log2 domain (q is
-// pre-multiplied by log2(e) / sqrt(HD)), causal mask on the blocks that reach the rows'
-// own positions.  Q and P enter the MMAs as bf16.
+// time (bf16, copied to padded shared memory with cp.async through a ring of kAttnStages
+// buffers), S = Q K^T and O += P V by mma.sync m16n8k16 with fp32 accumulation, online
+// softmax in the log2 domain (q is pre-multiplied by log2(e) / sqrt(HD)), causal mask on
+// the blocks that reach the rows' own positions.  Q and P enter the MMAs as bf16.  The
+// CTAs of one (head, sequence) start with the last query block, the one with the most
+// key blocks, so the short ones fill the tail of the launch.
+template <int HD> struct AttnStages {
+    static constexpr int value = HD == 64 ? 3 : 2;  // HD 128: two stages keep 2 CTAs per SM
+};
 template <int HD>
 __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, const float *qkv_blk, uint16_t *out_blk,
                                                               size_t lo_off, int layer, const PfSegs sg) {
     constexpr int QB = 64, KB = 64, LD = HD + 8;  // rows per CTA, keys per block, padded row (elements)
+    constexpr int NST = AttnStages<HD>::value;
     // segment blockIdx.z of the block: its rows, sequence and first position
     const int sgi = blockIdx.z, seq = sg.seq[sgi], p0 = sg.pos0[sgi], T = sg.count[sgi];
-    if ((int)blockIdx.x * QB >= T) return;
+    const int qb = (int)(gridDim.x - 1 - blockIdx.x);  // query block, longest first
+    if (qb * QB >= T) return;
     const float *qkv = qkv_blk + (size_t)sg.row[sgi] * m.qkv.rows;
     uint16_t *out = out_blk + (size_t)sg.row[sgi] * m.n_heads * HD;
     extern __shared__ __align__(16) uint16_t sm[];
     uint16_t *qs = sm;                  // [QB][LD]
-    // double-buffered keys / values: buffer b = [KB][LD] keys, then [KB][LD] values
+    // key / value ring: buffer b = [KB][LD] keys, then [KB][LD] values
     auto kbuf = [&](int b) { return qs + QB * LD + b * 2 * KB * LD; };
     auto vbuf = [&](int b) { return qs + QB * LD + b * 2 * KB * LD + KB * LD; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g4 = lane >> 2, t4 = lane & 3;
     const int h = blockIdx.y, KV = m.n_kv_heads, G = m.n_heads / KV, g = h / G;
-    const int q0 = blockIdx.x * QB;                       // first row of the CTA
+    const int q0 = qb * QB;                               // first row of the CTA
     const int last = p0 + min(T, q0 + QB) - 1;            // last position any row reads
+    const size_t rowbytes = (size_t)HD * 2;
+
+    // key / value block k0 into buffer b as one cp.async group (zeros past `last`); past
+    // the end an empty group, so that every iteration waits for the same group count.
+    // A thread copies the same 16-byte column of rows j0, j0 + RPP, ...; with pages of 64
+    // positions or more (or no paging) the block lies in one page, so one table lookup
+    // gives every row.
+    auto load = [&](int k0, int b) {
+        if (k0 <= last) {
+            constexpr int PPR = HD / 8, RPP = 128 / PPR;  // 16-byte pieces per row, rows per pass
+            const int j0 = tid / PPR, c = (tid % PPR) * 8;
+            const bool one_page = m.kv_shift >= 6;
+            const size_t row0 = one_page ? kv_row(m, layer, seq, g, k0) : 0;
+#pragma unroll
+            for (int i = 0; i < KB / RPP; i++) {
+                const int j = j0 + i * RPP, kp = k0 + j;
+                uint16_t *kd = kbuf(b) + j * LD + c, *vd = vbuf(b) + j * LD + c;
+                if (kp <= last) {
+                    const size_t row = one_page ? row0 + j : kv_row(m, layer, seq, g, kp);
+                    const size_t src = row * rowbytes + c * 2;
+                    cp_async16(kd, m.kc + src);
+                    cp_async16(vd, m.vc + src);
+                } else {
+                    *(uint4 *)kd = make_uint4(0, 0, 0, 0);
+                    *(uint4 *)vd = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    // the first NST - 1 key / value blocks load while the Q tile is read
+#pragma unroll
+    for (int b = 0; b < NST - 1; b++) load(b * KB, b);
+
+    // Q tile: fp32 -> scaled bf16; every thread's 16-byte loads are issued before use
     const float qscale = rsqrtf((float)HD) * 1.4426950408889634f;
-    // Q tile: fp32 -> scaled bf16
-    for (int e = tid; e < QB * HD; e += blockDim.x) {
-        const int r = e / HD, d = e - r * HD, t = q0 + r;
-        float v = 0.f;
-        if (t < T) v = qkv[(size_t)t * m.qkv.rows + ((size_t)g * (G + 2) + (h - g * G)) * HD + d] * qscale;
-        qs[r * LD + d] = f32_to_bf16_bits(v);
+    const size_t qcol = ((size_t)g * (G + 2) + (h - g * G)) * HD;
+    constexpr int QV = QB * HD / 4 / 128;  // float4 per thread
+    float4 qv[QV];
+#pragma unroll
+    for (int i = 0; i < QV; i++) {
+        const int e = (tid + i * 128) * 4, r = e / HD, d = e - r * HD, t = q0 + r;
+        qv[i] = t < T ? *(const float4 *)(qkv + (size_t)t * m.qkv.rows + qcol + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < QV; i++) {
+        const int e = (tid + i * 128) * 4, r = e / HD, d = e - r * HD;
+        *(uint2 *)(qs + r * LD + d) = make_uint2(pack_bf16x2(qv[i].x * qscale, qv[i].y * qscale),
+                                                 pack_bf16x2(qv[i].z * qscale, qv[i].w * qscale));
     }
     __syncthreads();
     uint32_t qa[HD / 16][4];  // A fragments of this warp's 16 rows
@@ -210,32 +259,13 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
     for (int n = 0; n < HD / 8; n++) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};  // rows g4, g4 + 8
     const int pos0 = p0 + q0 + warp * 16 + g4, pos1 = pos0 + 8;    // this lane's two rows
-    const size_t rowbytes = (size_t)HD * 2;
 
-    // key / value block k0 into buffer b: cp.async pieces, zeros past `last`
-    auto load = [&](int k0, int b) {
-        for (int e = tid; e < KB * (HD / 8); e += blockDim.x) {  // 16-byte pieces
-            const int j = e / (HD / 8), c = (e - j * (HD / 8)) * 8, kp = k0 + j;
-            uint16_t *kd = kbuf(b) + j * LD + c, *vd = vbuf(b) + j * LD + c;
-            if (kp <= last) {
-                const size_t src = kv_row(m, layer, seq, g, kp) * rowbytes + c * 2;
-                cp_async16(kd, m.kc + src);
-                cp_async16(vd, m.vc + src);
-            } else {
-                *(uint4 *)kd = make_uint4(0, 0, 0, 0);
-                *(uint4 *)vd = make_uint4(0, 0, 0, 0);
-            }
-        }
-        cp_async_commit();
-    };
-    load(0, 0);
     for (int k0 = 0, kb = 0; k0 <= last; k0 += KB, kb++) {
-        // the next block loads while this one is computed
-        const bool more = k0 + KB <= last;
-        if (more) load(k0 + KB, (kb + 1) & 1);
-        cp_async_wait_upto(more ? 1 : 0);
+        // block kb + NST - 1 loads while this one is computed
+        load(k0 + (NST - 1) * KB, (kb + NST - 1) % NST);
+        cp_async_wait_upto(NST - 1);
         __syncthreads();  // block kb (and its zero fill) is visible to every warp
-        const uint16_t *ks = kbuf(kb & 1), *vs = vbuf(kb & 1);
+        const uint16_t *ks = kbuf(kb % NST), *vs = vbuf(kb % NST);
         // S = Q K^T for 64 keys: 8 tiles of 8 keys
         float sc[KB / 8][4];
 #pragma unroll
@@ -269,7 +299,7 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float c0 = exp2f(mrow[0] - mx0), c1 = exp2f(mrow[1] - mx1);  // exp2(-inf) = 0
+        const float c0 = fast_exp2(mrow[0] - mx0), c1 = fast_exp2(mrow[1] - mx1);  // exp2(-inf) = 0
         mrow[0] = mx0;
         mrow[1] = mx1;
         lrow[0] *= c0;
@@ -285,14 +315,14 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
 #pragma unroll
         for (int kk = 0; kk < KB / 16; kk++) {
             float p[8];
-            p[0] = exp2f(sc[2 * kk][0] - mx0);
-            p[1] = exp2f(sc[2 * kk][1] - mx0);
-            p[2] = exp2f(sc[2 * kk][2] - mx1);
-            p[3] = exp2f(sc[2 * kk][3] - mx1);
-            p[4] = exp2f(sc[2 * kk + 1][0] - mx0);
-            p[5] = exp2f(sc[2 * kk + 1][1] - mx0);
-            p[6] = exp2f(sc[2 * kk + 1][2] - mx1);
-            p[7] = exp2f(sc[2 * kk + 1][3] - mx1);
+            p[0] = fast_exp2(sc[2 * kk][0] - mx0);
+            p[1] = fast_exp2(sc[2 * kk][1] - mx0);
+            p[2] = fast_exp2(sc[2 * kk][2] - mx1);
+            p[3] = fast_exp2(sc[2 * kk][3] - mx1);
+            p[4] = fast_exp2(sc[2 * kk + 1][0] - mx0);
+            p[5] = fast_exp2(sc[2 * kk + 1][1] - mx0);
+            p[6] = fast_exp2(sc[2 * kk + 1][2] - mx1);
+            p[7] = fast_exp2(sc[2 * kk + 1][3] - mx1);
             lrow[0] += p[0] + p[1] + p[4] + p[5];
             lrow[1] += p[2] + p[3] + p[6] + p[7];
             uint32_t pa[4];
@@ -336,7 +366,7 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, con
 }
 
 template <int HD>
-static size_t attn_tc_smem() { return (size_t)5 * 64 * (HD + 8) * 2; }  // Q + two K / V buffers
+static size_t attn_tc_smem() { return (size_t)(1 + 2 * AttnStages<HD>::value) * 64 * (HD + 8) * 2; }  // Q + K / V ring
 
 // argmax of one row (lowest index on ties); a NaN sets the status word.
 // Row blockIdx.x of v [rows][n]: its argmax (lowest index on ties) into out[blockIdx.x].

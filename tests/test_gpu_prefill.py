@@ -127,3 +127,40 @@ def test_batched_prefill_refuses_bad_arguments(slm):
     assert eng.prefill_batch([0, 1], toks, [20, 20], None, ids) == ESTATE
     assert eng.seq_len(0) == 0
     eng.close()
+
+
+def test_batched_prefill_smol_16x512_equals_one_prefill_per_sequence(slm):
+    """The batch-16 workload's prefill at full size: 16 SmolLM2-135M-shaped prompts of 512
+    tokens (bf16 weights and cache) in one slm_prefill_batch call, i.e. one block of 8,192
+    rows through every norm, GEMM, RoPE/append and attention launch, against one prefill
+    per sequence (512-row blocks; the oracle pins that path on the small shapes above).
+    Only the order of fp32 sums may differ (the norm kernels differ by block size), so the
+    logits agree within the bf16-cache tolerance and the ids under the gap rule."""
+    s = synth.SMOL.replace(max_seq=528, max_batch=16, kv_dtype=synth.DTYPE_BF16)
+    W = synth.make_weights(s, seed=61)
+    B, P = 16, 512
+    prompts = [synth.make_prompt(s, r, P) for r in range(B)]
+    dev = torch.device("cuda")
+    a = slm.Engine(s, W)
+    toks = torch.as_tensor(np.concatenate(prompts).astype(np.int32)).to(dev)
+    lg = torch.zeros((B, s.vocab), dtype=torch.float32, device=dev)
+    ids = torch.zeros(B, dtype=torch.int32, device=dev)
+    assert a.prefill_batch(list(range(B)), toks, [P] * B, lg, ids) == 0, a.last_error()
+    assert a.sync() == 0, a.last_error()
+    lg, ids = lg.cpu().numpy(), ids.cpu().numpy()
+    assert np.isfinite(lg).all()
+    b = slm.Engine(s, W)
+    for r in (0, 5, 15):
+        lgb, nid = b.prefill_checked(r, prompts[r], want_logits=True)
+        lgb = lgb.cpu().numpy()
+        check_logits(lg[r], lgb, 2e-2, f"batched vs single prefill, seq {r}")
+        check_id(int(ids[r]), lgb, int(nid.item()), f"batched vs single prefill, seq {r}")
+        for layer in (0, s.n_layers - 1):
+            ka, va = a.kv(layer, r)
+            kb, vb = b.kv(layer, r)
+            assert ka.shape == kb.shape == (s.n_kv_heads, P, s.head_dim)
+            assert np.abs(ka - kb).max() <= 2e-2 * np.abs(kb).max()
+            assert np.abs(va - vb).max() <= 2e-2 * np.abs(vb).max()
+    assert b.sync() == 0
+    a.close()
+    b.close()
