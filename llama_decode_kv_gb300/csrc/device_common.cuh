@@ -107,6 +107,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// ---- programmatic dependent launch (the prefill's chain of kernels)
+//
+// A kernel launched by launch_pdl() may be scheduled while its predecessor in the stream
+// is still running.  pdl_wait() blocks until that predecessor has completed and its
+// memory writes are visible, so it comes before the first read of anything an earlier
+// kernel wrote (and before any write); pdl_trigger() then lets the successor be
+// scheduled.  Both are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at{};
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- warp-level tensor-core pieces (mma.sync, ldmatrix): bf16 x bf16 -> fp32
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {

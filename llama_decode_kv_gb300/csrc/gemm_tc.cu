@@ -157,6 +157,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tn_kernel(const __g
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // A, B and the residual come from earlier kernels (launched with launch_pdl)
+    pdl_trigger();
 
     if (warp == 4 && lane == 0) {
         // producer: for each of this CTA's tiles, A rows m0.., B rows n0.., K block kb;
@@ -360,12 +362,11 @@ cudaError_t gemm_bf16_tn(const GemmArgs &args, cudaStream_t stream) {
     if (!sms && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0) != cudaSuccess) return cudaErrorUnknown;
     const long long mt = (args.M + kBM - 1) / kBM;
     const long long t128 = mt * ((args.N + 127) / 128), t64 = mt * ((args.N + 63) / 64);
-    if (t128 >= 148) {
-        gemm_bf16_tn_kernel<128><<<(unsigned)std::min<long long>(t128, sms), kGemmThreads, kGemmSmem, stream>>>(args);
-    } else {
-        gemm_bf16_tn_kernel<64><<<(unsigned)std::min<long long>(t64, sms), kGemmThreads, kGemmSmem, stream>>>(args);
-    }
-    return cudaGetLastError();
+    if (t128 >= 148)
+        return launch_pdl(gemm_bf16_tn_kernel<128>, dim3((unsigned)std::min<long long>(t128, sms)), dim3(kGemmThreads),
+                          (size_t)kGemmSmem, stream, args);
+    return launch_pdl(gemm_bf16_tn_kernel<64>, dim3((unsigned)std::min<long long>(t64, sms)), dim3(kGemmThreads),
+                      (size_t)kGemmSmem, stream, args);
 }
 
 }  // namespace slm

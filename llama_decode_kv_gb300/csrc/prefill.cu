@@ -42,6 +42,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
 
 // x[t][:] = E[tok[t]] (widened); one CTA per row.
 __global__ void embed_rows_kernel(const Model m, const int *tokens, float *x, int *status) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     int tok = __ldg(tokens + t);
     if (tok < 0 || tok >= m.vocab) {
@@ -64,6 +66,8 @@ __device__ __forceinline__ void split_store(uint16_t *hi, uint16_t *lo, size_t i
 // one CTA per row (a few hundred rows: every thread of the row's CTA takes a few
 // elements, the shortest chain).
 __global__ void rmsnorm_bf16_kernel(const float *x, const float *g, uint16_t *out, size_t lo_off, int dim, float eps) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[32];
     const int t = blockIdx.x;
     const float *r = x + (size_t)t * dim;
@@ -84,6 +88,8 @@ __global__ void rmsnorm_bf16_kernel(const float *x, const float *g, uint16_t *ou
 // CTAs: measured 16.6 -> ~8 us per launch at 8,192 rows of 576).
 __global__ void rmsnorm_bf16_rows_kernel(const float *x, const float *g, uint16_t *out, size_t lo_off, int dim,
                                          float eps, int rows) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (t >= rows) return;
     const float *r = x + (size_t)t * dim;
@@ -94,73 +100,82 @@ __global__ void rmsnorm_bf16_rows_kernel(const float *x, const float *g, uint16_
     for (int k = lane; k < dim; k += 32) split_store(out, out + lo_off, (size_t)t * dim + k, (r[k] * rs) * g[k]);
 }
 
-static void rmsnorm_launch(const float *x, const float *g, uint16_t *out, size_t lo_off, int dim, float eps, int rows,
-                           cudaStream_t s) {
+static cudaError_t rmsnorm_launch(const float *x, const float *g, uint16_t *out, size_t lo_off, int dim, float eps,
+                                  int rows, cudaStream_t s) {
     if (rows >= 2048)
-        rmsnorm_bf16_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, g, out, lo_off, dim, eps, rows);
+        return launch_pdl(rmsnorm_bf16_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, x, g, out, lo_off, dim, eps, rows);
     else
-        rmsnorm_bf16_kernel<<<rows, 256, 0, s>>>(x, g, out, lo_off, dim, eps);
+        return launch_pdl(rmsnorm_bf16_kernel, dim3(rows), dim3(256), 0, s, x, g, out, lo_off, dim, eps);
 }
 
-// RoPE of q (in place) and k; k and v of positions p0 + t appended to the cache.
+// RoPE of q (in place) and k; k and v of positions p0 + t appended to the bf16 cache.
 // qkv rows are grouped per kv head, [q heads g*G .. g*G+G-1; k; v], each head's columns
 // in RoPE pairs (column 2i = dim i, column 2i + 1 = dim i + hd/2, the weights' stored
-// order).  The row is read into shared memory first and written back in natural order.
-// Rows per CTA of the RoPE / append kernel: up to 4, as many row buffers as fit 48 KB.
-static inline int rope_rpc(const Model &m) { return std::max(1, std::min(4, 12288 / m.qkv.rows)); }
+// order); q leaves in natural order.  One warp per row: lane l takes the pairs l, l + 32,
+// ... of every head (hd/2 is a multiple of 32), as 8-byte loads of up to 8 heads at a
+// time, all in flight, before any of those heads is written back.
+static inline int rope_rpc(int rows) { return rows >= 4096 ? 8 : 2; }  // rows (warps) per CTA
 
-// One warp per row, blockDim / 32 rows per CTA, each warp with its own row buffer in
-// shared memory ([qkv.rows] floats per warp).  (One CTA per row measured 33 us per
-// launch at 8,192 rows.)
-template <bool KVBF16>
-__global__ void rope_append_kernel(const Model m, float *qkv, int layer, const PfSegs sg, int rows) {
-    extern __shared__ float rowbufs[];
+template <int HD>
+__global__ void __launch_bounds__(256) rope_append_kernel(const Model m, float *qkv, int layer, const PfSegs sg,
+                                                          int rows) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int HALF = HD / 2, PPL = HALF / 32, CH = 8;  // pairs per lane and head, heads per round
     const int lane = threadIdx.x & 31;
-    float *rowbuf = rowbufs + (size_t)(threadIdx.x >> 5) * m.qkv.rows;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // row of the block
     if (t >= rows) return;  // (no block-wide barrier below: each warp keeps to its row)
     int k = 0;
     while (k + 1 < sg.n && t >= sg.row[k + 1]) k++;
     const int seq = sg.seq[k], pos = sg.pos0[k] + (t - sg.row[k]);
-    const int hd = m.head_dim, half = hd / 2, KV = m.n_kv_heads, G = m.n_heads / KV;
-    const float *rope = m.rope + (size_t)pos * half * 2;
+    const int KV = m.n_kv_heads, G = m.n_heads / KV, S = G + 2, heads = KV * S;
     float *row = qkv + (size_t)t * m.qkv.rows;
-    const size_t rowbytes = (size_t)hd * (KVBF16 ? 2 : 4);
-    for (int e = lane; e < m.qkv.rows; e += 32) rowbuf[e] = row[e];
-    __syncwarp();
-    for (int e = lane; e < KV * (G + 2) * half; e += 32) {
-        const int g = e / ((G + 2) * half), r = e - g * (G + 2) * half;
-        const int j = r / half, i = r - j * half;  // head slot j in the group: q (< G), k (= G), v (= G + 1)
-        const size_t h0 = ((size_t)g * (G + 2) + j) * hd;
-        float *h = row + h0;
-        const float cs = rope[2 * i], sn = rope[2 * i + 1];
-        const float a = rowbuf[h0 + 2 * i], b = rowbuf[h0 + 2 * i + 1];
-        if (j <= G) {
-            const float a2 = a * cs - b * sn, b2 = a * sn + b * cs;
+    float2 cs[PPL];  // (cos, sin) of this lane's pairs at this position
+#pragma unroll
+    for (int p = 0; p < PPL; p++) cs[p] = *(const float2 *)(m.rope + ((size_t)pos * HALF + lane + 32 * p) * 2);
+    for (int j0 = 0; j0 < heads; j0 += CH) {
+        float2 v[CH][PPL];
+#pragma unroll
+        for (int c = 0; c < CH; c++)
+#pragma unroll
+            for (int p = 0; p < PPL; p++)
+                v[c][p] = j0 + c < heads ? *(const float2 *)(row + (size_t)(j0 + c) * HD + 2 * (lane + 32 * p))
+                                         : make_float2(0.f, 0.f);
+        __syncwarp();  // every lane has read these heads before any lane overwrites them
+#pragma unroll
+        for (int c = 0; c < CH; c++) {
+            const int jh = j0 + c;
+            if (jh >= heads) break;
+            const int g = jh / S, j = jh - g * S;  // kv group, slot: q (< G), k (= G), v (= G + 1)
             if (j < G) {
-                h[i] = a2;
-                h[i + half] = b2;
-                continue;
-            }
-            uint8_t *kd = m.kc + kv_row(m, layer, seq, g, pos) * rowbytes;
-            if (KVBF16) {
-                ((uint16_t *)kd)[i] = f32_to_bf16_bits(a2);
-                ((uint16_t *)kd)[i + half] = f32_to_bf16_bits(b2);
+                float *h = row + (size_t)jh * HD;
+#pragma unroll
+                for (int p = 0; p < PPL; p++) {
+                    const int i = lane + 32 * p;
+                    const float a = v[c][p].x, b = v[c][p].y, cn = cs[p].x, sn = cs[p].y;
+                    h[i] = a * cn - b * sn;
+                    h[i + HALF] = a * sn + b * cn;
+                }
             } else {
-                ((float *)kd)[i] = a2;
-                ((float *)kd)[i + half] = b2;
-            }
-        } else {
-            uint8_t *vd = m.vc + kv_row(m, layer, seq, g, pos) * rowbytes;
-            if (KVBF16) {
-                ((uint16_t *)vd)[i] = f32_to_bf16_bits(a);
-                ((uint16_t *)vd)[i + half] = f32_to_bf16_bits(b);
-            } else {
-                ((float *)vd)[i] = a;
-                ((float *)vd)[i + half] = b;
+                uint16_t *d = (uint16_t *)((j == G ? m.kc : m.vc) + kv_row(m, layer, seq, g, pos) * (size_t)(HD * 2));
+#pragma unroll
+                for (int p = 0; p < PPL; p++) {
+                    const int i = lane + 32 * p;
+                    const float a = v[c][p].x, b = v[c][p].y, cn = cs[p].x, sn = cs[p].y;
+                    d[i] = f32_to_bf16_bits(j == G ? a * cn - b * sn : a);
+                    d[i + HALF] = f32_to_bf16_bits(j == G ? a * sn + b * cn : b);
+                }
             }
         }
     }
+}
+
+static cudaError_t rope_launch(const Model &m, float *qkv, int layer, const PfSegs &sg, int rows, cudaStream_t s) {
+    const int rpc = rope_rpc(rows);
+    if (m.head_dim == 64)
+        return launch_pdl(rope_append_kernel<64>, dim3((rows + rpc - 1) / rpc), dim3(32 * rpc), 0, s, m, qkv, layer, sg, rows);
+    else
+        return launch_pdl(rope_append_kernel<128>, dim3((rows + rpc - 1) / rpc), dim3(32 * rpc), 0, s, m, qkv, layer, sg, rows);
 }
 
 // ---- tensor-core causal attention (flash-attention style, mma.sync bf16 -> fp32)
@@ -179,6 +194,8 @@ template <int HD> struct AttnStages {
 template <int HD>
 __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const Model m, const float *qkv_blk, uint16_t *out_blk,
                                                               size_t lo_off, int layer, const PfSegs sg) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int QB = 64, KB = 64, LD = HD + 8;  // rows per CTA, keys per block, padded row (elements)
     constexpr int NST = AttnStages<HD>::value;
     // segment blockIdx.z of the block: its rows, sequence and first position
@@ -371,6 +388,8 @@ static size_t attn_tc_smem() { return (size_t)(1 + 2 * AttnStages<HD>::value) * 
 // argmax of one row (lowest index on ties); a NaN sets the status word.
 // Row blockIdx.x of v [rows][n]: its argmax (lowest index on ties) into out[blockIdx.x].
 __global__ void argmax_kernel(const float *v, int n, int *out, int *status) {
+    pdl_wait();
+    pdl_trigger();
     v += (size_t)blockIdx.x * n;
     out += blockIdx.x;
     __shared__ float bv[32];
@@ -416,7 +435,7 @@ __global__ void argmax_kernel(const float *v, int n, int *out, int *status) {
 
 bool prefill_supported(const Model &m) {
     return m.weight_bf16 && m.kv_bf16 && m.dim % 64 == 0 && (m.n_heads * m.head_dim) % 64 == 0 &&
-           m.hidden % 8 == 0 && (m.head_dim == 64 || m.head_dim == 128) && (size_t)m.qkv.rows * 4 <= 48 * 1024;
+           m.hidden % 8 == 0 && (m.head_dim == 64 || m.head_dim == 128);
 }
 
 // Two maps per weight matrix: boxes of 64 rows (64-column tiles) and of 128 rows.
@@ -488,12 +507,11 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
     } while (0)
     for (int p0 = 0; p0 < n; p0 += p.rows) {
         const int T = n - p0 < p.rows ? n - p0 : p.rows;
-        embed_rows_kernel<<<T, 256, 0, s>>>(m, tokens + p0, p.x, m.status);
-        PF_CK(cudaGetLastError());
+        PF_CK(launch_pdl(embed_rows_kernel, dim3(T), dim3(256), 0, s, m, tokens + p0, p.x, m.status));
         const size_t xlo = (size_t)p.rows * m.dim, olo = (size_t)p.rows * qd, hlo = (size_t)p.rows * m.hidden;
         for (int l = 0; l < m.n_layers; l++) {
             const float *gn = m.norms + (size_t)l * 2 * m.dim;
-            rmsnorm_launch(p.x, gn, p.xn, xlo, m.dim, m.norm_eps, T, s);
+            PF_CK(rmsnorm_launch(p.x, gn, p.xn, xlo, m.dim, m.norm_eps, T, s));
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 0)], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
                        m.qkv.rows, m.status, s));
             PfSegs one{};
@@ -502,29 +520,29 @@ cudaError_t prefill_run(const Model &m, const PrefillPlan &p, int seq, const int
             one.pos0[0] = p0;
             one.count[0] = T;
             one.row[0] = 0;
-            rope_append_kernel<true><<<(T + rope_rpc(m) - 1) / rope_rpc(m), 32 * rope_rpc(m), (size_t)rope_rpc(m) * m.qkv.rows * 4, s>>>(m, p.qkv, l, one, T);
+            PF_CK(rope_launch(m, p.qkv, l, one, T, s));
             dim3 ag((T + 63) / 64, m.n_heads, 1);
             if (m.head_dim == 64)
-                attn_prefill_tc_kernel<64><<<ag, 128, attn_tc_smem<64>(), s>>>(m, p.qkv, p.o, olo, l, one);
+                PF_CK(launch_pdl(attn_prefill_tc_kernel<64>, ag, dim3(128), attn_tc_smem<64>(), s, m, (const float *)p.qkv, p.o,
+                                 olo, l, one));
             else
-                attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, one);
-            PF_CK(cudaGetLastError());
+                PF_CK(launch_pdl(attn_prefill_tc_kernel<128>, ag, dim3(128), attn_tc_smem<128>(), s, m, (const float *)p.qkv,
+                                 p.o, olo, l, one));
             PF_CK(gemm(p.o_map, p.o_lo_map, &p.maps[2 * (4 * l + 1)], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
-            rmsnorm_launch(p.x, gn + m.dim, p.xn, xlo, m.dim, m.norm_eps, T, s);
+            PF_CK(rmsnorm_launch(p.x, gn + m.dim, p.xn, xlo, m.dim, m.norm_eps, T, s));
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 2)], m.w13, T, GEMM_SWIGLU, nullptr, p.h, p.h + hlo,
                        m.hidden, m.status, s));
             PF_CK(gemm(p.h_map, p.h_lo_map, &p.maps[2 * (4 * l + 3)], m.w2, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
         }
         if (p0 + T == n) {  // logits of the last position (its normalised row goes to xn row 0)
-            rmsnorm_bf16_kernel<<<1, 256, 0, s>>>(p.x + (size_t)(T - 1) * m.dim, m.norms + (size_t)m.n_layers * 2 * m.dim,
-                                                  p.xn, xlo, m.dim, m.norm_eps);
+            PF_CK(launch_pdl(rmsnorm_bf16_kernel, dim3(1), dim3(256), 0, s, (const float *)(p.x + (size_t)(T - 1) * m.dim),
+                             (const float *)(m.norms + (size_t)m.n_layers * 2 * m.dim), p.xn, xlo, m.dim, m.norm_eps));
             float *lg = last_logits ? last_logits : p.logits;
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * m.n_layers)], m.emb, 1, GEMM_STORE_F32, lg, nullptr, nullptr,
                        m.vocab, m.status, s));
-            argmax_kernel<<<1, 1024, 0, s>>>(lg, m.vocab, next_id, m.status);
-            PF_CK(cudaGetLastError());
+            PF_CK(launch_pdl(argmax_kernel, dim3(1), dim3(1024), 0, s, (const float *)lg, m.vocab, next_id, m.status));
         }
     }
 #undef PF_CK
@@ -572,23 +590,23 @@ cudaError_t prefill_run_batch(const Model &m, const PrefillPlan &p, int nseq, co
             tab.row[k] = segs[k].row;
             maxcount = std::max(maxcount, segs[k].count);
         }
-        embed_rows_kernel<<<T, 256, 0, s>>>(m, tokens + r0, p.x, m.status);
-        PF_CK(cudaGetLastError());
+        PF_CK(launch_pdl(embed_rows_kernel, dim3(T), dim3(256), 0, s, m, tokens + r0, p.x, m.status));
         for (int l = 0; l < m.n_layers; l++) {
             const float *gn = m.norms + (size_t)l * 2 * m.dim;
-            rmsnorm_launch(p.x, gn, p.xn, xlo, m.dim, m.norm_eps, T, s);
+            PF_CK(rmsnorm_launch(p.x, gn, p.xn, xlo, m.dim, m.norm_eps, T, s));
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 0)], m.qkv, T, GEMM_STORE_F32, p.qkv, nullptr, nullptr,
                        m.qkv.rows, m.status, s));
-            rope_append_kernel<true><<<(T + rope_rpc(m) - 1) / rope_rpc(m), 32 * rope_rpc(m), (size_t)rope_rpc(m) * m.qkv.rows * 4, s>>>(m, p.qkv, l, tab, T);
+            PF_CK(rope_launch(m, p.qkv, l, tab, T, s));
             dim3 ag((maxcount + 63) / 64, m.n_heads, nsegs);  // every segment in one launch
             if (m.head_dim == 64)
-                attn_prefill_tc_kernel<64><<<ag, 128, attn_tc_smem<64>(), s>>>(m, p.qkv, p.o, olo, l, tab);
+                PF_CK(launch_pdl(attn_prefill_tc_kernel<64>, ag, dim3(128), attn_tc_smem<64>(), s, m, (const float *)p.qkv, p.o,
+                                 olo, l, tab));
             else
-                attn_prefill_tc_kernel<128><<<ag, 128, attn_tc_smem<128>(), s>>>(m, p.qkv, p.o, olo, l, tab);
-            PF_CK(cudaGetLastError());
+                PF_CK(launch_pdl(attn_prefill_tc_kernel<128>, ag, dim3(128), attn_tc_smem<128>(), s, m, (const float *)p.qkv,
+                                 p.o, olo, l, tab));
             PF_CK(gemm(p.o_map, p.o_lo_map, &p.maps[2 * (4 * l + 1)], m.wo, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
                        m.status, s));
-            rmsnorm_launch(p.x, gn + m.dim, p.xn, xlo, m.dim, m.norm_eps, T, s);
+            PF_CK(rmsnorm_launch(p.x, gn + m.dim, p.xn, xlo, m.dim, m.norm_eps, T, s));
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * l + 2)], m.w13, T, GEMM_SWIGLU, nullptr, p.h, p.h + hlo,
                        m.hidden, m.status, s));
             PF_CK(gemm(p.h_map, p.h_lo_map, &p.maps[2 * (4 * l + 3)], m.w2, T, GEMM_ADD_F32, p.x, nullptr, nullptr, m.dim,
@@ -601,17 +619,18 @@ cudaError_t prefill_run_batch(const Model &m, const PrefillPlan &p, int nseq, co
             const Seg &g = segs[j];
             if (g.pos0 + g.count != lens[g.idx]) continue;
             if (first < 0) first = g.idx;
-            rmsnorm_bf16_kernel<<<1, 256, 0, s>>>(p.x + (size_t)(g.row + g.count - 1) * m.dim,
-                                                  m.norms + (size_t)m.n_layers * 2 * m.dim, p.xn + (size_t)k * m.dim, xlo,
-                                                  m.dim, m.norm_eps);
+            PF_CK(launch_pdl(rmsnorm_bf16_kernel, dim3(1), dim3(256), 0, s,
+                             (const float *)(p.x + (size_t)(g.row + g.count - 1) * m.dim),
+                             (const float *)(m.norms + (size_t)m.n_layers * 2 * m.dim), p.xn + (size_t)k * m.dim, xlo,
+                             m.dim, m.norm_eps));
             k++;
         }
         if (k > 0) {
             float *lg = (last_logits ? last_logits : p.logits) + (last_logits ? (size_t)first * m.vocab : 0);
             PF_CK(gemm(p.xn_map, p.xn_lo_map, &p.maps[2 * (4 * m.n_layers)], m.emb, k, GEMM_STORE_F32, lg, nullptr,
                        nullptr, m.vocab, m.status, s));
-            argmax_kernel<<<k, 1024, 0, s>>>(lg, m.vocab, next_ids + first, m.status);  // one CTA per row
-            PF_CK(cudaGetLastError());
+            PF_CK(launch_pdl(argmax_kernel, dim3(k), dim3(1024), 0, s, (const float *)lg, m.vocab, next_ids + first,
+                             m.status));  // one CTA per row
         }
         r0 += T;
     }
