@@ -57,6 +57,41 @@ def test_tensor_prefill_matches_oracle(slm, n):
         assert np.abs(gk - ok).max() <= tol and np.abs(gv - ov).max() <= tol
 
 
+@pytest.mark.parametrize("n_kv_heads", [1, 2])
+def test_tensor_prefill_head_dim_128(slm, n_kv_heads):
+    """head_dim 128: the attention kernel's 2-stage ring and the RoPE / append kernel's two
+    pairs per lane and head; one prompt (two 64-row query blocks and a ragged third) and a
+    batched call with three prompts, against the oracle."""
+    s = SHAPE.replace(dim=256, n_heads=4, n_kv_heads=n_kv_heads, head_dim=128, max_seq=160, max_batch=3)
+    W = synth.make_weights(s, seed=25)
+    o = oracle.Model(s, W)
+    prompt = synth.make_prompt(s, 1, 150)
+    ref_logits, ref_id = o.prefill(0, prompt)
+    eng = slm.Engine(s, W)
+    lg, nid = eng.prefill_checked(0, prompt)
+    check_logits(lg.cpu().numpy(), ref_logits, 2e-2, "hd128 prefill")
+    check_id(int(nid.item()), ref_logits, ref_id, "hd128 prefill")
+    gk, gv = eng.kv(s.n_layers - 1, 0)
+    ok, ov = o.kv(s.n_layers - 1, 0)
+    assert np.abs(gk - ok).max() <= 2e-2 * max(1.0, float(np.abs(ok).max()))
+    assert np.abs(gv - ov).max() <= 2e-2 * max(1.0, float(np.abs(ov).max()))
+    lens = [17, 64, 99]
+    prompts = [synth.make_prompt(s, 4 + i, n) for i, n in enumerate(lens)]
+    b = slm.Engine(s, W)
+    dev = torch.device("cuda")
+    toks = torch.as_tensor(np.concatenate(prompts).astype(np.int32)).to(dev)
+    blg = torch.zeros((3, s.vocab), dtype=torch.float32, device=dev)
+    ids = torch.zeros(3, dtype=torch.int32, device=dev)
+    assert b.prefill_batch([0, 1, 2], toks, lens, blg, ids) == 0, b.last_error()
+    assert b.sync() == 0, b.last_error()
+    for i, p in enumerate(prompts):
+        ref, rid = oracle.Model(s, W).prefill(0, p)
+        check_logits(blg[i].cpu().numpy(), ref, 2e-2, f"hd128 batched prefill seq {i}")
+        check_id(int(ids[i].item()), ref, rid, f"hd128 batched prefill seq {i}")
+    eng.close()
+    b.close()
+
+
 def test_tensor_prefill_equals_token_by_token_prefill_closely(slm):
     # The same prompt through the tensor-core path (>= 16 tokens) and, token by token,
     # through the decode kernel (15 tokens then 1 decode step per further token).
