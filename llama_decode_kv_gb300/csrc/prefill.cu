@@ -18,7 +18,9 @@
 // and finally the logits of each sequence's last position (GEMM with the tied
 // embedding) and its argmax.  The block equations are those of the decode step
 // (kasahare 0.4.0 / simple-llm, "Architecture"); weights enter as stored (bf16), the
-// residual stream and every accumulation are fp32.
+// residual stream and every accumulation are fp32.  Every kernel of this chain is
+// launched with programmatic dependent launch (launch_pdl) and waits for its predecessor
+// (pdl_wait) before it reads anything, so launches overlap the previous kernel's tail.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
