@@ -207,6 +207,34 @@ def test_api_errors_on_device(slm):
     assert eng.sync() == slm.SLM_OK
 
 
+@pytest.mark.parametrize("batch", [1, 2])
+def test_decode_into_the_last_cache_slot(slm, batch):
+    """Prompts that leave a few free positions (tensor-core prefill, bf16 weights and
+    cache), then decode steps up to the last slot, max_seq - 1, against the oracle (one
+    row: the cluster kernel; two rows: the persistent kernel); one more step is refused
+    with SLM_ECAPACITY and changes nothing."""
+    s = synth.TINY.replace(max_batch=batch, max_seq=64, weight_dtype=synth.DTYPE_BF16, kv_dtype=synth.DTYPE_BF16,
+                           dim=256, n_heads=4, n_kv_heads=1, head_dim=64)
+    W = synth.make_weights(s, seed=71)
+    lens = [60, 57][:batch]
+    prompts = [synth.make_prompt(s, r, lens[r]) for r in range(batch)]
+    steps = 4  # row 0 decodes positions 60..63
+    rows = list(range(batch))
+    ref_ids, ref_logits = oracle_reference(s, prompts, steps, rows, seed=71)
+    eng = _engine(slm, s, W)
+    if batch == 1:
+        assert eng.cluster_plan() is not None
+    g_logits, g_ids = gpu_teacher_forced(eng, s, prompts, ref_ids, steps, batch, rows)
+    compare_runs(s, ref_ids, ref_logits, g_logits, g_ids, rows, f"last slot, batch {batch}")
+    assert eng.seq_len(0) == s.max_seq
+    tok = torch.tensor([1], dtype=torch.int32, device="cuda")
+    ids = torch.empty(1, dtype=torch.int32, device="cuda")
+    assert eng.decode_step([0], tok, [s.max_seq], None, ids) == slm.SLM_ECAPACITY
+    assert eng.seq_len(0) == s.max_seq
+    assert eng.sync() == 0, eng.last_error()
+    eng.close()
+
+
 def test_host_buffers_give_the_same_results(slm):
     s = synth.TINY.replace(max_batch=2)
     W = synth.make_weights(s, seed=3)

@@ -170,6 +170,53 @@ def test_paged_fork_shares_pages_and_copies_on_write(slm):
         check_logits(res[st][2], np.asarray(lo)[0], tolerance(s), f"clone row 2 step {st}")
 
 
+def test_paged_fork_at_a_page_boundary(slm):
+    """A source that ends exactly at a page boundary (32 positions, pages of 16): the
+    clones share both full pages and there is no partial page to copy, so every row's first
+    step takes a fresh page and nothing is copied; the rows then decode exactly as on a
+    contiguous cache, and a clone matches the oracle."""
+    s = synth.TINY.replace(max_batch=3, max_seq=96, kv_dtype=synth.DTYPE_BF16, dim=256, n_heads=4, n_kv_heads=1,
+                           head_dim=64)
+    W = synth.make_weights(s, seed=73)
+    prompt = synth.make_prompt(s, 0, 32)
+    dev = torch.device("cuda")
+    outs = {}
+    for page in (0, 16):
+        eng = slm.Engine(s, W, kv_page_size=page)
+        _, nid = eng.prefill_checked(0, prompt, want_logits=False)
+        free0 = eng.pages_free()
+        assert eng.fork(0, [1, 2]) == 0, eng.last_error()
+        if page:
+            assert eng.pages_free() == free0
+            t0 = eng.page_table(0)
+            assert all(np.array_equal(eng.page_table(r)[:2], t0[:2]) for r in (1, 2))
+        toks = [(int(nid.item()) + 5 * r) % s.vocab for r in range(3)]
+        res, fed = [], []
+        for st in range(18):  # crosses into the fourth page at position 48
+            fed.append(list(toks))
+            lg, ids = eng.decode_checked([0, 1, 2], torch.tensor(toks, dtype=torch.int32, device=dev), [32 + st] * 3,
+                                         want_logits=True)
+            res.append(lg.cpu().numpy())
+            toks = [int(x) for x in ids.cpu().numpy()]
+            if page and st == 0:
+                assert eng.pages_free() == free0 - 3  # one fresh page per row, no copies
+                t = [eng.page_table(r) for r in range(3)]
+                assert len({int(x[2]) for x in t}) == 3
+        assert eng.sync() == 0, eng.last_error()
+        outs[page] = (res, fed)
+        eng.close()
+    assert outs[0][1] == outs[16][1]
+    for st, (a, b) in enumerate(zip(outs[0][0], outs[16][0])):
+        assert np.array_equal(a, b), f"step {st}: forked rows differ between the cache layouts"
+    import oracle
+    o = oracle.Model(s.replace(max_batch=1), W)
+    o.prefill(0, prompt)
+    res, fed = outs[16]
+    for st in range(len(res)):
+        lo, _ = o.decode_step([0], [fed[st][1]], [32 + st])
+        check_logits(res[st][1], np.asarray(lo)[0], tolerance(s), f"clone row 1 step {st}")
+
+
 def test_paged_pool_exhaustion(slm):
     """A pool too small for every row: the step that needs a page no one has returns
     SLM_ECAPACITY and changes nothing; after a reset frees pages the same step runs,

@@ -147,6 +147,39 @@ def test_batched_prefill_equals_one_prefill_per_sequence(slm):
     b.close()
 
 
+def test_batched_prefill_with_short_prompts(slm):
+    """A batch holding prompts below the tensor-core minimum (1 and 15 tokens) beside
+    longer ones (16, 70) takes the one-sequence-at-a-time path (token by token for the
+    short prompts); every sequence's logits and id against the oracle, and a decode step
+    on top of all four."""
+    s = SHAPE.replace(max_seq=96, max_batch=4)
+    W = synth.make_weights(s, seed=33)
+    lens = [1, 15, 16, 70]
+    prompts = [synth.make_prompt(s, 7 + i, n) for i, n in enumerate(lens)]
+    dev = torch.device("cuda")
+    eng = slm.Engine(s, W)
+    toks = torch.as_tensor(np.concatenate(prompts).astype(np.int32)).to(dev)
+    lg = torch.zeros((4, s.vocab), dtype=torch.float32, device=dev)
+    ids = torch.zeros(4, dtype=torch.int32, device=dev)
+    assert eng.prefill_batch([0, 1, 2, 3], toks, lens, lg, ids) == 0, eng.last_error()
+    assert eng.sync() == 0, eng.last_error()
+    m = oracle.Model(s, W)
+    refs = []
+    for i, p in enumerate(prompts):
+        ref, rid = m.prefill(i, p)
+        check_logits(lg[i].cpu().numpy(), ref, 2e-2, f"short-prompt batch seq {i}")
+        check_id(int(ids[i].item()), ref, rid, f"short-prompt batch seq {i}")
+        assert eng.seq_len(i) == lens[i]
+        refs.append(rid)
+    rl, rid = m.decode_step([0, 1, 2, 3], refs, lens)
+    gl, gid = eng.decode_checked([0, 1, 2, 3], torch.tensor(refs, dtype=torch.int32, device=dev), lens)
+    for i in range(4):
+        check_logits(gl[i].cpu().numpy(), rl[i], 2e-2, f"decode after short-prompt batch, seq {i}")
+        check_id(int(gid[i].item()), rl[i], int(rid[i]), f"decode after short-prompt batch, seq {i}")
+    assert eng.sync() == 0
+    eng.close()
+
+
 def test_batched_prefill_refuses_bad_arguments(slm):
     s = SHAPE.replace(max_seq=64, max_batch=3)
     eng = slm.Engine(s, synth.make_weights(s, seed=3))
