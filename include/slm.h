@@ -24,7 +24,10 @@
  *     "host" pointers are ordinary host memory.  Where a parameter says "host or
  *     device", the library checks the pointer's kind itself.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
- *     Work is enqueued asynchronously on it unless the call says otherwise.
+ *     Work is enqueued asynchronously on it unless the call says otherwise.  Stream
+ *     order holds as usual: the prefill's kernels are launched with programmatic
+ *     dependent launch among themselves, and each waits for the work before it on the
+ *     stream to complete before it reads or writes any memory.
  *   - A context is not thread-safe: calls on one context must not overlap.
  *   - Every device-side wait in the library's kernels is bounded in time; a wait that
  *     runs out sets the context's device status word, which slm_sync() reports as
